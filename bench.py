@@ -1,0 +1,320 @@
+#!/usr/bin/env python
+"""Batch-1 greedy decode throughput of the Qwen3-0.6B-shape Q8_0 workload
+(511-token prompt prefilled, then greedy decode steps at positions 511..638)
+on GB300, against the HBM roofline, with the oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tqd|reference]
+
+A step is one decode token: embed, 28 layers, final norm, lm_head, argmax.
+Timed tokens run as device-chained windows of up to 128 tokens starting at
+position 511 (the sequence is truncated back to the prompt between windows,
+outside the timed region).  Inputs are resident in HBM; every token streams
+~766 MB of weights and KV, more than the 129 MB L2, so no L2 flush is needed.
+Multi-GPU runs are independent replicas (one model per GPU, no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "batch-1 decode tokens/sec (Qwen3-0.6B-shape Q8_0) and % of HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "qwen3_0.6b"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4096, help="timed decode tokens")
+    p.add_argument("--warmup", type=int, default=256, help="untimed decode tokens first")
+    p.add_argument("--impl", choices=["tqd", "reference"], default="tqd")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    p.add_argument("--schedule", choices=["persistent", "graph"], default="persistent")
+    p.add_argument("--e2e-steps", type=int, default=128)
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, r in rows:
+            for n, v in zip(names, r[1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [r[0] for r in rows] if rows else []
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ oracle baseline
+
+def oracle_sample(wl, seconds: float, max_steps: int | None = None):
+    """Oracle decode steps at the workload's shape after a seeded stand-in KV
+    history of prompt_len rows (no oracle prefill); returns (tok/s, steps,
+    threads, seconds)."""
+    import oracle
+    cfg = wl.model
+    model = synth.make_model(cfg, wl.model_seed)
+    k, v = synth.kv_fill(cfg, 7, 0, wl.prompt_len, -1.0, 1.0)
+    om = oracle.OracleModel(model, wl.prompt_len + wl.decode_steps)
+    om.kv_load(k, v)
+    del k, v
+    tok, pos, n = int(synth.prompt(wl)[-1]), wl.prompt_len, 0
+    t0 = time.perf_counter()
+    while True:
+        tok, _ = om.step(tok, pos)
+        pos += 1
+        n += 1
+        el = time.perf_counter() - t0
+        if (max_steps is not None and n >= max_steps) or (max_steps is None and el >= seconds) \
+                or pos >= wl.prompt_len + wl.decode_steps:
+            break
+    return n / el, n, oracle.max_threads(), el
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value: float) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, value: float) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return None
+    # warm-up steps, then K timed oracle steps on the host cores
+    if args.warmup:
+        oracle_sample(wl, 0, max_steps=min(args.warmup, 3))
+    k = max(1, min(args.steps, wl.decode_steps))
+    tps, n, cores, el = oracle_sample(wl, 0, max_steps=k)
+    sample = (f"{n} oracle decode steps at positions {wl.prompt_len}..{wl.prompt_len + n - 1} after a "
+              f"seeded stand-in KV history of {wl.prompt_len} rows (no oracle prefill)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": 1000.0 * el / n, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "prompt_len": wl.prompt_len, "batch": wl.batch},
+        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_tqd(args, wl, world, rank, local, pg):
+    import torch
+    import token_quantized_decode_gb300 as tqd
+
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    cfg = wl.model
+    model = synth.make_model(cfg, wl.model_seed)
+    ids = synth.prompt(wl)
+    P, D = wl.prompt_len, wl.decode_steps
+    schedule = tqd.TQD_SCHED_PERSISTENT if args.schedule == "persistent" else tqd.TQD_SCHED_GRAPH
+    dec = tqd.Decoder(model, P + D, 1, schedule, stream=stream)
+    del model
+    first = dec.prefill(ids)
+
+    def windows(n_tokens):
+        out, left = [], n_tokens
+        while left > 0:
+            out.append(min(left, D))
+            left -= out[-1]
+        return out
+
+    # warm-up
+    for n in windows(args.warmup):
+        dec.truncate(P)
+        dec.generate(first, n)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev = []
+    barrier(pg)
+    torch.cuda.synchronize()
+    total_bytes = 0
+    launches = 0
+    for n in windows(args.steps):
+        dec.truncate(P)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        dec.generate(first, n)
+        e.record(stream)
+        ev.append((s, e, n))
+        total_bytes += sum(dec.step_bytes(p) for p in range(P, P + n))
+        launches += 1 if schedule == tqd.TQD_SCHED_PERSISTENT else n * dec.phase_count
+    torch.cuda.synchronize()
+    barrier(pg)
+    clocks = sampler.stop()
+    t_ms = sum(s.elapsed_time(e) for s, e, _ in ev)
+    tokens = sum(n for _, _, n in ev)
+    t_max = max_over_ranks(pg, t_ms)
+    all_tokens = sum_over_ranks(pg, tokens)
+    value = all_tokens / (t_max / 1000.0)
+    per_launch_bytes = total_bytes / len(ev)
+    per_launch_ms = t_ms / len(ev)
+
+    # end to end through the C ABI: one tqd_decode_step per token, host token
+    # in, host token out, the host round trip inside the timed region
+    dec.truncate(P)
+    torch.cuda.synchronize()
+    tok, pos = first, P
+    n_e2e = min(args.e2e_steps, D)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        tok = dec.decode_step(tok, pos)
+        pos += 1
+    e2e_s = time.perf_counter() - t0
+    e2e_val = sum_over_ranks(pg, n_e2e) / max_over_ranks(pg, e2e_s)
+
+    hbm, kind = peaks()
+    achieved = per_launch_bytes / (per_launch_ms / 1000.0) / 1e9
+    mean_step_bytes = total_bytes / tokens
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": tokens,
+        "warmup": args.warmup, "ms_per_step": t_max / tokens, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "prompt_len": P, "decode_positions": f"{P}..{P + D - 1}",
+                   "batch": wl.batch, "schedule": args.schedule, "weights": "Q8_0 (34-byte blocks), resident",
+                   "l2": "inputs larger than L2: each token streams %.0f MB vs 129 MB L2" % (mean_step_bytes / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "k_persistent<Q8_0>" if schedule == tqd.TQD_SCHED_PERSISTENT else "whole step",
+                     "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
+                     "peak_kind": f"{kind} copy bandwidth"},
+        "step_roofline_frac": (mean_step_bytes / (hbm * 1e9)) / (t_max / tokens / 1000.0),
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4 + 16,
+                "api": "tqd_decode_step per token (host token in, host token out)"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    dec.close()
+    return line
+
+
+def main():
+    args = parse()
+    wl = synth.WORKLOADS[args.workload]
+    world, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, wl, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line = run_tqd(args, wl, world, rank, local, pg)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            tps, n, cores, el = oracle_sample(wl, args.cpu_seconds)
+            line["cpu_baseline"] = {
+                "value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": (f"{n} oracle decode steps ({el:.1f} s) at positions {wl.prompt_len}.. after a seeded "
+                           f"stand-in KV history of {wl.prompt_len} rows")}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

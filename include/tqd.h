@@ -1,0 +1,258 @@
+/*
+ * tqd.h — C ABI of libtqd, a GPU-resident greedy decoder for Qwen3-shaped
+ * models with Q8_0 (or bf16) weights, built for sm_103a (GB300).
+ *
+ * What the library computes is the per-token decode step described by the
+ * inferno.rs blog, "IV.4: One command buffer per token": embed the input
+ * token, run every layer (RMSNorm, Q/K/V projections, per-head QK-norm, RoPE,
+ * append to the KV cache, GQA attention, output projection + residual,
+ * RMSNorm, gate/up projections, SwiGLU, down projection + residual), then the
+ * final norm, the lm_head projection and the argmax, with weights and KV
+ * cache resident on the GPU and only the next token id read back
+ * (sections "Eight kernels" and "One command buffer").  The bf16 variant is
+ * the Llama-style step without QK-norm of "Adding Metal to my Rust LLM engine",
+ * section "What the kernels do".
+ *
+ * Conventions for every call:
+ *  - Every function except tqd_destroy and tqd_status_name returns an
+ *    int32_t status (TQD_OK = 0).  Arguments are validated before any GPU
+ *    work; a refused call changes nothing.
+ *  - Host pointers are owned by the caller and are never retained past the
+ *    call.  All device memory is owned by the library (one arena per model,
+ *    allocated by tqd_create, freed by tqd_destroy).  Functions named
+ *    tqd_op_* take DEVICE pointers owned by the caller instead.
+ *  - `stream` arguments are cudaStream_t values passed as void* (NULL = the
+ *    legacy default stream).  A model runs all its work on the stream given
+ *    to tqd_create.
+ *  - After TQD_ERR_CUDA or TQD_ERR_DEVICE_TIMEOUT a model is poisoned: every
+ *    later call but tqd_destroy returns TQD_ERR_POISONED.
+ *  - A model is not thread-safe: calls on one model must not overlap.
+ */
+#ifndef TQD_H
+#define TQD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tqd_status {
+  TQD_OK = 0,
+  TQD_ERR_BAD_ARG = 1,             /* NULL pointer, out-of-range id, bad size */
+  TQD_ERR_UNSUPPORTED_CONFIG = 2,  /* config this build cannot run; see tqd_last_error() */
+  TQD_ERR_NO_DEVICE = 3,           /* no CUDA device, or not an sm_103 device */
+  TQD_ERR_CUDA = 4,                /* a CUDA runtime call failed (model poisoned) */
+  TQD_ERR_OOM = 5,                 /* device allocation failed (nothing leaked) */
+  TQD_ERR_CAPACITY = 6,            /* position would exceed max_seq */
+  TQD_ERR_POS_MISMATCH = 7,        /* pos is not the sequence's next position */
+  TQD_ERR_DEVICE_TIMEOUT = 8,      /* a bounded device-side wait gave up (model poisoned) */
+  TQD_ERR_NUMERIC = 9,             /* every logit was NaN: no argmax exists */
+  TQD_ERR_POISONED = 10            /* an earlier fatal error; only tqd_destroy is valid */
+} tqd_status;
+
+enum { TQD_WEIGHT_Q8_0 = 0, TQD_WEIGHT_BF16 = 1 };
+
+/* Execution schedule of one decode step (both compute the same thing):
+ *  TQD_SCHED_GRAPH       one CUDA graph per token, one kernel per fused phase
+ *  TQD_SCHED_PERSISTENT  one cooperative persistent kernel per token (or per
+ *                        tqd_generate call), phases separated by bounded grid
+ *                        barriers. */
+enum { TQD_SCHED_GRAPH = 0, TQD_SCHED_PERSISTENT = 1 };
+
+/* Model hyper-parameters ("One command buffer per token", section "The seam":
+ * the plan's hidden, heads, kv heads, head_dim, intermediate, vocab, rms_eps,
+ * rope_theta), plus this library's capacity fields. */
+typedef struct tqd_config {
+  int32_t n_layers;
+  int32_t hidden;        /* H; Q8_0 needs H % 32 == 0, bf16 needs H % 8 == 0 */
+  int32_t n_heads;       /* query heads */
+  int32_t n_kv_heads;    /* key/value heads; n_heads % n_kv_heads == 0 */
+  int32_t head_dim;      /* 64 or 128 */
+  int32_t intermediate;  /* SwiGLU width I */
+  int32_t vocab;         /* V; the lm_head has V rows */
+  int32_t qk_norm;       /* 1: per-head RMSNorm of q and k before RoPE (Qwen3) */
+  int32_t weight_type;   /* TQD_WEIGHT_Q8_0 or TQD_WEIGHT_BF16 */
+  float rope_theta;
+  float rms_eps;
+  int32_t max_seq;       /* KV rows per sequence (positions 0 .. max_seq-1) */
+  int32_t max_batch;     /* sequences held by the model (each its own KV) */
+  int32_t schedule;      /* TQD_SCHED_* */
+} tqd_config;
+
+/* One layer's weights on the host.  Matrices are row-major [rows x cols]:
+ *  Q8_0: rows * cols/32 blocks of 34 bytes (f16 scale little-endian, then 32
+ *        int8 quants), row after row — the block of "Eight kernels";
+ *  bf16: rows * cols uint16 bit patterns.
+ * Shapes: wq [n_heads*head_dim x H], wk, wv [n_kv_heads*head_dim x H],
+ * wo [H x n_heads*head_dim], w_gate, w_up [I x H], w_down [H x I].
+ * Norm gains are f32: attn_norm, ffn_norm [H]; q_norm, k_norm [head_dim]
+ * (ignored, may be NULL, when qk_norm == 0). */
+typedef struct tqd_layer_weights {
+  const float* attn_norm;
+  const void* wq;
+  const void* wk;
+  const void* wv;
+  const void* wo;
+  const float* q_norm;
+  const float* k_norm;
+  const float* ffn_norm;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+} tqd_layer_weights;
+
+typedef struct tqd_host_weights {
+  const tqd_layer_weights* layers; /* [n_layers] */
+  const float* out_norm;           /* [H] */
+  const void* lm_head;             /* [V x H], same format as the layers */
+  const void* embed;               /* [V x H] token embedding; NULL = tied to lm_head */
+} tqd_host_weights;
+
+typedef struct tqd_model tqd_model;
+
+/* Name of a status code ("TQD_OK", ...); "TQD_UNKNOWN_STATUS" for others.
+ * Needs no device.  ("Metal LLM decode", section "Status codes and the
+ * dispatch budget": a status-name call that works on any host.) */
+const char* tqd_status_name(int32_t status);
+
+/* Human-readable detail of the last refusal on this thread (e.g. every
+ * mismatched config field); "" when none.  Valid until the next call. */
+const char* tqd_last_error(void);
+
+/* Validate cfg, allocate the device arena (weights, KV cache for max_batch
+ * sequences, activations, RoPE cos/sin table), upload and repack the weights
+ * once, and prepare the per-token schedule.  On success *out owns the model.
+ * Errors: BAD_ARG, UNSUPPORTED_CONFIG (nothing touched the GPU), NO_DEVICE,
+ * OOM, CUDA.  ("One command buffer per token", GpuDecoder::try_new in
+ * section "Resident state": upload once, allocate scratch once.) */
+int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* weights, void* stream,
+                   tqd_model** out);
+
+/* Free everything the model owns.  NULL-safe.  Synchronises the model's stream. */
+void tqd_destroy(tqd_model* model);
+
+/* Forget sequence `seq`'s history: its next position becomes 0. */
+int32_t tqd_reset(tqd_model* model, int32_t seq);
+
+/* Drop positions n_pos .. next_pos-1 of sequence seq (0 <= n_pos <=
+ * next_pos): the KV rows of positions below n_pos are kept, so decoding can
+ * resume from a prefilled prompt without prefilling it again.
+ * Errors: BAD_ARG. */
+int32_t tqd_truncate(tqd_model* model, int32_t seq, int32_t n_pos);
+
+/* The sequence's next position (number of filled KV rows). */
+int32_t tqd_next_pos(tqd_model* model, int32_t seq, int32_t* pos_out);
+
+/* Run the prompt ids[0..n-1] through the decoder on the GPU at positions
+ * next_pos .. next_pos+n-1 (the decode step repeated, which is the same
+ * computation as causal attention over the prompt), then write the greedy
+ * next token to *next_out.  Errors: BAD_ARG (n <= 0, id out of range),
+ * CAPACITY. */
+int32_t tqd_prefill(tqd_model* model, int32_t seq, const int32_t* ids, int32_t n,
+                    int32_t* next_out);
+
+/* Replace sequence seq's KV cache with n_pos host rows: k, v are f32
+ * [n_layers][n_pos][n_kv_heads*head_dim] holding post-RoPE keys and values
+ * ("One command buffer per token", section "The cache comes over once").
+ * Sets next_pos = n_pos.  Errors: BAD_ARG, CAPACITY. */
+int32_t tqd_kv_upload(tqd_model* model, int32_t seq, int32_t n_pos, const float* k,
+                      const float* v);
+
+/* One greedy decode step: feed `token` at position `pos`, which must equal
+ * the sequence's next position, append its K/V row, and write the argmax of
+ * the logits (ties to the lowest index, NaN never wins) to *next_out.  Four
+ * bytes cross back to the host.  Errors: BAD_ARG, POS_MISMATCH, CAPACITY,
+ * NUMERIC (all logits NaN).  ("One command buffer per token", section "One
+ * command buffer": decode_step.) */
+int32_t tqd_decode_step(tqd_model* model, int32_t seq, int32_t token, int32_t pos,
+                        int32_t* next_out);
+
+/* n_steps chained greedy steps: the first feeds first_token at next_pos, each
+ * later one feeds the previous argmax, entirely on the device (no host
+ * round trip between steps).  ids_out[i] receives the i-th generated id.
+ * Errors: as tqd_decode_step. */
+int32_t tqd_generate(tqd_model* model, int32_t seq, int32_t first_token, int32_t n_steps,
+                     int32_t* ids_out);
+
+/* Copy the logits of sequence seq's last step (f32 [vocab]) to host_out.
+ * A debugging and parity hook, off the decode path ("One command buffer per
+ * token", read_logits). */
+int32_t tqd_read_logits(tqd_model* model, int32_t seq, float* host_out);
+
+/* Number of device phases one decode step runs (kernel launches for
+ * TQD_SCHED_GRAPH, grid-barrier-separated phases for TQD_SCHED_PERSISTENT) —
+ * the analogue of the per-token dispatch budget of "Metal LLM decode". */
+int32_t tqd_phase_count(tqd_model* model, int32_t* out);
+
+/* Algorithmic HBM bytes of one decode step at position pos (weights read
+ * once, pos+1 KV rows read per layer, one KV row written per layer). */
+int32_t tqd_step_bytes(tqd_model* model, int32_t pos, int64_t* bytes_out);
+
+/* ------------------------------------------------------------------------
+ * Operator entry points (device pointers, caller-owned, on `stream`).
+ * They run the same device code as the decode step, one phase at a time, so
+ * each can be checked on its own ("The correctness ladder", rung one).
+ * All return BAD_ARG for NULL pointers or unsupported sizes, CUDA on a launch
+ * failure; they allocate nothing.
+ * ------------------------------------------------------------------------ */
+
+/* Repack a Q8_0 matrix from 34-byte blocks (rows x cols/32 blocks) into the
+ * library's row layout: per row, cols int8 quants then cols/32 f16 scales,
+ * padded to a multiple of 16 bytes (cols * 17/16 bytes when cols % 256 == 0;
+ * cols % 32 == 0). */
+int32_t tqd_op_q8_0_repack(const uint8_t* w_blocks, int64_t rows, int64_t cols, uint8_t* w_rows,
+                           void* stream);
+
+/* y[r] = sum_b scale_rb * sum_j quant_rbj * x[32b+j] over a repacked Q8_0
+ * matrix ("Eight kernels", q8_matvec).  x f32 [cols], y f32 [rows]. */
+int32_t tqd_op_q8_0_matvec(const uint8_t* w_rows, int64_t rows, int64_t cols, const float* x,
+                           float* y, void* stream);
+
+/* y = W x for a bf16 matrix [rows x cols] (cols % 8 == 0). */
+int32_t tqd_op_bf16_matvec(const uint16_t* w, int64_t rows, int64_t cols, const float* x,
+                           float* y, void* stream);
+
+/* out[r] = x[r] * (mean(x[r]^2) + eps)^(-1/2) * g for `rows` rows of n
+ * ("Eight kernels", rms_norm_row).  n <= 16384. */
+int32_t tqd_op_rmsnorm(const float* x, const float* g, int32_t rows, int32_t n, float eps,
+                       float* out, void* stream);
+
+/* Fill table [max_pos][head_dim/2] of (cos a, sin a) f32 pairs with
+ * a = p * theta^(-i/(head_dim/2)), computed in f64 on the device. */
+int32_t tqd_op_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* table,
+                          void* stream);
+
+/* Half-split RoPE in place on n_heads heads of x at position pos, using a
+ * table from tqd_op_rope_table ("Eight kernels", rope_row). */
+int32_t tqd_op_rope(float* x, int32_t n_heads, int32_t head_dim, int32_t pos, const float* table,
+                    void* stream);
+
+/* Split-K decode attention ("Eight kernels", attention_decode, restated as a
+ * flash-decode over n_chunks key ranges with a log-sum-exp combine):
+ * q f32 [n_heads*hd], K, V f32 [S][n_kv*hd], out f32 [n_heads*hd].
+ * `scratch` is caller-owned device memory of
+ * tqd_attention_scratch_bytes(n_heads, n_kv, hd, n_chunks) bytes; the call
+ * leaves it ready for reuse.  hd must be 64 or 128; 1 <= n_chunks <= 1024. */
+int32_t tqd_op_attention(const float* q, const float* K, const float* V, int32_t S,
+                         int32_t n_heads, int32_t n_kv, int32_t head_dim, int32_t n_chunks,
+                         float* out, void* scratch, void* stream);
+size_t tqd_attention_scratch_bytes(int32_t n_heads, int32_t n_kv, int32_t head_dim,
+                                   int32_t n_chunks);
+
+/* out = silu(g) * u elementwise, silu(z) = z / (1 + e^-z)
+ * ("Eight kernels", silu_hadamard). */
+int32_t tqd_op_silu_mul(const float* g, const float* u, int64_t n, float* out, void* stream);
+
+/* *idx_out = index of the largest x (ties -> lowest index, NaN never wins,
+ * -1 when all NaN) ("Eight kernels", argmax_row).  scratch: caller-owned
+ * device memory of tqd_argmax_scratch_bytes() bytes. */
+int32_t tqd_op_argmax(const float* x, int64_t n, int32_t* idx_out, void* scratch, void* stream);
+size_t tqd_argmax_scratch_bytes(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQD_H */

@@ -1,0 +1,96 @@
+"""The C ABI without a GPU: the library builds, loads, exports every
+function include/tqd.h declares, names its statuses, and refuses bad
+configurations before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+import token_quantized_decode_gb300 as tqd
+from token_quantized_decode_gb300 import _lib
+from token_quantized_decode_gb300 import build as tqd_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tqd.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    tqd_build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+char\s*\*|int32_t|void|size_t)\s+(tqd_\w+)\s*\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in tqd.h but not exported"
+    assert set(names) == set(_lib.exported_symbols())
+
+
+def test_status_names_need_no_device(L):
+    for i, n in enumerate(_lib.STATUS_NAMES):
+        assert tqd.tqd_status_name(i) == n
+    assert tqd.tqd_status_name(-1) == "TQD_UNKNOWN_STATUS"
+    assert tqd.tqd_status_name(1000) == "TQD_UNKNOWN_STATUS"
+
+
+def test_config_struct_layout_matches_header(L):
+    # 11 int32 / float fields before max_seq, then max_seq, max_batch, schedule
+    assert ctypes.sizeof(_lib.tqd_config) == 14 * 4
+    assert ctypes.sizeof(_lib.tqd_layer_weights) == 11 * ctypes.sizeof(ctypes.c_void_p)
+    assert ctypes.sizeof(_lib.tqd_host_weights) == 4 * ctypes.sizeof(ctypes.c_void_p)
+
+
+def test_bad_configs_are_refused_before_any_device_work(L):
+    m = synth.make_model(synth.TINY, 0)
+    w = tqd.make_host_weights(m)
+    bad = [("head_dim", 96), ("n_kv_heads", 3), ("max_seq", 0), ("max_batch", 0), ("schedule", 7),
+           ("hidden", 250), ("weight_type", 5)]
+    for field, val in bad:
+        c = tqd.make_config(synth.TINY, 16)
+        setattr(c, field, val)
+        with pytest.raises(tqd.TQDError) as ei:
+            tqd.tqd_create(c, w)
+        assert ei.value.name == "TQD_ERR_UNSUPPORTED_CONFIG", (field, ei.value)
+    # every mismatched field is named in one refusal
+    c = tqd.make_config(synth.TINY, 16)
+    c.head_dim = 96
+    c.max_seq = 0
+    with pytest.raises(tqd.TQDError) as ei:
+        tqd.tqd_create(c, w)
+    msg = str(ei.value)
+    assert "head_dim" in msg and "max_seq" in msg
+
+
+def test_null_arguments_are_refused(L):
+    assert L.tqd_create(None, None, None, None) == _lib.TQD_ERR_BAD_ARG
+    assert L.tqd_decode_step(None, 0, 0, 0, None) == _lib.TQD_ERR_BAD_ARG
+    assert L.tqd_generate(None, 0, 0, 1, None) == _lib.TQD_ERR_BAD_ARG
+    assert L.tqd_phase_count(None, None) == _lib.TQD_ERR_BAD_ARG
+    assert L.tqd_op_argmax(None, 0, None, None, None) == _lib.TQD_ERR_BAD_ARG
+    assert L.tqd_op_q8_0_matvec(None, 4, 96, None, None, None) == _lib.TQD_ERR_BAD_ARG
+    L.tqd_destroy(None)  # NULL-safe
+
+
+def test_no_device_is_a_status_not_a_crash(L):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    m = synth.make_model(synth.TINY, 0)
+    with pytest.raises(tqd.TQDError) as ei:
+        tqd.Decoder(m, 16)
+    assert ei.value.name == "TQD_ERR_NO_DEVICE"
+
+
+def test_scratch_size_queries(L):
+    assert L.tqd_attention_scratch_bytes(16, 8, 128, 19) == 4 * (16 * 19 * 128 + 16 * 19 * 2 + 8)
+    assert L.tqd_attention_scratch_bytes(0, 8, 128, 19) == 0
+    assert L.tqd_argmax_scratch_bytes() > 0

@@ -1,0 +1,214 @@
+"""Python binding of libtqd, the GB300 (sm_103a) greedy decoder for
+Qwen3-shaped models with Q8_0 or bf16 weights.
+
+Every function here marshals arguments into one call of the C ABI of the
+same name (include/tqd.h); all computation runs in the library's CUDA
+kernels.  PyTorch is used only to hand device memory (tensor data pointers)
+and streams to the operator entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from ._lib import (TQD_SCHED_GRAPH, TQD_SCHED_PERSISTENT, TQD_WEIGHT_BF16, TQD_WEIGHT_Q8_0, TQDError,
+                   check, lib, tqd_config, tqd_host_weights, tqd_layer_weights)
+
+__all__ = [
+    "TQDError", "TQD_SCHED_GRAPH", "TQD_SCHED_PERSISTENT", "TQD_WEIGHT_Q8_0", "TQD_WEIGHT_BF16",
+    "make_config", "make_host_weights", "tqd_status_name", "tqd_create", "tqd_destroy", "tqd_reset",
+    "tqd_truncate", "tqd_next_pos", "tqd_prefill", "tqd_kv_upload", "tqd_decode_step", "tqd_generate",
+    "tqd_read_logits", "tqd_phase_count", "tqd_step_bytes", "Decoder",
+]
+
+_LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "q_norm", "k_norm", "ffn_norm", "w_gate", "w_up",
+                 "w_down")
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("arrays passed to libtqd must be C-contiguous")
+        return a.ctypes.data
+    return int(a.data_ptr())  # torch tensor
+
+
+def _stream(stream):
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def make_config(model_cfg, max_seq: int, max_batch: int = 1, schedule: int = TQD_SCHED_GRAPH) -> tqd_config:
+    """tqd_config from an object with the model's hyper-parameter fields
+    (n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab,
+    qk_norm, weight_type 'q8_0' | 'bf16', rope_theta, rms_eps)."""
+    c = tqd_config()
+    for f in ("n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "intermediate", "vocab"):
+        setattr(c, f, int(getattr(model_cfg, f)))
+    c.qk_norm = int(bool(model_cfg.qk_norm))
+    c.weight_type = {"q8_0": TQD_WEIGHT_Q8_0, "bf16": TQD_WEIGHT_BF16}[model_cfg.weight_type]
+    c.rope_theta = float(model_cfg.rope_theta)
+    c.rms_eps = float(model_cfg.rms_eps)
+    c.max_seq = int(max_seq)
+    c.max_batch = int(max_batch)
+    c.schedule = int(schedule)
+    return c
+
+
+class HostWeights:
+    """tqd_host_weights over host arrays; keeps the arrays alive."""
+
+    def __init__(self, layers, lm_head, out_norm, embed=None):
+        self._keep = [lm_head, out_norm, embed, layers]
+        n = len(layers)
+        self._layers = (tqd_layer_weights * n)()
+        for i, d in enumerate(layers):
+            for f in _LAYER_FIELDS:
+                setattr(self._layers[i], f, _ptr(d.get(f)))
+        self.struct = tqd_host_weights()
+        self.struct.layers = ctypes.cast(self._layers, ctypes.POINTER(tqd_layer_weights))
+        self.struct.out_norm = _ptr(out_norm)
+        self.struct.lm_head = _ptr(lm_head)
+        self.struct.embed = _ptr(embed)
+
+
+def make_host_weights(model) -> HostWeights:
+    """From an object with .layers (list of dicts of arrays), .lm_head,
+    .out_norm and optionally .embed."""
+    return HostWeights(model.layers, model.lm_head, model.out_norm, getattr(model, "embed", None))
+
+
+# ------------------------------------------------------------------ C ABI calls
+
+def tqd_status_name(status: int) -> str:
+    return lib().tqd_status_name(int(status)).decode()
+
+
+def tqd_create(config: tqd_config, weights: HostWeights, stream=None) -> int:
+    h = ctypes.c_void_p()
+    check(lib().tqd_create(ctypes.byref(config), ctypes.byref(weights.struct), _stream(stream),
+                           ctypes.byref(h)), "tqd_create")
+    return h.value
+
+
+def tqd_destroy(handle) -> None:
+    if handle:
+        lib().tqd_destroy(handle)
+
+
+def tqd_reset(handle, seq: int = 0) -> None:
+    check(lib().tqd_reset(handle, seq), "tqd_reset")
+
+
+def tqd_truncate(handle, seq: int, n_pos: int) -> None:
+    check(lib().tqd_truncate(handle, seq, int(n_pos)), "tqd_truncate")
+
+
+def tqd_next_pos(handle, seq: int = 0) -> int:
+    p = ctypes.c_int32()
+    check(lib().tqd_next_pos(handle, seq, ctypes.byref(p)), "tqd_next_pos")
+    return p.value
+
+
+def tqd_prefill(handle, seq: int, ids) -> int:
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    nxt = ctypes.c_int32()
+    check(lib().tqd_prefill(handle, seq, ids.ctypes.data, ids.size, ctypes.byref(nxt)), "tqd_prefill")
+    return nxt.value
+
+
+def tqd_kv_upload(handle, seq: int, k, v) -> None:
+    """k, v float32 [n_layers, n_pos, kv_width] host arrays."""
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    check(lib().tqd_kv_upload(handle, seq, k.shape[1], k.ctypes.data, v.ctypes.data), "tqd_kv_upload")
+
+
+def tqd_decode_step(handle, seq: int, token: int, pos: int) -> int:
+    nxt = ctypes.c_int32()
+    check(lib().tqd_decode_step(handle, seq, int(token), int(pos), ctypes.byref(nxt)), "tqd_decode_step")
+    return nxt.value
+
+
+def tqd_generate(handle, seq: int, first_token: int, n_steps: int, out=None) -> np.ndarray:
+    ids = out if out is not None else np.empty(n_steps, dtype=np.int32)
+    check(lib().tqd_generate(handle, seq, int(first_token), int(n_steps), ids.ctypes.data), "tqd_generate")
+    return ids
+
+
+def tqd_read_logits(handle, seq: int, vocab: int, out=None) -> np.ndarray:
+    logits = out if out is not None else np.empty(vocab, dtype=np.float32)
+    check(lib().tqd_read_logits(handle, seq, logits.ctypes.data), "tqd_read_logits")
+    return logits
+
+
+def tqd_phase_count(handle) -> int:
+    n = ctypes.c_int32()
+    check(lib().tqd_phase_count(handle, ctypes.byref(n)), "tqd_phase_count")
+    return n.value
+
+
+def tqd_step_bytes(handle, pos: int) -> int:
+    b = ctypes.c_int64()
+    check(lib().tqd_step_bytes(handle, int(pos), ctypes.byref(b)), "tqd_step_bytes")
+    return b.value
+
+
+class Decoder:
+    """Owns one model handle (tqd_create ... tqd_destroy)."""
+
+    def __init__(self, model, max_seq: int, max_batch: int = 1, schedule: int = TQD_SCHED_GRAPH,
+                 stream=None):
+        self.cfg = model.cfg
+        self.config = make_config(model.cfg, max_seq, max_batch, schedule)
+        self._weights = make_host_weights(model)
+        self.handle = tqd_create(self.config, self._weights, stream)
+        self._weights = None  # uploaded; host copies no longer needed by the library
+
+    def close(self):
+        if getattr(self, "handle", None):
+            tqd_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        self.close()
+
+    def prefill(self, ids, seq: int = 0) -> int:
+        return tqd_prefill(self.handle, seq, ids)
+
+    def decode_step(self, token: int, pos: int, seq: int = 0) -> int:
+        return tqd_decode_step(self.handle, seq, token, pos)
+
+    def generate(self, first_token: int, n_steps: int, seq: int = 0) -> np.ndarray:
+        return tqd_generate(self.handle, seq, first_token, n_steps)
+
+    def logits(self, seq: int = 0) -> np.ndarray:
+        return tqd_read_logits(self.handle, seq, self.cfg.vocab)
+
+    def kv_upload(self, k, v, seq: int = 0):
+        tqd_kv_upload(self.handle, seq, k, v)
+
+    def truncate(self, n_pos: int, seq: int = 0):
+        tqd_truncate(self.handle, seq, n_pos)
+
+    def next_pos(self, seq: int = 0) -> int:
+        return tqd_next_pos(self.handle, seq)
+
+    def reset(self, seq: int = 0):
+        tqd_reset(self.handle, seq)
+
+    @property
+    def phase_count(self) -> int:
+        return tqd_phase_count(self.handle)
+
+    def step_bytes(self, pos: int) -> int:
+        return tqd_step_bytes(self.handle, pos)
+
+
+from . import ops  # noqa: E402,F401  (operator entry points on torch tensors)

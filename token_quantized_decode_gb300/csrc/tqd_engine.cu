@@ -1,0 +1,767 @@
+// Host engine and C ABI of libtqd (declarations and contracts in tqd.h).
+//
+// A model owns one device arena: repacked weights, the RoPE cos/sin table,
+// and per sequence its KV cache, token history, activations and the
+// split-K / argmax partials.  Weights are uploaded once; a decode step
+// moves four bytes of token id each way ("One command buffer per token",
+// sections "Resident state" and "One command buffer").
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "tqd.h"
+#include "tqd_internal.h"
+
+using namespace tqd;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+void set_error(const char* fmt, ...) {
+  char buf[1024];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct SeqSlot {
+  DevSeq d{};
+  int32_t next_pos = 0;
+  cudaGraphExec_t g_full = nullptr;
+  cudaGraphExec_t g_layers = nullptr;
+};
+
+}  // namespace
+
+struct tqd_model {
+  tqd_config cfg{};
+  cudaStream_t stream = nullptr;
+  int device = 0, num_sms = 0;
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+  DevModel dm{};
+  std::vector<SeqSlot> seqs;
+  std::vector<DevLayer> host_layers;  // host copy of dm.layers (launch arguments)
+  int32_t* h_tokens = nullptr;  // pinned staging [max_seq + 1]
+  DevState* h_state = nullptr;  // pinned
+  bool poisoned = false;
+  bool pdl = true;
+  int blocks_qkv = 0, blocks_o = 0, blocks_gu = 0, blocks_d = 0, blocks_lm = 0;
+  int blocks_persist = 0;
+  int64_t weight_bytes = 0;
+};
+
+namespace {
+
+int32_t fail_cuda(tqd_model* m, cudaError_t e, const char* what) {
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  if (m) m->poisoned = true;
+  return TQD_ERR_CUDA;
+}
+
+#define CK(call, what)                                  \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return fail_cuda(m, e_, what); \
+  } while (0)
+
+// Bytes of one stored row of a matrix with `cols` columns.
+size_t row_bytes(int wtype, int cols) {
+  return wtype == TQD_WEIGHT_Q8_0 ? q8_row_bytes(cols) : static_cast<size_t>(cols) * 2;
+}
+// Bytes of one host row (34-byte blocks for Q8_0).
+size_t host_row_bytes(int wtype, int cols) {
+  return wtype == TQD_WEIGHT_Q8_0 ? static_cast<size_t>(cols) / 32 * 34
+                                  : static_cast<size_t>(cols) * 2;
+}
+
+int32_t validate_config(const tqd_config* c) {
+  std::string bad;
+  auto need = [&](bool ok, const char* msg) {
+    if (!ok) {
+      if (!bad.empty()) bad += "; ";
+      bad += msg;
+    }
+  };
+  need(c->n_layers >= 1, "n_layers must be >= 1");
+  need(c->hidden >= 1, "hidden must be >= 1");
+  need(c->n_heads >= 1 && c->n_kv_heads >= 1 && c->n_heads % c->n_kv_heads == 0,
+       "n_heads must be a positive multiple of n_kv_heads");
+  need(c->head_dim == 64 || c->head_dim == 128, "head_dim must be 64 or 128");
+  if (c->n_kv_heads >= 1)
+    need(attention_supported(c->head_dim == 64 ? 64 : 128, c->n_heads / c->n_kv_heads),
+         "n_heads / n_kv_heads must be 1, 2, 3, 4 or 8");
+  need(c->intermediate >= 1, "intermediate must be >= 1");
+  need(c->vocab >= 1, "vocab must be >= 1");
+  need(c->qk_norm == 0 || c->qk_norm == 1, "qk_norm must be 0 or 1");
+  need(c->weight_type == TQD_WEIGHT_Q8_0 || c->weight_type == TQD_WEIGHT_BF16,
+       "weight_type must be TQD_WEIGHT_Q8_0 or TQD_WEIGHT_BF16");
+  need(c->max_seq >= 1 && c->max_seq <= (1 << 24), "max_seq must be in [1, 2^24]");
+  need(c->max_batch >= 1 && c->max_batch <= 64, "max_batch must be in [1, 64]");
+  need(c->schedule == TQD_SCHED_GRAPH || c->schedule == TQD_SCHED_PERSISTENT,
+       "schedule must be TQD_SCHED_GRAPH or TQD_SCHED_PERSISTENT");
+  need(std::isfinite(c->rope_theta) && c->rope_theta > 0.f, "rope_theta must be > 0");
+  need(std::isfinite(c->rms_eps) && c->rms_eps >= 0.f, "rms_eps must be >= 0");
+  const int qw = c->n_heads * c->head_dim;
+  if (c->weight_type == TQD_WEIGHT_Q8_0) {
+    need(c->hidden % 32 == 0, "Q8_0 needs hidden % 32 == 0");
+    need(qw % 32 == 0, "Q8_0 needs n_heads*head_dim % 32 == 0");
+    need(c->intermediate % 32 == 0, "Q8_0 needs intermediate % 32 == 0");
+  } else {
+    need(c->hidden % 8 == 0, "bf16 needs hidden % 8 == 0");
+    need(qw % 8 == 0, "bf16 needs n_heads*head_dim % 8 == 0");
+    need(c->intermediate % 8 == 0, "bf16 needs intermediate % 8 == 0");
+  }
+  const int fmt = c->weight_type == TQD_WEIGHT_Q8_0 ? kFmtQ8 : kFmtBF16;
+  if (bad.empty()) {
+    need(matvec_cpl(fmt, c->hidden) != 0, "hidden too large for the matvec kernels");
+    need(matvec_cpl(fmt, qw) != 0, "n_heads*head_dim too large for the matvec kernels");
+    need(matvec_cpl(fmt, c->intermediate) != 0, "intermediate too large for the matvec kernels");
+  }
+  if (!bad.empty()) {
+    set_error("unsupported config: %s", bad.c_str());
+    return TQD_ERR_UNSUPPORTED_CONFIG;
+  }
+  return TQD_OK;
+}
+
+int32_t check_weights(const tqd_config* c, const tqd_host_weights* w) {
+  if (!w->layers || !w->out_norm || !w->lm_head) {
+    set_error("weights: layers, out_norm and lm_head are required");
+    return TQD_ERR_BAD_ARG;
+  }
+  for (int l = 0; l < c->n_layers; ++l) {
+    const tqd_layer_weights& L = w->layers[l];
+    if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.ffn_norm || !L.w_gate || !L.w_up ||
+        !L.w_down || (c->qk_norm && (!L.q_norm || !L.k_norm))) {
+      set_error("weights: layer %d has a NULL tensor", l);
+      return TQD_ERR_BAD_ARG;
+    }
+  }
+  return TQD_OK;
+}
+
+// Matvec blocks for `rows` rows with K columns on the graph schedule.
+int matvec_blocks(int fmt, int rows, int K, int num_sms, int cap) {
+  const int cpl = matvec_cpl(fmt, K);
+  const int R = cpl >= 4 ? 2 : 8 / cpl;
+  const int groups = (rows + R - 1) / R;
+  int b = (groups + kMatvecThreads / 32 - 1) / (kMatvecThreads / 32);
+  const int lim = cap > 0 ? cap : 4 * num_sms;
+  if (b > lim) b = lim;
+  return b < 1 ? 1 : b;
+}
+
+cudaError_t enqueue_step(tqd_model* m, SeqSlot& s, bool full) {
+  const DevModel& dm = m->dm;
+  const int fmt = dm.wtype;
+  const bool pdl = m->pdl;
+  cudaStream_t st = m->stream;
+  cudaError_t e = launch_embed(dm, s.d, st, false);
+  if (e != cudaSuccess) return e;
+  const std::vector<DevLayer>& layers = m->host_layers;
+  for (int l = 0; l < dm.n_layers; ++l) {
+    const DevLayer& L = layers[l];
+    MatvecLaunch a{};
+    a.eps = dm.eps;
+    a.seq = s.d;
+    a.max_seq = dm.max_seq;
+    // norm + QKV
+    a.W = L.wqkv; a.row_bytes = dm.row_bytes_h; a.K = dm.H; a.rows = dm.qw + 2 * dm.kvw;
+    a.epi = kEpiStore; a.y = s.d.qkv; a.src = s.d.x; a.norm_g = L.attn_norm; a.lm_head = false;
+    if ((e = launch_matvec(fmt, a, m->blocks_qkv, st, pdl)) != cudaSuccess) return e;
+    if ((e = launch_attention(dm, s.d, l, st, pdl)) != cudaSuccess) return e;
+    // O + residual
+    a.W = L.wo; a.row_bytes = dm.row_bytes_qw; a.K = dm.qw; a.rows = dm.H;
+    a.epi = kEpiResid; a.y = s.d.x; a.src = s.d.attn; a.norm_g = nullptr;
+    if ((e = launch_matvec(fmt, a, m->blocks_o, st, pdl)) != cudaSuccess) return e;
+    // norm + gate/up + SwiGLU
+    a.W = L.wgu; a.row_bytes = dm.row_bytes_h; a.K = dm.H; a.rows = 2 * dm.I;
+    a.epi = kEpiSwiGLU; a.y = s.d.h; a.src = s.d.x; a.norm_g = L.ffn_norm;
+    if ((e = launch_matvec(fmt, a, m->blocks_gu, st, pdl)) != cudaSuccess) return e;
+    // down + residual
+    a.W = L.wd; a.row_bytes = dm.row_bytes_i; a.K = dm.I; a.rows = dm.H;
+    a.epi = kEpiResid; a.y = s.d.x; a.src = s.d.h; a.norm_g = nullptr;
+    if ((e = launch_matvec(fmt, a, m->blocks_d, st, pdl)) != cudaSuccess) return e;
+  }
+  if (full) {
+    MatvecLaunch a{};
+    a.eps = dm.eps;
+    a.seq = s.d;
+    a.max_seq = dm.max_seq;
+    a.W = dm.lm_head; a.row_bytes = dm.row_bytes_h; a.K = dm.H; a.rows = dm.V;
+    a.epi = kEpiArgmax; a.y = s.d.logits; a.src = s.d.x; a.norm_g = dm.out_norm; a.lm_head = true;
+    return launch_matvec(fmt, a, m->blocks_lm, st, pdl);
+  }
+  return launch_advance(s.d, st, pdl);
+}
+
+int32_t capture(tqd_model* m, SeqSlot& s, bool full, cudaGraphExec_t* out) {
+  cudaGraph_t g = nullptr;
+  CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
+  cudaError_t e = enqueue_step(m, s, full);
+  cudaError_t e2 = cudaStreamEndCapture(m->stream, &g);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return fail_cuda(m, e, "capture step");
+  }
+  if (e2 != cudaSuccess) return fail_cuda(m, e2, "end capture");
+  e = cudaGraphInstantiate(out, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return fail_cuda(m, e, "instantiate graph");
+  return TQD_OK;
+}
+
+// Enqueue n steps for sequence s; steps with index >= full_from run the
+// lm_head and argmax.
+int32_t run_steps(tqd_model* m, SeqSlot& s, int n, int full_from) {
+  if (m->cfg.schedule == TQD_SCHED_PERSISTENT) {
+    CK(launch_persistent(m->dm, s.d, n, full_from, m->blocks_persist, m->stream),
+       "persistent launch");
+    return TQD_OK;
+  }
+  if (!s.g_full) {
+    int32_t rc = capture(m, s, true, &s.g_full);
+    if (rc) return rc;
+  }
+  if (full_from > 0 && !s.g_layers) {
+    int32_t rc = capture(m, s, false, &s.g_layers);
+    if (rc) return rc;
+  }
+  for (int i = 0; i < n; ++i)
+    CK(cudaGraphLaunch(i >= full_from ? s.g_full : s.g_layers, m->stream), "graph launch");
+  return TQD_OK;
+}
+
+// Read the device state back, synchronise, and turn error bits into a status.
+int32_t finish(tqd_model* m, SeqSlot& s) {
+  CK(cudaMemcpyAsync(m->h_state, s.d.state, sizeof(DevState), cudaMemcpyDeviceToHost, m->stream),
+     "read state");
+  CK(cudaStreamSynchronize(m->stream), "synchronize");
+  const uint32_t err = m->h_state->err;
+  if (err == 0) return TQD_OK;
+  if (err & (kErrGridBarrier | kErrMbarrier)) {
+    m->poisoned = true;
+    set_error("device wait timed out (error bits 0x%x)", err);
+    return TQD_ERR_DEVICE_TIMEOUT;
+  }
+  // clear recoverable bits so the sequence can continue after a reset
+  CK(cudaMemsetAsync(&s.d.state->err, 0, sizeof(uint32_t), m->stream), "clear error");
+  CK(cudaStreamSynchronize(m->stream), "synchronize");
+  if (err & kErrAllNaN) {
+    set_error("every logit was NaN");
+    return TQD_ERR_NUMERIC;
+  }
+  if (err & kErrCapacity) {
+    set_error("position beyond max_seq");
+    return TQD_ERR_CAPACITY;
+  }
+  set_error("token id outside the vocabulary");
+  return TQD_ERR_BAD_ARG;
+}
+
+int32_t check_model(tqd_model* m, int32_t seq) {
+  if (!m) {
+    set_error("model is NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  if (m->poisoned) {
+    set_error("model is poisoned by an earlier fatal error");
+    return TQD_ERR_POISONED;
+  }
+  if (seq < 0 || seq >= m->cfg.max_batch) {
+    set_error("seq %d outside [0, %d)", seq, m->cfg.max_batch);
+    return TQD_ERR_BAD_ARG;
+  }
+  return TQD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tqd_status_name(int32_t s) {
+  switch (s) {
+    case TQD_OK: return "TQD_OK";
+    case TQD_ERR_BAD_ARG: return "TQD_ERR_BAD_ARG";
+    case TQD_ERR_UNSUPPORTED_CONFIG: return "TQD_ERR_UNSUPPORTED_CONFIG";
+    case TQD_ERR_NO_DEVICE: return "TQD_ERR_NO_DEVICE";
+    case TQD_ERR_CUDA: return "TQD_ERR_CUDA";
+    case TQD_ERR_OOM: return "TQD_ERR_OOM";
+    case TQD_ERR_CAPACITY: return "TQD_ERR_CAPACITY";
+    case TQD_ERR_POS_MISMATCH: return "TQD_ERR_POS_MISMATCH";
+    case TQD_ERR_DEVICE_TIMEOUT: return "TQD_ERR_DEVICE_TIMEOUT";
+    case TQD_ERR_NUMERIC: return "TQD_ERR_NUMERIC";
+    case TQD_ERR_POISONED: return "TQD_ERR_POISONED";
+    default: return "TQD_UNKNOWN_STATUS";
+  }
+}
+
+const char* tqd_last_error(void) { return g_last_error.c_str(); }
+
+void tqd_destroy(tqd_model* m) {
+  if (!m) return;
+  if (m->stream) cudaStreamSynchronize(m->stream);
+  for (SeqSlot& s : m->seqs) {
+    if (s.g_full) cudaGraphExecDestroy(s.g_full);
+    if (s.g_layers) cudaGraphExecDestroy(s.g_layers);
+  }
+  if (m->arena) cudaFree(m->arena);
+  if (m->h_tokens) cudaFreeHost(m->h_tokens);
+  if (m->h_state) cudaFreeHost(m->h_state);
+  delete m;
+}
+
+int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* stream,
+                   tqd_model** out) {
+  g_last_error.clear();
+  if (!cfg || !w || !out) {
+    set_error("cfg, weights and out must be non-NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  *out = nullptr;
+  int32_t rc = validate_config(cfg);
+  if (rc) return rc;
+  if ((rc = check_weights(cfg, w))) return rc;
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    set_error("no CUDA device");
+    return TQD_ERR_NO_DEVICE;
+  }
+  tqd_model* m = new tqd_model();
+  m->cfg = *cfg;
+  m->stream = static_cast<cudaStream_t>(stream);
+  cudaDeviceProp prop;
+  cudaError_t pe = cudaGetDevice(&m->device);
+  if (pe == cudaSuccess) pe = cudaGetDeviceProperties(&prop, m->device);
+  if (pe != cudaSuccess) {
+    set_error("device query failed: %s", cudaGetErrorString(pe));
+    delete m;
+    return TQD_ERR_CUDA;
+  }
+  if (prop.major * 10 + prop.minor != 103) {
+    set_error("device %s is sm_%d%d; this library is built for sm_103a", prop.name, prop.major,
+              prop.minor);
+    delete m;
+    return TQD_ERR_NO_DEVICE;
+  }
+  m->num_sms = prop.multiProcessorCount;
+  if (const char* e = getenv("TQD_PDL")) m->pdl = atoi(e) != 0;
+
+  const int L = cfg->n_layers, H = cfg->hidden, hd = cfg->head_dim, nq = cfg->n_heads,
+            nkv = cfg->n_kv_heads, I = cfg->intermediate, V = cfg->vocab, S = cfg->max_seq;
+  const int qw = nq * hd, kvw = nkv * hd, wt = cfg->weight_type;
+  const int fmt = wt == TQD_WEIGHT_Q8_0 ? kFmtQ8 : kFmtBF16;
+  const size_t rbh = row_bytes(wt, H), rbq = row_bytes(wt, qw), rbi = row_bytes(wt, I);
+  int nch = (S + 31) / 32;
+  if (nch > m->num_sms / nkv) nch = m->num_sms / nkv;
+  if (nch < 1) nch = 1;
+
+  // ---- arena layout ----
+  const size_t A = 256;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, A);
+    return o;
+  };
+  struct LayerOff { size_t wqkv, wo, wgu, wd, an, qn, kn, fn; };
+  std::vector<LayerOff> lo(L);
+  for (int l = 0; l < L; ++l) {
+    lo[l].wqkv = take(rbh * (qw + 2 * kvw));
+    lo[l].wo = take(rbq * H);
+    lo[l].wgu = take(rbh * 2 * I);
+    lo[l].wd = take(rbi * H);
+    lo[l].an = take(4 * H);
+    lo[l].qn = take(4 * hd);
+    lo[l].kn = take(4 * hd);
+    lo[l].fn = take(4 * H);
+  }
+  const size_t o_lm = take(rbh * V);
+  const size_t o_embed = w->embed ? take(rbh * V) : o_lm;
+  const size_t o_onorm = take(4 * H);
+  const size_t o_rope = take(sizeof(float2) * static_cast<size_t>(S) * (hd / 2));
+  const size_t o_layers = take(sizeof(DevLayer) * L);
+  const size_t weights_end = off;
+  struct SeqOff { size_t state, tokens, kc, vc, x, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar; };
+  std::vector<SeqOff> so(cfg->max_batch);
+  const size_t kv_bytes = sizeof(float) * static_cast<size_t>(L) * S * kvw;
+  for (int b = 0; b < cfg->max_batch; ++b) {
+    so[b].state = take(sizeof(DevState));
+    so[b].tokens = take(4 * (static_cast<size_t>(S) + 1));
+    so[b].kc = take(kv_bytes);
+    so[b].vc = take(kv_bytes);
+    so[b].x = take(4 * H);
+    so[b].qkv = take(4 * (qw + 2 * kvw));
+    so[b].attn = take(4 * qw);
+    so[b].h = take(4 * I);
+    so[b].logits = take(4 * static_cast<size_t>(V));
+    so[b].po = take(4 * static_cast<size_t>(nq) * nch * hd);
+    so[b].pml = take(4 * static_cast<size_t>(nq) * nch * 2);
+    so[b].acnt = take(4 * nkv);
+    so[b].av = take(4 * kMaxArgmaxBlocks);
+    so[b].ai = take(4 * kMaxArgmaxBlocks);
+    so[b].acount = take(4);
+    so[b].bar = take(8);
+  }
+  m->arena_bytes = off;
+  cudaError_t ce = cudaMalloc(&m->arena, m->arena_bytes);
+  if (ce != cudaSuccess) {
+    cudaGetLastError();
+    set_error("cudaMalloc of %zu bytes failed: %s", m->arena_bytes, cudaGetErrorString(ce));
+    delete m;
+    return TQD_ERR_OOM;
+  }
+  if (cudaMallocHost(&m->h_tokens, 4 * (static_cast<size_t>(S) + 1)) != cudaSuccess ||
+      cudaMallocHost(&m->h_state, sizeof(DevState)) != cudaSuccess) {
+    cudaGetLastError();
+    set_error("pinned host allocation failed");
+    tqd_destroy(m);
+    return TQD_ERR_OOM;
+  }
+  uint8_t* base = m->arena;
+  cudaStream_t st = m->stream;
+  auto fail = [&](cudaError_t e, const char* what) {
+    int32_t r = fail_cuda(m, e, what);
+    tqd_destroy(m);
+    return r;
+  };
+  cudaError_t e = cudaMemsetAsync(base + weights_end, 0, m->arena_bytes - weights_end, st);
+  if (e != cudaSuccess) return fail(e, "clear sequence state");
+
+  // ---- weights: upload once, repack Q8_0 blocks into the row layout ----
+  uint8_t* tmp = nullptr;
+  if (wt == TQD_WEIGHT_Q8_0) {
+    size_t maxm = host_row_bytes(wt, H) * static_cast<size_t>(V);
+    size_t lm = host_row_bytes(wt, H) * (qw > 2 * I ? qw : 2 * I);
+    if (lm > maxm) maxm = lm;
+    if (host_row_bytes(wt, I) * H > maxm) maxm = host_row_bytes(wt, I) * H;
+    if (host_row_bytes(wt, qw) * H > maxm) maxm = host_row_bytes(wt, qw) * H;
+    ce = cudaMalloc(&tmp, maxm);
+    if (ce != cudaSuccess) {
+      cudaGetLastError();
+      set_error("cudaMalloc of the upload buffer failed: %s", cudaGetErrorString(ce));
+      tqd_destroy(m);
+      return TQD_ERR_OOM;
+    }
+  }
+  int64_t wbytes = 0;
+  // upload `rows` x `cols` host rows to destination rows dst_row0 + r*step
+  auto put = [&](const void* src, int rows, int cols, size_t dst_off, int dst_row0,
+                 int step) -> cudaError_t {
+    const size_t hrb = host_row_bytes(wt, cols), rb = row_bytes(wt, cols);
+    wbytes += static_cast<int64_t>(rb) * rows;
+    if (wt == TQD_WEIGHT_Q8_0) {
+      cudaError_t r = cudaMemcpyAsync(tmp, src, hrb * rows, cudaMemcpyHostToDevice, st);
+      if (r != cudaSuccess) return r;
+      r = launch_q8_repack(tmp, rows, cols, base + dst_off, dst_row0, step, st);
+      if (r != cudaSuccess) return r;
+      return cudaStreamSynchronize(st);  // tmp is reused by the next upload
+    }
+    return cudaMemcpy2DAsync(base + dst_off + rb * dst_row0, rb * step, src, hrb, hrb, rows,
+                             cudaMemcpyHostToDevice, st);
+  };
+  auto put_f32 = [&](const float* src, int n, size_t dst_off) -> cudaError_t {
+    wbytes += 4ll * n;
+    return cudaMemcpyAsync(base + dst_off, src, 4ull * n, cudaMemcpyHostToDevice, st);
+  };
+  std::vector<DevLayer> dl(L);
+  for (int l = 0; l < L; ++l) {
+    const tqd_layer_weights& W = w->layers[l];
+    if ((e = put(W.wq, qw, H, lo[l].wqkv, 0, 1)) != cudaSuccess ||
+        (e = put(W.wk, kvw, H, lo[l].wqkv, qw, 1)) != cudaSuccess ||
+        (e = put(W.wv, kvw, H, lo[l].wqkv, qw + kvw, 1)) != cudaSuccess ||
+        (e = put(W.wo, H, qw, lo[l].wo, 0, 1)) != cudaSuccess ||
+        (e = put(W.w_gate, I, H, lo[l].wgu, 0, 2)) != cudaSuccess ||
+        (e = put(W.w_up, I, H, lo[l].wgu, 1, 2)) != cudaSuccess ||
+        (e = put(W.w_down, H, I, lo[l].wd, 0, 1)) != cudaSuccess ||
+        (e = put_f32(W.attn_norm, H, lo[l].an)) != cudaSuccess ||
+        (e = put_f32(W.ffn_norm, H, lo[l].fn)) != cudaSuccess) {
+      if (tmp) cudaFree(tmp);
+      return fail(e, "upload layer weights");
+    }
+    if (cfg->qk_norm && ((e = put_f32(W.q_norm, hd, lo[l].qn)) != cudaSuccess ||
+                         (e = put_f32(W.k_norm, hd, lo[l].kn)) != cudaSuccess)) {
+      if (tmp) cudaFree(tmp);
+      return fail(e, "upload qk-norm gains");
+    }
+    dl[l].wqkv = base + lo[l].wqkv;
+    dl[l].wo = base + lo[l].wo;
+    dl[l].wgu = base + lo[l].wgu;
+    dl[l].wd = base + lo[l].wd;
+    dl[l].attn_norm = reinterpret_cast<const float*>(base + lo[l].an);
+    dl[l].q_norm = reinterpret_cast<const float*>(base + lo[l].qn);
+    dl[l].k_norm = reinterpret_cast<const float*>(base + lo[l].kn);
+    dl[l].ffn_norm = reinterpret_cast<const float*>(base + lo[l].fn);
+  }
+  if ((e = put(w->lm_head, V, H, o_lm, 0, 1)) != cudaSuccess ||
+      (w->embed && (e = put(w->embed, V, H, o_embed, 0, 1)) != cudaSuccess) ||
+      (e = put_f32(w->out_norm, H, o_onorm)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(base + o_layers, dl.data(), sizeof(DevLayer) * L,
+                           cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (e = launch_rope_table(static_cast<double>(cfg->rope_theta), hd, S,
+                             reinterpret_cast<float2*>(base + o_rope), st)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess) {
+    if (tmp) cudaFree(tmp);
+    return fail(e, "upload head weights");
+  }
+  if (tmp) cudaFree(tmp);
+  m->host_layers = dl;
+  if (w->embed) wbytes -= static_cast<int64_t>(row_bytes(wt, H)) * V;  // one row per step
+  m->weight_bytes = wbytes;
+
+  DevModel& dm = m->dm;
+  dm.n_layers = L; dm.H = H; dm.nq = nq; dm.nkv = nkv; dm.hd = hd; dm.I = I; dm.V = V;
+  dm.qk_norm = cfg->qk_norm; dm.wtype = fmt; dm.max_seq = S;
+  dm.qw = qw; dm.kvw = kvw; dm.n_chunks = nch;
+  dm.eps = cfg->rms_eps;
+  dm.attn_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
+  dm.row_bytes_h = rbh; dm.row_bytes_qw = rbq; dm.row_bytes_i = rbi;
+  dm.layers = reinterpret_cast<const DevLayer*>(base + o_layers);
+  dm.lm_head = base + o_lm;
+  dm.embed = base + o_embed;
+  dm.out_norm = reinterpret_cast<const float*>(base + o_onorm);
+  dm.rope = reinterpret_cast<const float2*>(base + o_rope);
+
+  m->seqs.resize(cfg->max_batch);
+  for (int b = 0; b < cfg->max_batch; ++b) {
+    DevSeq& d = m->seqs[b].d;
+    d.state = reinterpret_cast<DevState*>(base + so[b].state);
+    d.tokens = reinterpret_cast<int32_t*>(base + so[b].tokens);
+    d.kcache = reinterpret_cast<float*>(base + so[b].kc);
+    d.vcache = reinterpret_cast<float*>(base + so[b].vc);
+    d.x = reinterpret_cast<float*>(base + so[b].x);
+    d.qkv = reinterpret_cast<float*>(base + so[b].qkv);
+    d.attn = reinterpret_cast<float*>(base + so[b].attn);
+    d.h = reinterpret_cast<float*>(base + so[b].h);
+    d.logits = reinterpret_cast<float*>(base + so[b].logits);
+    d.part_o = reinterpret_cast<float*>(base + so[b].po);
+    d.part_ml = reinterpret_cast<float*>(base + so[b].pml);
+    d.attn_count = reinterpret_cast<uint32_t*>(base + so[b].acnt);
+    d.amax_v = reinterpret_cast<float*>(base + so[b].av);
+    d.amax_i = reinterpret_cast<int32_t*>(base + so[b].ai);
+    d.amax_count = reinterpret_cast<uint32_t*>(base + so[b].acount);
+    d.bar = reinterpret_cast<uint32_t*>(base + so[b].bar);
+  }
+  m->blocks_qkv = matvec_blocks(fmt, qw + 2 * kvw, H, m->num_sms, 0);
+  m->blocks_o = matvec_blocks(fmt, H, qw, m->num_sms, 0);
+  m->blocks_gu = matvec_blocks(fmt, 2 * I, H, m->num_sms, 0);
+  m->blocks_d = matvec_blocks(fmt, H, I, m->num_sms, 0);
+  m->blocks_lm = matvec_blocks(fmt, V, H, m->num_sms, kMaxArgmaxBlocks);
+  if (cfg->schedule == TQD_SCHED_PERSISTENT) {
+    const int per_sm = persistent_blocks_per_sm(fmt);
+    if (per_sm < 1) {
+      set_error("persistent kernel cannot be resident on an SM");
+      tqd_destroy(m);
+      return TQD_ERR_UNSUPPORTED_CONFIG;
+    }
+    m->blocks_persist = m->num_sms;
+  }
+  *out = m;
+  return TQD_OK;
+}
+
+int32_t tqd_reset(tqd_model* m, int32_t seq) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  SeqSlot& s = m->seqs[seq];
+  CK(cudaMemsetAsync(s.d.state, 0, sizeof(DevState), m->stream), "reset state");
+  CK(cudaStreamSynchronize(m->stream), "synchronize");
+  s.next_pos = 0;
+  return TQD_OK;
+}
+
+int32_t tqd_truncate(tqd_model* m, int32_t seq, int32_t n_pos) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  SeqSlot& s = m->seqs[seq];
+  if (n_pos < 0 || n_pos > s.next_pos) {
+    set_error("truncate to %d outside [0, %d]", n_pos, s.next_pos);
+    return TQD_ERR_BAD_ARG;
+  }
+  DevState st{};
+  st.pos = static_cast<uint32_t>(n_pos);
+  *m->h_state = st;
+  CK(cudaMemcpyAsync(s.d.state, m->h_state, sizeof(DevState), cudaMemcpyHostToDevice, m->stream),
+     "set position");
+  CK(cudaStreamSynchronize(m->stream), "synchronize");
+  s.next_pos = n_pos;
+  return TQD_OK;
+}
+
+int32_t tqd_next_pos(tqd_model* m, int32_t seq, int32_t* pos_out) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!pos_out) {
+    set_error("pos_out is NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  *pos_out = m->seqs[seq].next_pos;
+  return TQD_OK;
+}
+
+int32_t tqd_prefill(tqd_model* m, int32_t seq, const int32_t* ids, int32_t n, int32_t* next_out) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!ids || !next_out || n <= 0) {
+    set_error("prefill needs ids, next_out and n > 0");
+    return TQD_ERR_BAD_ARG;
+  }
+  SeqSlot& s = m->seqs[seq];
+  const int32_t pos = s.next_pos;
+  if (static_cast<int64_t>(pos) + n > m->cfg.max_seq) {
+    set_error("prefill of %d tokens at position %d exceeds max_seq %d", n, pos, m->cfg.max_seq);
+    return TQD_ERR_CAPACITY;
+  }
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= m->cfg.vocab) {
+      set_error("token id %d at index %d outside the vocabulary", ids[i], i);
+      return TQD_ERR_BAD_ARG;
+    }
+  memcpy(m->h_tokens, ids, 4ull * n);
+  CK(cudaMemcpyAsync(s.d.tokens + pos, m->h_tokens, 4ull * n, cudaMemcpyHostToDevice, m->stream),
+     "upload prompt");
+  if ((rc = run_steps(m, s, n, n - 1))) return rc;
+  CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + pos + n, 4, cudaMemcpyDeviceToHost, m->stream),
+     "read next token");
+  if ((rc = finish(m, s))) return rc;
+  s.next_pos = pos + n;
+  *next_out = m->h_tokens[0];
+  return TQD_OK;
+}
+
+int32_t tqd_kv_upload(tqd_model* m, int32_t seq, int32_t n_pos, const float* k, const float* v) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!k || !v || n_pos < 0) {
+    set_error("kv_upload needs k, v and n_pos >= 0");
+    return TQD_ERR_BAD_ARG;
+  }
+  if (n_pos > m->cfg.max_seq) {
+    set_error("n_pos %d exceeds max_seq %d", n_pos, m->cfg.max_seq);
+    return TQD_ERR_CAPACITY;
+  }
+  SeqSlot& s = m->seqs[seq];
+  const size_t kvw = static_cast<size_t>(m->dm.kvw);
+  if (n_pos > 0) {
+    const size_t w = 4 * kvw * n_pos, dpitch = 4 * kvw * m->cfg.max_seq;
+    CK(cudaMemcpy2DAsync(s.d.kcache, dpitch, k, w, w, m->cfg.n_layers, cudaMemcpyHostToDevice,
+                         m->stream),
+       "upload K");
+    CK(cudaMemcpy2DAsync(s.d.vcache, dpitch, v, w, w, m->cfg.n_layers, cudaMemcpyHostToDevice,
+                         m->stream),
+       "upload V");
+  }
+  DevState st{};
+  st.pos = static_cast<uint32_t>(n_pos);
+  *m->h_state = st;
+  CK(cudaMemcpyAsync(s.d.state, m->h_state, sizeof(DevState), cudaMemcpyHostToDevice, m->stream),
+     "set position");
+  CK(cudaStreamSynchronize(m->stream), "synchronize");
+  s.next_pos = n_pos;
+  return TQD_OK;
+}
+
+int32_t tqd_decode_step(tqd_model* m, int32_t seq, int32_t token, int32_t pos, int32_t* next_out) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!next_out || token < 0 || token >= m->cfg.vocab) {
+    set_error("decode_step needs next_out and a token in [0, vocab)");
+    return TQD_ERR_BAD_ARG;
+  }
+  SeqSlot& s = m->seqs[seq];
+  if (pos != s.next_pos) {
+    set_error("pos %d is not the sequence's next position %d", pos, s.next_pos);
+    return TQD_ERR_POS_MISMATCH;
+  }
+  if (pos >= m->cfg.max_seq) {
+    set_error("position %d is beyond max_seq %d", pos, m->cfg.max_seq);
+    return TQD_ERR_CAPACITY;
+  }
+  m->h_tokens[0] = token;
+  CK(cudaMemcpyAsync(s.d.tokens + pos, m->h_tokens, 4, cudaMemcpyHostToDevice, m->stream),
+     "write token");
+  if ((rc = run_steps(m, s, 1, 0))) return rc;
+  CK(cudaMemcpyAsync(m->h_tokens + 1, s.d.tokens + pos + 1, 4, cudaMemcpyDeviceToHost, m->stream),
+     "read next token");
+  if ((rc = finish(m, s))) return rc;
+  s.next_pos = pos + 1;
+  *next_out = m->h_tokens[1];
+  return TQD_OK;
+}
+
+int32_t tqd_generate(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_steps,
+                     int32_t* ids_out) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!ids_out || n_steps <= 0 || first_token < 0 || first_token >= m->cfg.vocab) {
+    set_error("generate needs ids_out, n_steps > 0 and a first token in [0, vocab)");
+    return TQD_ERR_BAD_ARG;
+  }
+  SeqSlot& s = m->seqs[seq];
+  const int32_t pos = s.next_pos;
+  if (static_cast<int64_t>(pos) + n_steps > m->cfg.max_seq) {
+    set_error("%d steps at position %d exceed max_seq %d", n_steps, pos, m->cfg.max_seq);
+    return TQD_ERR_CAPACITY;
+  }
+  m->h_tokens[0] = first_token;
+  CK(cudaMemcpyAsync(s.d.tokens + pos, m->h_tokens, 4, cudaMemcpyHostToDevice, m->stream),
+     "write token");
+  if ((rc = run_steps(m, s, n_steps, 0))) return rc;
+  CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + pos + 1, 4ull * n_steps, cudaMemcpyDeviceToHost,
+                     m->stream),
+     "read tokens");
+  if ((rc = finish(m, s))) return rc;
+  s.next_pos = pos + n_steps;
+  memcpy(ids_out, m->h_tokens, 4ull * n_steps);
+  return TQD_OK;
+}
+
+int32_t tqd_read_logits(tqd_model* m, int32_t seq, float* host_out) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!host_out) {
+    set_error("host_out is NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  CK(cudaMemcpyAsync(host_out, m->seqs[seq].d.logits, 4ull * m->cfg.vocab, cudaMemcpyDeviceToHost,
+                     m->stream),
+     "read logits");
+  CK(cudaStreamSynchronize(m->stream), "synchronize");
+  return TQD_OK;
+}
+
+int32_t tqd_phase_count(tqd_model* m, int32_t* out) {
+  if (!m || !out) {
+    set_error("model and out must be non-NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  const int L = m->cfg.n_layers;
+  *out = m->cfg.schedule == TQD_SCHED_GRAPH ? 5 * L + 2 : 5 * L + 1;
+  return TQD_OK;
+}
+
+int32_t tqd_step_bytes(tqd_model* m, int32_t pos, int64_t* bytes_out) {
+  if (!m || !bytes_out || pos < 0) {
+    set_error("model, bytes_out and pos >= 0 required");
+    return TQD_ERR_BAD_ARG;
+  }
+  const int64_t kv_row = 4ll * m->dm.kvw * 2 * m->cfg.n_layers;  // K and V, all layers
+  *bytes_out = m->weight_bytes + static_cast<int64_t>(row_bytes(m->cfg.weight_type, m->cfg.hidden)) +
+               kv_row * (static_cast<int64_t>(pos) + 1) + kv_row;
+  return TQD_OK;
+}
+
+}  // extern "C"

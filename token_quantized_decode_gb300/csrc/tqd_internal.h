@@ -1,0 +1,97 @@
+// Host-side interface between the engine / operator entry points and the
+// kernels translation unit.  Every launcher returns the cudaError_t of the
+// launch; none synchronises.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tqd_device.cuh"
+
+namespace tqd {
+
+constexpr int kMatvecThreads = 256;      // 8 warps per matvec block (graph schedule)
+constexpr int kAttnThreads = 128;        // 4 warps per attention block (graph schedule)
+constexpr int kPersistThreads = 512;     // 16 warps per persistent block
+constexpr int kMaxArgmaxBlocks = 2048;   // bound on lm_head blocks (argmax candidates)
+
+// Chunks of 16 bytes per lane needed for a row of K weights, rounded up to an
+// instantiated value; 0 when K is too long for the matvec kernels.
+__host__ __device__ inline int matvec_cpl(int fmt, int K) {
+  const int epc = fmt == 0 ? 16 : 8;
+  if (K <= 0 || K % epc) return 0;
+  const int need = (K / epc + 31) / 32;
+  if (need <= 2) return need;
+  if (need <= 4) return 4;
+  if (need <= 6) return 6;
+  if (need <= 8) return 8;
+  if (need <= 12) return 12;
+  return 0;
+}
+
+// Bytes of one stored Q8_0 row of K weights: K quants, K/32 f16 scales,
+// padded to a multiple of 16 bytes (no padding when K % 256 == 0).
+__host__ __device__ inline size_t q8_row_bytes(int64_t K) {
+  return static_cast<size_t>((K + K / 16 + 15) / 16 * 16);
+}
+
+// Shared memory (bytes) of the matvec kernel for K columns.
+__host__ __device__ inline size_t matvec_smem_bytes(int K) {
+  const int kpad = (K + 3) & ~3;
+  return static_cast<size_t>(kpad) * 4 + 64 * 4 + 16;
+}
+
+struct MatvecLaunch {
+  const uint8_t* W;
+  size_t row_bytes;
+  int K, rows, epi;
+  float* y;
+  const float* src;     // vector staged into shared memory (K floats)
+  const float* norm_g;  // RMSNorm gain applied to the staged vector, or nullptr
+  float eps;
+  // lm_head only: the step's argmax epilogue
+  bool lm_head;
+  DevSeq seq;
+  int max_seq;
+};
+
+cudaError_t launch_matvec(int fmt, const MatvecLaunch& a, int blocks, cudaStream_t st, bool pdl);
+
+cudaError_t launch_embed(const DevModel& m, const DevSeq& s, cudaStream_t st, bool pdl);
+cudaError_t launch_attention(const DevModel& m, const DevSeq& s, int layer, cudaStream_t st,
+                             bool pdl);
+cudaError_t launch_advance(const DevSeq& s, cudaStream_t st, bool pdl);
+
+// One cooperative launch running n_steps decode steps (the last `full_steps`
+// of them with the lm_head and argmax; earlier ones are prefill positions).
+cudaError_t launch_persistent(const DevModel& m, const DevSeq& s, int n_steps, int full_from,
+                              int blocks, cudaStream_t st);
+int persistent_blocks_per_sm(int fmt);
+size_t persistent_smem_bytes(const DevModel& m);
+
+// Set-up kernels.
+cudaError_t launch_q8_repack(const uint8_t* src_blocks, int64_t rows, int64_t cols, uint8_t* dst,
+                             int64_t dst_row0, int64_t dst_row_step, cudaStream_t st);
+cudaError_t launch_rope_table(double theta, int head_dim, int max_pos, float2* table,
+                              cudaStream_t st);
+
+// Operator entry points' kernels.
+cudaError_t launch_op_matvec(int fmt, const uint8_t* W, size_t row_bytes, int rows, int K,
+                             const float* x, float* y, cudaStream_t st);
+cudaError_t launch_op_rmsnorm(const float* x, const float* g, int rows, int n, float eps,
+                              float* out, cudaStream_t st);
+cudaError_t launch_op_rope(float* x, int n_heads, int head_dim, const float2* row,
+                           cudaStream_t st);
+cudaError_t launch_op_attention(const float* q, const float* K, const float* V, int S, int nq,
+                                int nkv, int hd, int n_chunks, float* out, float* part_o,
+                                float* part_ml, uint32_t* count, cudaStream_t st);
+cudaError_t launch_op_silu_mul(const float* g, const float* u, int64_t n, float* out,
+                               cudaStream_t st);
+cudaError_t launch_op_argmax(const float* x, int64_t n, int32_t* out, float* cand_v,
+                             int32_t* cand_i, uint32_t* count, cudaStream_t st);
+constexpr int kOpArgmaxBlocks = 304;
+
+bool attention_supported(int hd, int group);
+
+}  // namespace tqd
