@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=128)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kv-source", choices=["prefill", "upload"], default="prefill",
+                   help="prefill the prompt on the GPU, or upload a seeded stand-in KV history of the same "
+                        "length (for profiling captures that should not include the prefill launches)")
     return p.parse_args()
 
 
@@ -214,7 +217,13 @@ def run_tqd(args, wl, world, rank, local, pg):
     schedule = tqd.TQD_SCHED_PERSISTENT if args.schedule == "persistent" else tqd.TQD_SCHED_GRAPH
     dec = tqd.Decoder(model, P + D, 1, schedule, stream=stream)
     del model
-    first = dec.prefill(ids)
+    if args.kv_source == "prefill":
+        first = dec.prefill(ids)
+    else:
+        k, v = synth.kv_fill(cfg, 7, 0, P, -1.0, 1.0)
+        dec.kv_upload(k, v)
+        del k, v
+        first = int(ids[-1])
 
     def windows(n_tokens):
         out, left = [], n_tokens

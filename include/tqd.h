@@ -21,9 +21,11 @@
  *    call.  All device memory is owned by the library (one arena per model,
  *    allocated by tqd_create, freed by tqd_destroy).  Functions named
  *    tqd_op_* take DEVICE pointers owned by the caller instead.
- *  - `stream` arguments are cudaStream_t values passed as void* (NULL = the
- *    legacy default stream).  A model runs all its work on the stream given
- *    to tqd_create.
+ *  - `stream` arguments are cudaStream_t values passed as void*.  A model
+ *    runs all its work on the stream given to tqd_create; when that is NULL
+ *    the model creates a private non-blocking stream and destroys it in
+ *    tqd_destroy.  Operator entry points run on the stream given (NULL = the
+ *    legacy default stream).
  *  - After TQD_ERR_CUDA or TQD_ERR_DEVICE_TIMEOUT a model is poisoned: every
  *    later call but tqd_destroy returns TQD_ERR_POISONED.
  *  - A model is not thread-safe: calls on one model must not overlap.

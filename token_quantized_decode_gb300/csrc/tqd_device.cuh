@@ -215,8 +215,16 @@ struct DevLayer {
 struct DevState {  // per sequence, in device memory
   uint32_t pos;    // next position (= KV rows filled)
   uint32_t err;    // kErr* bits
-  uint32_t steps;  // steps completed by the current persistent launch
+  uint32_t steps;  // steps completed (diagnostic)
   uint32_t pad;
+};
+
+// Grid barrier of the persistent schedule: a monotonic arrival count and the
+// number of barriers completed so far.  Set to zero once at creation and never
+// reset, so every barrier's target is (completed + 1) * blocks.
+struct DevBarrier {
+  unsigned long long count;
+  unsigned long long epoch;
 };
 
 struct DevModel {
@@ -237,7 +245,7 @@ struct DevModel {
 struct DevSeq {
   DevState* state;
   int32_t* tokens;        // [max_seq + 1]: input token of each position
-  float* kcache;          // [n_layers][max_seq][kvw]
+  float* kcache;          // [n_layers][n_kv_heads][max_seq][head_dim]
   float* vcache;
   float* x;               // [H] residual stream
   float* qkv;             // [qw + 2 kvw] raw projections
@@ -250,7 +258,8 @@ struct DevSeq {
   float* amax_v;          // [max_ctas] per-CTA argmax candidates
   int32_t* amax_i;
   uint32_t* amax_count;   // [1]
-  uint32_t* bar;          // [2] grid barrier: count, generation
+  DevBarrier* bar;        // grid barrier of the persistent schedule
+  float* x_mid;           // [H] residual after the attention block
 };
 
 }  // namespace tqd

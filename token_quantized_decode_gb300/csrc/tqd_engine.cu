@@ -46,6 +46,7 @@ struct SeqSlot {
 struct tqd_model {
   tqd_config cfg{};
   cudaStream_t stream = nullptr;
+  bool own_stream = false;  // created by tqd_create (caller passed NULL)
   int device = 0, num_sms = 0;
   uint8_t* arena = nullptr;
   size_t arena_bytes = 0;
@@ -319,6 +320,7 @@ void tqd_destroy(tqd_model* m) {
   if (m->arena) cudaFree(m->arena);
   if (m->h_tokens) cudaFreeHost(m->h_tokens);
   if (m->h_state) cudaFreeHost(m->h_state);
+  if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
   delete m;
 }
 
@@ -358,6 +360,16 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     return TQD_ERR_NO_DEVICE;
   }
   m->num_sms = prop.multiProcessorCount;
+  if (!m->stream) {
+    // the legacy default stream cannot be captured into a graph
+    pe = cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking);
+    if (pe != cudaSuccess) {
+      set_error("stream creation failed: %s", cudaGetErrorString(pe));
+      delete m;
+      return TQD_ERR_CUDA;
+    }
+    m->own_stream = true;
+  }
   if (const char* e = getenv("TQD_PDL")) m->pdl = atoi(e) != 0;
 
   const int L = cfg->n_layers, H = cfg->hidden, hd = cfg->head_dim, nq = cfg->n_heads,
@@ -365,8 +377,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const int qw = nq * hd, kvw = nkv * hd, wt = cfg->weight_type;
   const int fmt = wt == TQD_WEIGHT_Q8_0 ? kFmtQ8 : kFmtBF16;
   const size_t rbh = row_bytes(wt, H), rbq = row_bytes(wt, qw), rbi = row_bytes(wt, I);
-  int nch = (S + 31) / 32;
-  if (nch > m->num_sms / nkv) nch = m->num_sms / nkv;
+  // split-K attention chunks: one (kv head, chunk) item per SM
+  int nch = m->num_sms / nkv;
   if (nch < 1) nch = 1;
 
   // ---- arena layout ----
@@ -395,7 +407,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const size_t o_rope = take(sizeof(float2) * static_cast<size_t>(S) * (hd / 2));
   const size_t o_layers = take(sizeof(DevLayer) * L);
   const size_t weights_end = off;
-  struct SeqOff { size_t state, tokens, kc, vc, x, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar; };
+  struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar; };
   std::vector<SeqOff> so(cfg->max_batch);
   const size_t kv_bytes = sizeof(float) * static_cast<size_t>(L) * S * kvw;
   for (int b = 0; b < cfg->max_batch; ++b) {
@@ -404,6 +416,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].kc = take(kv_bytes);
     so[b].vc = take(kv_bytes);
     so[b].x = take(4 * H);
+    so[b].xmid = take(4 * H);
     so[b].qkv = take(4 * (qw + 2 * kvw));
     so[b].attn = take(4 * qw);
     so[b].h = take(4 * I);
@@ -414,14 +427,15 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].av = take(4 * kMaxArgmaxBlocks);
     so[b].ai = take(4 * kMaxArgmaxBlocks);
     so[b].acount = take(4);
-    so[b].bar = take(8);
+    so[b].bar = take(sizeof(DevBarrier));
   }
   m->arena_bytes = off;
   cudaError_t ce = cudaMalloc(&m->arena, m->arena_bytes);
   if (ce != cudaSuccess) {
     cudaGetLastError();
     set_error("cudaMalloc of %zu bytes failed: %s", m->arena_bytes, cudaGetErrorString(ce));
-    delete m;
+    m->arena = nullptr;
+    tqd_destroy(m);
     return TQD_ERR_OOM;
   }
   if (cudaMallocHost(&m->h_tokens, 4 * (static_cast<size_t>(S) + 1)) != cudaSuccess ||
@@ -543,6 +557,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.kcache = reinterpret_cast<float*>(base + so[b].kc);
     d.vcache = reinterpret_cast<float*>(base + so[b].vc);
     d.x = reinterpret_cast<float*>(base + so[b].x);
+    d.x_mid = reinterpret_cast<float*>(base + so[b].xmid);
     d.qkv = reinterpret_cast<float*>(base + so[b].qkv);
     d.attn = reinterpret_cast<float*>(base + so[b].attn);
     d.h = reinterpret_cast<float*>(base + so[b].h);
@@ -553,7 +568,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.amax_v = reinterpret_cast<float*>(base + so[b].av);
     d.amax_i = reinterpret_cast<int32_t*>(base + so[b].ai);
     d.amax_count = reinterpret_cast<uint32_t*>(base + so[b].acount);
-    d.bar = reinterpret_cast<uint32_t*>(base + so[b].bar);
+    d.bar = reinterpret_cast<DevBarrier*>(base + so[b].bar);
   }
   m->blocks_qkv = matvec_blocks(fmt, qw + 2 * kvw, H, m->num_sms, 0);
   m->blocks_o = matvec_blocks(fmt, H, qw, m->num_sms, 0);
@@ -561,9 +576,11 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   m->blocks_d = matvec_blocks(fmt, H, I, m->num_sms, 0);
   m->blocks_lm = matvec_blocks(fmt, V, H, m->num_sms, kMaxArgmaxBlocks);
   if (cfg->schedule == TQD_SCHED_PERSISTENT) {
-    const int per_sm = persistent_blocks_per_sm(fmt);
+    const int per_sm = persistent_blocks_per_sm(m->dm);
     if (per_sm < 1) {
-      set_error("persistent kernel cannot be resident on an SM");
+      cudaGetLastError();
+      set_error("persistent kernel cannot be resident on an SM (%zu bytes of shared memory)",
+                persistent_smem_bytes(m->dm));
       tqd_destroy(m);
       return TQD_ERR_UNSUPPORTED_CONFIG;
     }
@@ -656,13 +673,19 @@ int32_t tqd_kv_upload(tqd_model* m, int32_t seq, int32_t n_pos, const float* k, 
   SeqSlot& s = m->seqs[seq];
   const size_t kvw = static_cast<size_t>(m->dm.kvw);
   if (n_pos > 0) {
-    const size_t w = 4 * kvw * n_pos, dpitch = 4 * kvw * m->cfg.max_seq;
-    CK(cudaMemcpy2DAsync(s.d.kcache, dpitch, k, w, w, m->cfg.n_layers, cudaMemcpyHostToDevice,
-                         m->stream),
-       "upload K");
-    CK(cudaMemcpy2DAsync(s.d.vcache, dpitch, v, w, w, m->cfg.n_layers, cudaMemcpyHostToDevice,
-                         m->stream),
-       "upload V");
+    // host rows [layer][pos][kv head * head_dim] -> device [layer][kv head][pos][head_dim]
+    const size_t hd = static_cast<size_t>(m->dm.hd);
+    for (int l = 0; l < m->cfg.n_layers; ++l)
+      for (int g = 0; g < m->dm.nkv; ++g) {
+        const size_t src = (static_cast<size_t>(l) * n_pos) * kvw + g * hd;
+        const size_t dst = (static_cast<size_t>(l) * m->dm.nkv + g) * m->cfg.max_seq * hd;
+        CK(cudaMemcpy2DAsync(s.d.kcache + dst, 4 * hd, k + src, 4 * kvw, 4 * hd, n_pos,
+                             cudaMemcpyHostToDevice, m->stream),
+           "upload K");
+        CK(cudaMemcpy2DAsync(s.d.vcache + dst, 4 * hd, v + src, 4 * kvw, 4 * hd, n_pos,
+                             cudaMemcpyHostToDevice, m->stream),
+           "upload V");
+      }
   }
   DevState st{};
   st.pos = static_cast<uint32_t>(n_pos);

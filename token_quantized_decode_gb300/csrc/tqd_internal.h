@@ -13,7 +13,6 @@ namespace tqd {
 
 constexpr int kMatvecThreads = 256;      // 8 warps per matvec block (graph schedule)
 constexpr int kAttnThreads = 128;        // 4 warps per attention block (graph schedule)
-constexpr int kPersistThreads = 512;     // 16 warps per persistent block
 constexpr int kMaxArgmaxBlocks = 2048;   // bound on lm_head blocks (argmax candidates)
 
 // Chunks of 16 bytes per lane needed for a row of K weights, rounded up to an
@@ -67,7 +66,8 @@ cudaError_t launch_advance(const DevSeq& s, cudaStream_t st, bool pdl);
 // of them with the lm_head and argmax; earlier ones are prefill positions).
 cudaError_t launch_persistent(const DevModel& m, const DevSeq& s, int n_steps, int full_from,
                               int blocks, cudaStream_t st);
-int persistent_blocks_per_sm(int fmt);
+int persistent_blocks_per_sm(const DevModel& m);  // 0: unsupported or not resident
+bool persistent_supported(const DevModel& m);
 size_t persistent_smem_bytes(const DevModel& m);
 
 // Set-up kernels.

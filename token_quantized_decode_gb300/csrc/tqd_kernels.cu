@@ -4,8 +4,6 @@
 //    QK-norm + RoPE + KV append + split-K attention; O matvec + residual;
 //    norm + gate/up matvec + SwiGLU; down matvec + residual; norm + lm_head
 //    matvec + argmax), chained with programmatic dependent launch;
-//  - persistent schedule: one cooperative kernel running the same phases
-//    with bounded grid barriers between them;
 //  - set-up kernels (Q8_0 repack, RoPE table) and the operator kernels.
 //
 // The op order is the per-layer sequence of the inferno.rs blog, "IV.4: One
@@ -18,21 +16,8 @@
 namespace tqd {
 
 // ---------------------------------------------------------------------------
-// matvec dispatch over the instantiated chunk counts
+// matvec: one kernel per (format, chunks per lane), chosen on the host
 // ---------------------------------------------------------------------------
-template <int FMT>
-__device__ __forceinline__ void matvec_dispatch(int cpl, const MatvecJob& job, const float* xs,
-                                                int block, int nblocks, ArgmaxAcc& am) {
-  switch (cpl) {
-    case 1: matvec_phase<FMT, 1>(job, xs, block, nblocks, am); break;
-    case 2: matvec_phase<FMT, 2>(job, xs, block, nblocks, am); break;
-    case 4: matvec_phase<FMT, 4>(job, xs, block, nblocks, am); break;
-    case 6: matvec_phase<FMT, 6>(job, xs, block, nblocks, am); break;
-    case 8: matvec_phase<FMT, 8>(job, xs, block, nblocks, am); break;
-    default: matvec_phase<FMT, 12>(job, xs, block, nblocks, am); break;
-  }
-}
-
 // The end of a full step, run by one thread of the last lm_head block: the
 // argmax becomes the input token of the next position and the position
 // advances ("One command buffer": the four bytes read back).
@@ -54,7 +39,7 @@ struct MatvecKArgs {
   uint32_t* err;
 };
 
-template <int FMT>
+template <int FMT, int CPL>
 __global__ void __launch_bounds__(kMatvecThreads) k_matvec(MatvecKArgs args) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const MatvecLaunch& a = args.a;
@@ -73,7 +58,7 @@ __global__ void __launch_bounds__(kMatvecThreads) k_matvec(MatvecKArgs args) {
   if (a.norm_g) rmsnorm_smem(xs, a.norm_g, a.K, a.eps, red);
   ArgmaxAcc am{-INFINITY, INT_MAX};
   const MatvecJob job{a.W, a.row_bytes, a.K, a.rows, a.epi, a.y};
-  matvec_dispatch<FMT>(args.cpl, job, xs, blockIdx.x, gridDim.x, am);
+  matvec_phase<FMT, CPL>(job, xs, blockIdx.x, gridDim.x, am);
   if (a.lm_head) {
     float wv;
     int wi;
@@ -113,8 +98,14 @@ cudaError_t launch_matvec(int fmt, const MatvecLaunch& a, int blocks, cudaStream
   if (args.cpl == 0 || blocks <= 0) return cudaErrorInvalidValue;
   if (a.lm_head && blocks > kMaxArgmaxBlocks) return cudaErrorInvalidValue;
   void* params[] = {&args};
-  const void* fn = fmt == kFmtQ8 ? reinterpret_cast<const void*>(&k_matvec<kFmtQ8>)
-                                 : reinterpret_cast<const void*>(&k_matvec<kFmtBF16>);
+  const void* fn = nullptr;
+#define TQD_MV(F, C) \
+  if (fmt == F && args.cpl == C) fn = reinterpret_cast<const void*>(&k_matvec<F, C>);
+  TQD_MV(kFmtQ8, 1) TQD_MV(kFmtQ8, 2) TQD_MV(kFmtQ8, 4) TQD_MV(kFmtQ8, 6) TQD_MV(kFmtQ8, 8)
+  TQD_MV(kFmtQ8, 12) TQD_MV(kFmtBF16, 1) TQD_MV(kFmtBF16, 2) TQD_MV(kFmtBF16, 4)
+  TQD_MV(kFmtBF16, 6) TQD_MV(kFmtBF16, 8) TQD_MV(kFmtBF16, 12)
+#undef TQD_MV
+  if (!fn) return cudaErrorInvalidValue;
   return launch_ex(fn, dim3(blocks), dim3(kMatvecThreads), matvec_smem_bytes(a.K), st, pdl, false,
                    params);
 }
@@ -190,9 +181,11 @@ __device__ __forceinline__ AttnJob layer_attn_job(const DevModel& m, const DevSe
   a.q_norm = m.qk_norm ? m.layers[layer].q_norm : nullptr;
   a.k_norm = m.qk_norm ? m.layers[layer].k_norm : nullptr;
   a.rope = m.rope + static_cast<size_t>(pos) * (m.hd / 2);
+  // head-major cache: [layer][kv head][position][head_dim]
   a.kc = s.kcache + static_cast<size_t>(layer) * m.max_seq * m.kvw;
   a.vc = s.vcache + static_cast<size_t>(layer) * m.max_seq * m.kvw;
-  a.kvw = m.kvw;
+  a.head_stride = static_cast<size_t>(m.max_seq) * m.hd;
+  a.row_stride = static_cast<size_t>(m.hd);
   a.S = static_cast<int>(pos) + 1;
   a.nq = m.nq;
   a.nkv = m.nkv;
@@ -255,165 +248,6 @@ cudaError_t launch_attention(const DevModel& m, const DevSeq& s, int layer, cuda
   return launch_ex(reinterpret_cast<const void*>(&k_attention), dim3(m.nkv * m.n_chunks),
                    dim3(kAttnThreads), attn_smem_bytes(m.hd, G, kAttnThreads / 32), st, pdl,
                    false, params);
-}
-
-// ---------------------------------------------------------------------------
-// persistent schedule
-// ---------------------------------------------------------------------------
-// Grid barrier: arrive on a counter, the last arriver resets it and bumps the
-// generation; everyone else polls the generation with a %globaltimer bound.
-// Returns false (all threads) if the wait gave up.
-__device__ __forceinline__ bool grid_barrier(uint32_t* bar, uint32_t nblocks, uint32_t* err) {
-  __shared__ uint32_t s_ok;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t ok = 1;
-    const uint32_t gen = ld_acquire_u32(bar + 1);
-    __threadfence();
-    const uint32_t old = atomicAdd(bar, 1u);
-    if (old == nblocks - 1) {
-      bar[0] = 0u;
-      __threadfence();
-      st_release_u32(bar + 1, gen + 1);
-    } else {
-      const uint64_t t0 = global_timer_ns();
-      while (ld_acquire_u32(bar + 1) == gen) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-          atomicOr(err, kErrGridBarrier);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    s_ok = ok;
-  }
-  __syncthreads();
-  return s_ok != 0;
-}
-
-size_t persistent_smem_bytes(const DevModel& m) {
-  int kmax = m.H;
-  if (m.qw > kmax) kmax = m.qw;
-  if (m.I > kmax) kmax = m.I;
-  const size_t x = matvec_smem_bytes(kmax);
-  return x + attn_smem_bytes(m.hd, m.nq / m.nkv, kPersistThreads / 32);
-}
-
-template <int FMT>
-__global__ void __launch_bounds__(kPersistThreads, 1)
-    k_persistent(DevModel m, DevSeq s, int n_steps, int full_from) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  int kmax = m.H;
-  if (m.qw > kmax) kmax = m.qw;
-  if (m.I > kmax) kmax = m.I;
-  const int kpad = (kmax + 3) & ~3;
-  float* xs = reinterpret_cast<float*>(smem_raw);
-  float* red = xs + kpad;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 64);
-  float* asmem = reinterpret_cast<float*>(smem_raw + matvec_smem_bytes(kmax));
-  uint32_t* err = &s.state->err;
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  const int cpl_h = matvec_cpl(FMT, m.H), cpl_qw = matvec_cpl(FMT, m.qw),
-            cpl_i = matvec_cpl(FMT, m.I);
-  const uint32_t nb = gridDim.x;
-  const int G = m.nq / m.nkv;
-  const int n_items = m.nkv * m.n_chunks;
-  uint32_t parity = 0;
-  const uint32_t pos0 = __ldcg(&s.state->pos);
-  for (int step = 0; step < n_steps; ++step) {
-    const uint32_t pos = pos0 + step;
-    if (pos >= static_cast<uint32_t>(m.max_seq)) {
-      if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, kErrCapacity);
-      return;
-    }
-    const int tok = checked_token(m, s, pos);
-    for (int l = 0; l < m.n_layers; ++l) {
-      const DevLayer& L = m.layers[l];
-      ArgmaxAcc am{-INFINITY, INT_MAX};
-      // norm + QKV
-      if (l == 0) {
-        embed_row(m, tok, xs);
-        __syncthreads();
-        if (blockIdx.x == 0)
-          for (int i = threadIdx.x; i < m.H; i += blockDim.x) s.x[i] = xs[i];
-      } else if (!stage_vector(xs, s.x, m.H, bar, parity, err)) {
-        return;
-      }
-      rmsnorm_smem(xs, L.attn_norm, m.H, m.eps, red);
-      matvec_dispatch<FMT>(cpl_h, MatvecJob{L.wqkv, m.row_bytes_h, m.H, m.qw + 2 * m.kvw, kEpiStore, s.qkv},
-                           xs, blockIdx.x, nb, am);
-      if (!grid_barrier(s.bar, nb, err)) return;
-      // QK-norm + RoPE + append + split-K attention
-      {
-        const AttnJob a = layer_attn_job(m, s, l, pos);
-        for (int item = blockIdx.x; item < n_items; item += nb)
-          attention_dispatch(a, m.hd, G, item, asmem, err);
-      }
-      if (!grid_barrier(s.bar, nb, err)) return;
-      // O projection + residual
-      if (!stage_vector(xs, s.attn, m.qw, bar, parity, err)) return;
-      matvec_dispatch<FMT>(cpl_qw, MatvecJob{L.wo, m.row_bytes_qw, m.qw, m.H, kEpiResid, s.x}, xs,
-                           blockIdx.x, nb, am);
-      if (!grid_barrier(s.bar, nb, err)) return;
-      // norm + gate/up + SwiGLU
-      if (!stage_vector(xs, s.x, m.H, bar, parity, err)) return;
-      rmsnorm_smem(xs, L.ffn_norm, m.H, m.eps, red);
-      matvec_dispatch<FMT>(cpl_h, MatvecJob{L.wgu, m.row_bytes_h, m.H, 2 * m.I, kEpiSwiGLU, s.h},
-                           xs, blockIdx.x, nb, am);
-      if (!grid_barrier(s.bar, nb, err)) return;
-      // down projection + residual
-      if (!stage_vector(xs, s.h, m.I, bar, parity, err)) return;
-      matvec_dispatch<FMT>(cpl_i, MatvecJob{L.wd, m.row_bytes_i, m.I, m.H, kEpiResid, s.x}, xs,
-                           blockIdx.x, nb, am);
-      if (!grid_barrier(s.bar, nb, err)) return;
-    }
-    if (step >= full_from) {
-      // final norm + lm_head + argmax
-      if (!stage_vector(xs, s.x, m.H, bar, parity, err)) return;
-      rmsnorm_smem(xs, m.out_norm, m.H, m.eps, red);
-      ArgmaxAcc am{-INFINITY, INT_MAX};
-      matvec_dispatch<FMT>(cpl_h, MatvecJob{m.lm_head, m.row_bytes_h, m.H, m.V, kEpiArgmax, s.logits},
-                           xs, blockIdx.x, nb, am);
-      float wv;
-      int wi;
-      if (argmax_blocks(am, blockIdx.x, nb, s.amax_v, s.amax_i, s.amax_count, red, &wv, &wi)) {
-        if (threadIdx.x == 0) finish_step(s, pos, wi, m.max_seq);
-      }
-    } else if (blockIdx.x == 0 && threadIdx.x == 0) {
-      s.state->pos = pos + 1;
-      s.state->steps += 1;
-    }
-    if (!grid_barrier(s.bar, nb, err)) return;
-  }
-}
-
-int persistent_blocks_per_sm(int fmt) {
-  int n = 0;
-  const void* fn = fmt == kFmtQ8 ? reinterpret_cast<const void*>(&k_persistent<kFmtQ8>)
-                                 : reinterpret_cast<const void*>(&k_persistent<kFmtBF16>);
-  // smem is set per launch; the kernel needs well under the default limit
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kPersistThreads, 48 * 1024) !=
-      cudaSuccess)
-    return 0;
-  return n;
-}
-
-cudaError_t launch_persistent(const DevModel& m, const DevSeq& s, int n_steps, int full_from,
-                              int blocks, cudaStream_t st) {
-  void* params[] = {const_cast<DevModel*>(&m), const_cast<DevSeq*>(&s), &n_steps, &full_from};
-  const void* fn = m.wtype == kFmtQ8 ? reinterpret_cast<const void*>(&k_persistent<kFmtQ8>)
-                                     : reinterpret_cast<const void*>(&k_persistent<kFmtBF16>);
-  const size_t smem = persistent_smem_bytes(m);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  return launch_ex(fn, dim3(blocks), dim3(kPersistThreads), smem, st, false, true, params);
 }
 
 // ---------------------------------------------------------------------------
@@ -557,7 +391,8 @@ cudaError_t launch_op_attention(const float* q, const float* K, const float* V, 
   a.rope = nullptr;
   a.kc = const_cast<float*>(K);
   a.vc = const_cast<float*>(V);
-  a.kvw = nkv * hd;
+  a.head_stride = static_cast<size_t>(hd);  // K, V given as [S][n_kv * hd]
+  a.row_stride = static_cast<size_t>(nkv) * hd;
   a.S = S;
   a.nq = nq;
   a.nkv = nkv;

@@ -1,0 +1,977 @@
+// Persistent schedule: one cooperative launch runs whole decode steps (one
+// tqd_decode_step, a chain of tqd_generate steps, or a prefill), one block per
+// SM.  Sixteen consumer warps compute; one producer warp streams every byte
+// of weights and cached K/V the block will need — its static slice of every
+// phase of every layer — through a ring of shared-memory slots with 1-D bulk
+// copies (TMA), running ahead of the consumers across phase and layer
+// boundaries.  Weights never depend on activations, so the HBM stream keeps
+// flowing while the consumers wait at the grid barriers between dependent
+// phases.  Phases and op order follow the inferno.rs blog, "IV.4: One
+// command buffer per token", section "One command buffer".
+//
+// Synchronisation: a monotonic 64-bit arrival counter (release add, acquire
+// poll) between dependent phases; mbarriers for the ring; every wait is
+// bounded by %globaltimer and reports through the error word instead of
+// hanging.
+#include <climits>
+
+#include "tqd_internal.h"
+#include "tqd_phases.cuh"
+
+namespace tqd {
+namespace {
+
+constexpr int kCW = 15;                 // consumer warps (16 warps per block with the producer:
+                                        // four per SM sub-partition, up to 128 registers each)
+constexpr int kCT = kCW * 32;           // consumer threads
+constexpr int kThreads = kCT + 32;      // + the producer warp
+constexpr uint32_t kSlotBytes = 44 * 1024;
+constexpr int kSlots = 4;
+constexpr int kPartFloats = 320;        // per-task partial sums of one ring piece
+constexpr int kRedFloats = 64 + 2 * kPartFloats;
+constexpr int kMaxGain = 4;             // norm gains held per thread (H <= 4 * kCT)
+
+// ---------------------------------------------------------------- layout
+struct PLayout {
+  uint32_t ring, xraw, xin, scratch, red, bars, total;
+};
+
+__host__ __device__ inline uint32_t a16(uint32_t v) { return (v + 15u) & ~15u; }
+
+__host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
+
+// Elements per 16-byte weight chunk, and the padded shared-memory stride of
+// one chunk's x values (chunk c of lane c % 32: conflict-free 128-bit reads).
+__host__ __device__ inline int epc_of(int fmt) { return fmt == kFmtQ8 ? 16 : 8; }
+__host__ __device__ inline int xstride_of(int fmt) { return fmt == kFmtQ8 ? 20 : 12; }
+
+__host__ __device__ inline PLayout playout(const DevModel& m) {
+  PLayout L;
+  uint32_t off = 0;
+  L.ring = off;
+  off += kSlots * kSlotBytes;
+  L.xraw = off;
+  off += a16(4u * m.H);
+  const int kmax = imax(m.H, imax(m.qw, m.I));
+  L.xin = off;
+  off += a16(4u * (kmax / epc_of(m.wtype)) * xstride_of(m.wtype));
+  const int G = m.nq / m.nkv;
+  const int attn = G * m.hd + 2 * m.hd + imax(G * m.n_chunks * (m.hd + 2), kCW * G * (m.hd + 2));
+  L.scratch = off;
+  off += a16(4u * imax(imax(m.qw, m.I), attn));
+  L.red = off;
+  off += 4u * kRedFloats;
+  L.bars = off;
+  off += 8u * (2 * kSlots);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------- sync helpers
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory"); }
+
+// OR of a predicate over the consumer threads (uniform result).
+__device__ __forceinline__ bool csync_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "n"(kCT)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// mbarrier wait that gives up after kWaitLimitNs or as soon as another thread
+// has reported an error.
+__device__ __forceinline__ bool mwait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 63u) == 0) {
+      if (ld_volatile_u32(err) != 0) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(err, kErrMbarrier);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid barrier, split: every block arrives once per phase; a wait for epoch e
+// returns once all blocks have arrived e times in total.
+__device__ __forceinline__ void gb_arrive(DevBarrier* b) {
+  csync();
+  if (threadIdx.x == 0) red_release_add_u64(&b->count, 1ull);
+}
+
+// Returns false on every consumer thread if the wait failed (timeout or an
+// error reported elsewhere).
+__device__ __forceinline__ bool gb_wait(DevBarrier* b, unsigned long long target, uint32_t* err) {
+  bool fail = false;
+  if (threadIdx.x == 0) {
+    if (ld_acquire_u64(&b->count) < target) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_u64(&b->count) < target) {
+        if (ld_volatile_u32(err) != 0) {
+          fail = true;
+          break;
+        }
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(err, kErrGridBarrier);
+          fail = true;
+          break;
+        }
+      }
+    }
+  }
+  return !csync_or(fail);
+}
+
+// ---------------------------------------------------------------- f32x2
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// 16 Q8_0 quants (one 16-byte chunk) against 16 x values: sum q_j x_j.
+__device__ __forceinline__ float dot16_q8(uint4 w, const float4* x) {
+  const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t t = wv[k] ^ 0x80808080u;
+    float2 q01 = make_float2(__uint_as_float(__byte_perm(t, 0x4B000000u, 0x7640)),
+                             __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7641)));
+    float2 q23 = make_float2(__uint_as_float(__byte_perm(t, 0x4B000000u, 0x7642)),
+                             __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7643)));
+    q01 = fadd2(q01, bias);
+    q23 = fadd2(q23, bias);
+    const float4 xv = x[k];
+    a0 = ffma2(q01, make_float2(xv.x, xv.y), a0);
+    a1 = ffma2(q23, make_float2(xv.z, xv.w), a1);
+  }
+  return (a0.x + a0.y) + (a1.x + a1.y);
+}
+
+// 8 bf16 weights (one 16-byte chunk) against 8 x values.
+__device__ __forceinline__ float dot8_bf16(uint4 w, const float4* x) {
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  const float4 x0 = x[0], x1 = x[1];
+  a0 = ffma2(make_float2(bf16_lo(w.x), bf16_hi(w.x)), make_float2(x0.x, x0.y), a0);
+  a1 = ffma2(make_float2(bf16_lo(w.y), bf16_hi(w.y)), make_float2(x0.z, x0.w), a1);
+  a0 = ffma2(make_float2(bf16_lo(w.z), bf16_hi(w.z)), make_float2(x1.x, x1.y), a0);
+  a1 = ffma2(make_float2(bf16_lo(w.w), bf16_hi(w.w)), make_float2(x1.z, x1.w), a1);
+  return (a0.x + a0.y) + (a1.x + a1.y);
+}
+
+// ---------------------------------------------------------------- the ring
+struct Ring {
+  uint8_t* base;
+  uint64_t* full;
+  uint64_t* empty;
+  uint32_t n;  // pieces issued (producer) or consumed (consumers)
+};
+
+__device__ __forceinline__ uint8_t* slot_ptr(const Ring& r) {
+  return r.base + (r.n % kSlots) * kSlotBytes;
+}
+
+// Rows of a matrix a block owns in a phase: units of `align` rows split evenly.
+__device__ __forceinline__ void block_rows(int rows, int align, int b, int nb, int& r0, int& r1) {
+  const int units = rows / align;
+  r0 = static_cast<int>(static_cast<long long>(units) * b / nb) * align;
+  r1 = static_cast<int>(static_cast<long long>(units) * (b + 1) / nb) * align;
+}
+
+// Rows per ring piece: a multiple of 2 * kCW rows (one pair per consumer
+// warp) when that fits a slot, else the largest even count; at most 240.
+__device__ __forceinline__ int rows_per_piece(size_t rb) {
+  int r = static_cast<int>(kSlotBytes / rb);
+  if (r > 240) r = 240;
+  if (r >= 2 * kCW) return r / (2 * kCW) * (2 * kCW);
+  return r & ~1;
+}
+
+// K/V rows per attention piece (K rows then V rows in one slot).
+__device__ __forceinline__ int kv_rows_per_piece(int hd) {
+  return static_cast<int>(kSlotBytes / (2u * 4u * hd));
+}
+
+// The chunk [t0, t1) of positions item chunk c covers when S rows are live.
+__device__ __forceinline__ void chunk_range(int S, int n_chunks, int c, int& t0, int& t1) {
+  const int cs = (S + n_chunks - 1) / n_chunks;
+  t0 = min(S, c * cs);
+  t1 = min(S, t0 + cs);
+}
+
+// ---------------------------------------------------------------- producer
+struct Producer {
+  Ring r;
+  uint32_t* err;
+  bool ok;
+
+  __device__ bool acquire() {
+    const uint32_t slot = r.n % kSlots, use = r.n / kSlots;
+    if (use > 0 && !mwait(r.empty + slot, (use - 1) & 1u, err)) ok = false;
+    return ok;
+  }
+  __device__ void rows(const uint8_t* W, size_t rb, int r0, int r1) {
+    const int rpp = rows_per_piece(rb);
+    for (int a = r0; a < r1 && ok; a += rpp) {
+      const int n = min(rpp, r1 - a);
+      if (!acquire()) return;
+      const uint32_t bytes = static_cast<uint32_t>(n * rb);
+      uint64_t* fb = r.full + r.n % kSlots;
+      mbar_arrive_expect_tx(fb, bytes);
+      bulk_g2s(slot_ptr(r), W + static_cast<size_t>(a) * rb, bytes, fb);
+      ++r.n;
+    }
+  }
+  __device__ void kv(const float* kc, const float* vc, int hd, int t0, int t1) {
+    const int rpp = kv_rows_per_piece(hd);
+    for (int a = t0; a < t1 && ok; a += rpp) {
+      const int n = min(rpp, t1 - a);
+      if (!acquire()) return;
+      const uint32_t bytes = static_cast<uint32_t>(n) * hd * 4u;
+      uint64_t* fb = r.full + r.n % kSlots;
+      uint8_t* dst = slot_ptr(r);
+      mbar_arrive_expect_tx(fb, 2u * bytes);
+      bulk_g2s(dst, kc + static_cast<size_t>(a) * hd, bytes, fb);
+      bulk_g2s(dst + static_cast<size_t>(rpp) * hd * 4u, vc + static_cast<size_t>(a) * hd, bytes, fb);
+      ++r.n;
+    }
+  }
+  // Wait until every issued copy has landed (used when stopping early).
+  __device__ void drain() {
+    for (uint32_t k = 0; k < kSlots && k < r.n; ++k) {
+      const uint32_t q = r.n - 1 - k;
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(r.full + q % kSlots, (q / kSlots) & 1u))
+        if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+};
+
+__device__ void run_producer(const DevModel& m, const DevSeq& s, int n_steps, int full_from,
+                             uint32_t pos0, Ring ring) {
+  Producer P{ring, &s.state->err, true};
+  const int b = blockIdx.x, nb = gridDim.x;
+  const int n_items = m.nkv * m.n_chunks;
+  const int rows_qkv = m.qw + 2 * m.kvw;
+  int q0, q1, o0, o1, g0, g1, d0, d1, v0, v1;
+  block_rows(rows_qkv, 1, b, nb, q0, q1);
+  block_rows(m.H, 1, b, nb, o0, o1);
+  block_rows(2 * m.I, 2, b, nb, g0, g1);
+  block_rows(m.H, 1, b, nb, d0, d1);
+  block_rows(m.V, 1, b, nb, v0, v1);
+  for (int step = 0; step < n_steps && P.ok; ++step) {
+    const int pos = static_cast<int>(pos0) + step;
+    if (pos >= m.max_seq) break;
+    for (int l = 0; l < m.n_layers && P.ok; ++l) {
+      const DevLayer& L = m.layers[l];
+      P.rows(L.wqkv, m.row_bytes_h, q0, q1);
+      const size_t lay = static_cast<size_t>(l) * m.nkv * m.max_seq * m.hd;
+      for (int item = b; item < n_items; item += nb) {
+        const int g = item / m.n_chunks, c = item - g * m.n_chunks;
+        int t0, t1;
+        chunk_range(pos + 1, m.n_chunks, c, t0, t1);
+        const size_t head = lay + static_cast<size_t>(g) * m.max_seq * m.hd;
+        P.kv(s.kcache + head, s.vcache + head, m.hd, t0, min(t1, pos));
+      }
+      P.rows(L.wo, m.row_bytes_qw, o0, o1);
+      P.rows(L.wgu, m.row_bytes_h, g0, g1);
+      P.rows(L.wd, m.row_bytes_i, d0, d1);
+    }
+    if (step >= full_from) P.rows(m.lm_head, m.row_bytes_h, v0, v1);
+  }
+  if (!P.ok) P.drain();
+}
+
+// ---------------------------------------------------------------- consumers
+struct Cons {
+  const DevModel& m;
+  const DevSeq& s;
+  Ring r;
+  float* xraw;     // [H] plain vector (residual input of the phase)
+  float* xin;      // matvec input in the padded chunk layout
+  float* scr;      // staging / attention scratch
+  float* red;      // reductions and per-task partial sums
+  uint32_t rsel;   // alternating halves of the reduction scratch
+  uint32_t psel;   // alternating partial-sum buffers of mv_phase
+  uint32_t* err;
+  int fmt;
+  __device__ Cons(const DevModel& m_, const DevSeq& s_) : m(m_), s(s_) {}
+};
+
+// Stage n floats of global memory (written by other blocks before the last
+// grid barrier) into shared memory with 16-byte cp.async copies.  Every stage
+// follows a consumer sync, so earlier readers of dst are done.
+__device__ __forceinline__ void stage(Cons& C, float* dst, const float* src, int n) {
+  (void)C;
+  for (int i = threadIdx.x; i < n / 4; i += kCT)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst + 4 * i)),
+                 "l"(src + 4 * i)
+                 : "memory");
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+  csync();
+}
+
+__device__ __forceinline__ int xpad(int fmt, int e) {
+  return fmt == kFmtQ8 ? 20 * (e >> 4) + (e & 15) : 12 * (e >> 3) + (e & 7);
+}
+
+// Sum over the consumer threads with one sync (the scratch alternates halves).
+__device__ __forceinline__ float block_sum_c(Cons& C, float v) {
+  float* red = C.red + 16 * C.rsel;
+  C.rsel ^= 1u;
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  csync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCW; ++w) t += red[w];
+  return t;
+}
+
+// Norm gains a thread needs, loaded before the barrier wait (they are
+// constants, so their latency stays off the critical path).
+struct Gain {
+  float v[kMaxGain];
+};
+__device__ __forceinline__ void load_gain(Gain& g, const float* src, int K) {
+#pragma unroll
+  for (int j = 0; j < kMaxGain; ++j) {
+    const int i = threadIdx.x + kCT * j;
+    g.v[j] = i < K ? __ldg(src + i) : 0.f;
+  }
+}
+
+// xin <- padded(src * rsqrt(mean(src^2) + eps) * g)   ("Eight kernels",
+// rms_norm_row).
+__device__ __forceinline__ void to_xin_norm(Cons& C, const float* src, int K, const Gain& g) {
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxGain; ++j) {
+    const int i = threadIdx.x + kCT * j;
+    if (i < K) ss = fmaf(src[i], src[i], ss);
+  }
+  ss = block_sum_c(C, ss);
+  const float inv = rsqrtf(ss / static_cast<float>(K) + C.m.eps);
+#pragma unroll
+  for (int j = 0; j < kMaxGain; ++j) {
+    const int i = threadIdx.x + kCT * j;
+    if (i < K) C.xin[xpad(C.fmt, i)] = src[i] * inv * g.v[j];
+  }
+  csync();
+}
+
+// xin <- padded(src)
+__device__ __forceinline__ void to_xin(Cons& C, const float* src, int K) {
+  for (int i = threadIdx.x; i < K; i += kCT) C.xin[xpad(C.fmt, i)] = src[i];
+  csync();
+}
+
+struct MvOut {
+  int epi;
+  float* y;           // kEpiStore / kEpiArgmax: y[r]; kEpiSwiGLU: y[r/2]; kEpiResid: y[r]
+  const float* res;   // kEpiResid: residual source (shared memory), indexed by r
+  float bv;           // running argmax (kEpiArgmax), per epilogue thread
+  int bi;
+};
+
+// One phase of matvec rows [r0, r1) streamed through the ring.  Work in a
+// piece is split into tasks of (row pair, K segment); task partial sums go
+// through shared memory and one thread per row applies the epilogue.
+template <int FMT>
+__device__ void mv_phase(Cons& C, size_t rb, int K, int r0, int r1, MvOut& o) {
+  constexpr int EPC = FMT == kFmtQ8 ? 16 : 8;
+  constexpr int XS = FMT == kFmtQ8 ? 20 : 12;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nchunks = K / EPC;
+  const int iters = (nchunks + 31) / 32;  // chunk rounds per lane
+  const int rpp = rows_per_piece(rb);
+  for (int a = r0; a < r1; a += rpp) {
+    float* part = C.red + 64 + kPartFloats * C.psel;  // [tasks][2]
+    C.psel ^= 1u;
+    const int n = min(rpp, r1 - a);
+    const int pairs = (n + 1) >> 1;
+    int nseg = kCW / pairs;
+    if (nseg < 1) nseg = 1;
+    if (nseg > iters) nseg = iters;
+    const int tasks = pairs * nseg;
+    uint64_t* fb = C.r.full + C.r.n % kSlots;
+    mwait(fb, (C.r.n / kSlots) & 1u, C.err);
+    const uint8_t* slot = slot_ptr(C.r);
+    for (int t = warp; t < tasks; t += kCW) {
+      const int p = t / nseg, sg = t - p * nseg;
+      const int i0 = iters * sg / nseg, i1 = iters * (sg + 1) / nseg;
+      const int ra = 2 * p, rbw = 2 * p + 1;
+      const bool has_b = rbw < n;
+      const uint8_t* wa = slot + static_cast<size_t>(ra) * rb;
+      const uint8_t* wb = slot + static_cast<size_t>(has_b ? rbw : ra) * rb;
+      float acc_a = 0.f, acc_b = 0.f;
+#pragma unroll 1
+      for (int i = i0; i < i1; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nchunks) {
+          const float4* xp = reinterpret_cast<const float4*>(C.xin + XS * c);
+          const uint4 w0 = *reinterpret_cast<const uint4*>(wa + 16 * c);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(wb + 16 * c);
+          if (FMT == kFmtQ8) {
+            const float s0 = __half2float(*reinterpret_cast<const __half*>(wa + K + 2 * (c >> 1)));
+            const float s1 = __half2float(*reinterpret_cast<const __half*>(wb + K + 2 * (c >> 1)));
+            acc_a = fmaf(s0, dot16_q8(w0, xp), acc_a);
+            acc_b = fmaf(s1, dot16_q8(w1, xp), acc_b);
+          } else {
+            acc_a += dot8_bf16(w0, xp);
+            acc_b += dot8_bf16(w1, xp);
+          }
+        }
+      }
+      acc_a = warp_sum(acc_a);
+      acc_b = warp_sum(acc_b);
+      if (lane == 0) {
+        part[2 * t] = acc_a;
+        part[2 * t + 1] = acc_b;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(C.r.empty + C.r.n % kSlots)) : "memory");
+    ++C.r.n;
+    csync();
+    // epilogue: one thread per row (SwiGLU: one per pair)
+    if (o.epi == kEpiSwiGLU) {
+      for (int p = threadIdx.x; p < pairs; p += kCT) {
+        float g = 0.f, u = 0.f;
+        for (int sg = 0; sg < nseg; ++sg) {
+          g += part[2 * (p * nseg + sg)];
+          u += part[2 * (p * nseg + sg) + 1];
+        }
+        o.y[(a >> 1) + p] = silu_mul(g, u);
+      }
+    } else {
+      for (int i = threadIdx.x; i < n; i += kCT) {
+        const int p = i >> 1, w = i & 1;
+        float v = 0.f;
+        for (int sg = 0; sg < nseg; ++sg) v += part[2 * (p * nseg + sg) + w];
+        const int row = a + i;
+        if (o.epi == kEpiResid) {
+          o.y[row] = o.res[row] + v;
+        } else {
+          o.y[row] = v;
+          if (o.epi == kEpiArgmax) argmax_merge(o.bv, o.bi, v, row);
+        }
+      }
+    }
+  }
+}
+
+// Constants of the attention phase a lane needs (QK-norm gains and the RoPE
+// (cos, sin) pairs of the current position), loaded before the barrier wait.
+struct AttnPre {
+  float qg[4], kg[4];
+  float2 cs[2];
+};
+
+__device__ __forceinline__ void load_attn_pre(AttnPre& p, const DevModel& m, const DevLayer& L,
+                                              int pos) {
+  const int lane = threadIdx.x & 31;
+  const int nj = m.hd / 32;
+  const float2* rope = m.rope + static_cast<size_t>(pos) * (m.hd / 2);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    p.qg[j] = (m.qk_norm && j < nj) ? __ldg(L.q_norm + lane + 32 * j) : 1.f;
+    p.kg[j] = (m.qk_norm && j < nj) ? __ldg(L.k_norm + lane + 32 * j) : 1.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) p.cs[j] = j < nj / 2 ? __ldg(rope + lane + 32 * j) : make_float2(1.f, 0.f);
+}
+
+// Per-head RMSNorm (optional) and half-split RoPE of one head held as
+// lane-strided elements e_j = lane + 32 j ("Eight kernels", rms_norm_row and
+// rope_row), with the gains and rotation pairs already in registers.
+template <int HD>
+__device__ __forceinline__ void norm_rope_regs(float (&v)[HD / 32], const float* g, bool norm,
+                                               const float2* cs, float eps) {
+  constexpr int NJ = HD / 32;
+  if (norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) ss = fmaf(v[j], v[j], ss);
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / static_cast<float>(HD) + eps);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) v[j] = v[j] * inv * g[j];
+  }
+#pragma unroll
+  for (int j = 0; j < NJ / 2; ++j) {
+    const float u = v[j], w = v[j + NJ / 2];
+    v[j] = u * cs[j].x - w * cs[j].y;
+    v[j + NJ / 2] = u * cs[j].y + w * cs[j].x;
+  }
+}
+
+// Attention for item (g, c): queries of kv group g against the chunk's cached
+// rows (streamed through the ring) plus the new row; online softmax; the last
+// chunk of the group to finish combines all chunks ("Eight kernels",
+// attention_decode, as a split-K flash decode).
+template <int HD, int G>
+__device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnPre& pre) {
+  constexpr int NJ = HD / 32, DPL = HD / 32;
+  const DevModel& m = C.m;
+  const DevSeq& s = C.s;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* qs = C.scr;               // [G][HD]
+  float* knew = qs + G * HD;       // [HD]
+  float* vnew = knew + HD;         // [HD]
+  float* wst = vnew + HD;          // [kCW][G][HD + 2], then the group's partials
+  const int S = pos + 1;
+  int t0, t1;
+  chunk_range(S, m.n_chunks, c, t0, t1);
+  const bool has_new = t0 <= pos && pos < t1;
+  const int tc = min(t1, pos);     // cached rows end
+  if (warp < G) {
+    const int h = g * G + warp;
+    float v[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) v[j] = __ldcg(s.qkv + h * HD + lane + 32 * j);
+    norm_rope_regs<HD>(v, pre.qg, m.qk_norm != 0, pre.cs, m.eps);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) qs[warp * HD + lane + 32 * j] = v[j];
+  } else if (warp == kCW - 1 && has_new) {
+    // the new row: QK-norm + RoPE on k, append k and v to the cache
+    // ("Eight kernels", append_kv)
+    float kv[NJ], vv[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      kv[j] = __ldcg(s.qkv + m.qw + g * HD + lane + 32 * j);
+      vv[j] = __ldcg(s.qkv + m.qw + m.kvw + g * HD + lane + 32 * j);
+    }
+    norm_rope_regs<HD>(kv, pre.kg, m.qk_norm != 0, pre.cs, m.eps);
+    const size_t row = ((static_cast<size_t>(layer) * m.nkv + g) * m.max_seq + pos) * HD;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      s.kcache[row + lane + 32 * j] = kv[j];
+      s.vcache[row + lane + 32 * j] = vv[j];
+      knew[lane + 32 * j] = kv[j];
+      vnew[lane + 32 * j] = vv[j];
+    }
+    fence_proxy_async_global();  // later bulk copies read this row
+  }
+  csync();
+  float qv[G][DPL], mm[G], ll[G], oo[G][DPL];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    mm[hh] = -INFINITY;
+    ll[hh] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      qv[hh][e] = qs[hh * HD + lane * DPL + e];
+      oo[hh][e] = 0.f;
+    }
+  }
+  auto row_update = [&](const float* kr, const float* vr) {
+    float kf[DPL], vf[DPL];
+    if constexpr (DPL == 4) {
+      const float4 k4 = *reinterpret_cast<const float4*>(kr + lane * 4);
+      const float4 v4 = *reinterpret_cast<const float4*>(vr + lane * 4);
+      kf[0] = k4.x; kf[1] = k4.y; kf[2] = k4.z; kf[3] = k4.w;
+      vf[0] = v4.x; vf[1] = v4.y; vf[2] = v4.z; vf[3] = v4.w;
+    } else {
+      const float2 k2 = *reinterpret_cast<const float2*>(kr + lane * 2);
+      const float2 v2 = *reinterpret_cast<const float2*>(vr + lane * 2);
+      kf[0] = k2.x; kf[1] = k2.y;
+      vf[0] = v2.x; vf[1] = v2.y;
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) d = fmaf(qv[hh][e], kf[e], d);
+      const float sc = warp_sum(d) * m.attn_scale;
+      if (sc > mm[hh]) {
+        const float corr = expf(mm[hh] - sc);
+        mm[hh] = sc;
+        ll[hh] = ll[hh] * corr + 1.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) oo[hh][e] = fmaf(oo[hh][e], corr, vf[e]);
+      } else {
+        const float p = expf(sc - mm[hh]);
+        ll[hh] += p;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) oo[hh][e] = fmaf(p, vf[e], oo[hh][e]);
+      }
+    }
+  };
+  const int rpp = kv_rows_per_piece(HD);
+  for (int a = t0; a < tc; a += rpp) {
+    const int n = min(rpp, tc - a);
+    mwait(C.r.full + C.r.n % kSlots, (C.r.n / kSlots) & 1u, C.err);
+    const float* Ks = reinterpret_cast<const float*>(slot_ptr(C.r));
+    const float* Vs = Ks + static_cast<size_t>(rpp) * HD;
+    for (int t = warp; t < n; t += kCW) row_update(Ks + t * HD, Vs + t * HD);
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(C.r.empty + C.r.n % kSlots)) : "memory");
+    ++C.r.n;
+  }
+  if (has_new && warp == ((tc - t0) % kCW)) row_update(knew, vnew);
+  // merge the warps' states
+  const int stride = HD + 2;
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    float* w = wst + (warp * G + hh) * stride;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) w[lane * DPL + e] = oo[hh][e];
+    if (lane == 0) {
+      w[HD] = mm[hh];
+      w[HD + 1] = ll[hh];
+    }
+  }
+  csync();
+  for (int idx = threadIdx.x; idx < G * HD; idx += kCT) {
+    const int hh = idx / HD, d = idx - hh * HD;
+    float M = -INFINITY;
+    for (int w = 0; w < kCW; ++w) M = fmaxf(M, wst[(w * G + hh) * stride + HD]);
+    float O = 0.f, Lsum = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kCW; ++w) {
+        const float* ws = wst + (w * G + hh) * stride;
+        const float f = expf(ws[HD] - M);
+        O = fmaf(f, ws[d], O);
+        Lsum = fmaf(f, ws[HD + 1], Lsum);
+      }
+    }
+    const int h = g * G + hh;
+    s.part_o[(static_cast<size_t>(h) * m.n_chunks + c) * HD + d] = O;
+    if (d == 0) {
+      s.part_ml[(static_cast<size_t>(h) * m.n_chunks + c) * 2] = M;
+      s.part_ml[(static_cast<size_t>(h) * m.n_chunks + c) * 2 + 1] = Lsum;
+    }
+  }
+  csync();
+  __shared__ uint32_t s_last;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t old = atomicAdd(s.attn_count + g, 1u);
+    s_last = old == static_cast<uint32_t>(m.n_chunks) - 1u;
+    if (s_last) __threadfence();
+  }
+  csync();
+  if (!s_last) return;
+  // combine: stage the group's partials, then one output per (head, dim)
+  const int NC = m.n_chunks;
+  float* po = wst;                        // [G][NC][HD]
+  float* pml = po + G * NC * HD;          // [G][NC][2]
+  const float4* src_o = reinterpret_cast<const float4*>(s.part_o + static_cast<size_t>(g) * G * NC * HD);
+  for (int i = threadIdx.x; i < G * NC * HD / 4; i += kCT)
+    reinterpret_cast<float4*>(po)[i] = __ldcg(src_o + i);
+  const float* src_ml = s.part_ml + static_cast<size_t>(g) * G * NC * 2;
+  for (int i = threadIdx.x; i < G * NC * 2; i += kCT) pml[i] = __ldcg(src_ml + i);
+  csync();
+  for (int idx = threadIdx.x; idx < G * HD; idx += kCT) {
+    const int hh = idx / HD, d = idx - hh * HD;
+    float M = -INFINITY;
+    for (int cc = 0; cc < NC; ++cc) M = fmaxf(M, pml[(hh * NC + cc) * 2]);
+    float num = 0.f, den = 0.f;
+    for (int cc = 0; cc < NC; ++cc) {
+      const float mc = pml[(hh * NC + cc) * 2];
+      if (mc == -INFINITY) continue;
+      const float f = expf(mc - M);
+      num = fmaf(f, po[(hh * NC + cc) * HD + d], num);
+      den = fmaf(f, pml[(hh * NC + cc) * 2 + 1], den);
+    }
+    s.attn[(g * G + hh) * HD + d] = num / den;
+  }
+  if (threadIdx.x == 0) s.attn_count[g] = 0u;
+}
+
+template <int HD>
+__device__ __forceinline__ void attn_dispatch_g(Cons& C, int G, int layer, int g, int c, int pos,
+                                                const AttnPre& pre) {
+  switch (G) {
+    case 1: attn_item<HD, 1>(C, layer, g, c, pos, pre); break;
+    case 2: attn_item<HD, 2>(C, layer, g, c, pos, pre); break;
+    case 3: attn_item<HD, 3>(C, layer, g, c, pos, pre); break;
+    default: attn_item<HD, 4>(C, layer, g, c, pos, pre); break;
+  }
+}
+
+template <int FMT>
+__device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0) {
+  const DevModel& m = C.m;
+  const DevSeq& s = C.s;
+  const int b = blockIdx.x, nb = gridDim.x;
+  DevBarrier* bar = s.bar;
+  unsigned long long epoch = s.bar->epoch;  // barriers completed before this launch
+  const int n_items = m.nkv * m.n_chunks;
+  const int G = m.nq / m.nkv;
+  int q0, q1, o0, o1, g0, g1, d0, d1, v0, v1;
+  block_rows(m.qw + 2 * m.kvw, 1, b, nb, q0, q1);
+  block_rows(m.H, 1, b, nb, o0, o1);
+  block_rows(2 * m.I, 2, b, nb, g0, g1);
+  block_rows(m.H, 1, b, nb, d0, d1);
+  block_rows(m.V, 1, b, nb, v0, v1);
+  auto arrive = [&]() {
+    gb_arrive(bar);
+    ++epoch;
+  };
+  auto wait = [&]() { return gb_wait(bar, epoch * static_cast<unsigned long long>(nb), C.err); };
+  for (int step = 0; step < n_steps; ++step) {
+    const uint32_t pos = pos0 + step;
+    if (pos >= static_cast<uint32_t>(m.max_seq)) {
+      if (b == 0 && threadIdx.x == 0) atomicOr(C.err, kErrCapacity);
+      break;
+    }
+    if (step > 0 && !wait()) return;  // the previous step's token is written
+    int tok = __ldcg(s.tokens + pos);
+    if (tok < 0 || tok >= m.V) {
+      if (threadIdx.x == 0) atomicOr(C.err, kErrBadToken);
+      tok = 0;
+    }
+    for (int l = 0; l < m.n_layers; ++l) {
+      const DevLayer L = m.layers[l];  // pointers read before any wait
+      MvOut o{};
+      Gain gain;
+      load_gain(gain, L.attn_norm, m.H);
+      // ---- RMSNorm + QKV ----
+      if (l == 0) {
+        csync();
+        if (FMT == kFmtQ8) {
+          const uint8_t* row = m.embed + static_cast<size_t>(tok) * m.row_bytes_h;
+          const __half* sc = reinterpret_cast<const __half*>(row + m.H);
+          for (int i = threadIdx.x; i < m.H; i += kCT)
+            C.xraw[i] = __half2float(sc[i >> 5]) * static_cast<float>(static_cast<int8_t>(row[i]));
+        } else {
+          const uint16_t* row = reinterpret_cast<const uint16_t*>(m.embed + static_cast<size_t>(tok) * m.row_bytes_h);
+          for (int i = threadIdx.x; i < m.H; i += kCT) C.xraw[i] = __uint_as_float(static_cast<uint32_t>(row[i]) << 16);
+        }
+        csync();
+      } else {
+        if (!wait()) return;
+        stage(C, C.xraw, s.x, m.H);
+      }
+      to_xin_norm(C, C.xraw, m.H, gain);
+      o.epi = kEpiStore;
+      o.y = s.qkv;
+      mv_phase<FMT>(C, m.row_bytes_h, m.H, q0, q1, o);
+      arrive();
+      // ---- QK-norm + RoPE + append + attention ----
+      AttnPre pre;
+      load_attn_pre(pre, m, L, static_cast<int>(pos));
+      if (!wait()) return;
+      for (int item = b; item < n_items; item += nb) {
+        const int g = item / m.n_chunks, c = item - g * m.n_chunks;
+        if (m.hd == 128) attn_dispatch_g<128>(C, G, l, g, c, pos, pre);
+        else attn_dispatch_g<64>(C, G, l, g, c, pos, pre);
+        csync();
+      }
+      arrive();
+      // ---- O projection + residual ----
+      load_gain(gain, L.ffn_norm, m.H);  // for the next phase
+      if (!wait()) return;
+      stage(C, C.scr, s.attn, m.qw);
+      to_xin(C, C.scr, m.qw);
+      o.epi = kEpiResid;
+      o.y = s.x_mid;
+      o.res = C.xraw;
+      mv_phase<FMT>(C, m.row_bytes_qw, m.qw, o0, o1, o);
+      arrive();
+      // ---- RMSNorm + gate/up + SwiGLU ----
+      if (!wait()) return;
+      stage(C, C.xraw, s.x_mid, m.H);
+      to_xin_norm(C, C.xraw, m.H, gain);
+      o.epi = kEpiSwiGLU;
+      o.y = s.h;
+      mv_phase<FMT>(C, m.row_bytes_h, m.H, g0, g1, o);
+      arrive();
+      // ---- down projection + residual ----
+      if (!wait()) return;
+      stage(C, C.scr, s.h, m.I);
+      to_xin(C, C.scr, m.I);
+      o.epi = kEpiResid;
+      o.y = s.x;
+      o.res = C.xraw;
+      mv_phase<FMT>(C, m.row_bytes_i, m.I, d0, d1, o);
+      arrive();
+    }
+    if (step >= full_from) {
+      // ---- final RMSNorm + lm_head + argmax ----
+      Gain gain;
+      load_gain(gain, m.out_norm, m.H);
+      if (!wait()) return;
+      stage(C, C.xraw, s.x, m.H);
+      to_xin_norm(C, C.xraw, m.H, gain);
+      MvOut o{};
+      o.epi = kEpiArgmax;
+      o.y = s.logits;
+      o.bv = -INFINITY;
+      o.bi = INT_MAX;
+      mv_phase<FMT>(C, m.row_bytes_h, m.H, v0, v1, o);
+      // block candidate -> global candidates -> the last block picks the winner
+      warp_argmax(o.bv, o.bi);
+      int* redi = reinterpret_cast<int*>(C.red + 32);
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      if (lane == 0) {
+        C.red[warp] = o.bv;
+        redi[warp] = o.bi;
+      }
+      csync();
+      __shared__ uint32_t s_last;
+      if (threadIdx.x == 0) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int w = 0; w < kCW; ++w) argmax_merge(bv, bi, C.red[w], redi[w]);
+        s.amax_v[b] = bv;
+        s.amax_i[b] = bi;
+        __threadfence();
+        const uint32_t old = atomicAdd(s.amax_count, 1u);
+        s_last = old == static_cast<uint32_t>(nb) - 1u;
+        if (s_last) __threadfence();
+      }
+      csync();
+      if (s_last) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int k = threadIdx.x; k < nb; k += kCT) argmax_merge(bv, bi, __ldcg(s.amax_v + k), __ldcg(s.amax_i + k));
+        warp_argmax(bv, bi);
+        if (lane == 0) {
+          C.red[warp] = bv;
+          redi[warp] = bi;
+        }
+        csync();
+        if (threadIdx.x == 0) {
+          float v = -INFINITY;
+          int i = INT_MAX;
+          for (int w = 0; w < kCW; ++w) argmax_merge(v, i, C.red[w], redi[w]);
+          int next = i;
+          if (i == INT_MAX) {
+            atomicOr(C.err, kErrAllNaN);
+            next = -1;
+          }
+          if (pos + 1 <= static_cast<uint32_t>(m.max_seq)) s.tokens[pos + 1] = next;
+          s.state->pos = pos + 1;
+          s.state->steps += 1;
+          *s.amax_count = 0u;
+        }
+      }
+      arrive();
+    } else if (b == 0 && threadIdx.x == 0) {
+      s.state->pos = pos + 1;
+      s.state->steps += 1;
+    }
+  }
+  if (b == 0 && threadIdx.x == 0) s.bar->epoch = epoch;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_persist(DevModel m, DevSeq s, int n_steps, int full_from) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  const PLayout L = playout(m);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  uint64_t* empty = full + kSlots;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kCW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint32_t pos0 = __ldcg(&s.state->pos);
+  Ring ring{sm + L.ring, full, empty, 0};
+  if (threadIdx.x >= kCT) {
+    if (threadIdx.x == kCT) run_producer(m, s, n_steps, full_from, pos0, ring);
+    return;
+  }
+  Cons C(m, s);
+  C.r = ring;
+  C.xraw = reinterpret_cast<float*>(sm + L.xraw);
+  C.xin = reinterpret_cast<float*>(sm + L.xin);
+  C.scr = reinterpret_cast<float*>(sm + L.scratch);
+  C.red = reinterpret_cast<float*>(sm + L.red);
+  C.rsel = 0;
+  C.psel = 0;
+  C.err = &s.state->err;
+  C.fmt = FMT;
+  run_consumers<FMT>(C, n_steps, full_from, pos0);
+}
+
+const void* persist_fn(int fmt) {
+  return fmt == kFmtQ8 ? reinterpret_cast<const void*>(&k_persist<kFmtQ8>)
+                       : reinterpret_cast<const void*>(&k_persist<kFmtBF16>);
+}
+
+}  // namespace
+
+size_t persistent_smem_bytes(const DevModel& m) { return playout(m).total; }
+
+bool persistent_supported(const DevModel& m) {
+  const int G = m.nq / m.nkv;
+  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && m.H <= kMaxGain * kCT;
+}
+
+int persistent_blocks_per_sm(const DevModel& m) {
+  if (!persistent_supported(m)) return 0;
+  const void* fn = persist_fn(m.wtype);
+  const size_t smem = persistent_smem_bytes(m);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_persistent(const DevModel& m, const DevSeq& s, int n_steps, int full_from,
+                              int blocks, cudaStream_t st) {
+  void* params[] = {const_cast<DevModel*>(&m), const_cast<DevSeq*>(&s), &n_steps, &full_from};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = persistent_smem_bytes(m);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, persist_fn(m.wtype), params);
+}
+
+}  // namespace tqd

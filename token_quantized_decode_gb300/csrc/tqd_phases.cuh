@@ -274,9 +274,10 @@ struct AttnJob {
   const float* q_norm;   // [HD] or nullptr
   const float* k_norm;
   const float2* rope;    // (cos, sin) row of the current position, or nullptr
-  float* kc;             // [>= S][kvw] keys of this layer (post-RoPE)
-  float* vc;
-  int kvw, S, nq, nkv, n_chunks;
+  float* kc;             // keys of this layer (post-RoPE): row t of kv head g at
+  float* vc;             //   kc + g * head_stride + t * row_stride
+  size_t head_stride, row_stride;
+  int S, nq, nkv, n_chunks;
   float eps, scale;
   float* part_o;         // [nq][n_chunks][HD]
   float* part_ml;        // [nq][n_chunks][2]
@@ -350,8 +351,8 @@ __device__ void attention_item(const AttnJob& a, int g, int c, float* smem, uint
       vv[j] = ld_cg(a.v_new + g * HD + lane + 32 * j);
     }
     head_norm_rope<HD>(kv, a.k_norm, a.rope, a.eps);
-    float* krow = a.kc + static_cast<size_t>(pos) * a.kvw + g * HD;
-    float* vrow = a.vc + static_cast<size_t>(pos) * a.kvw + g * HD;
+    float* krow = a.kc + g * a.head_stride + static_cast<size_t>(pos) * a.row_stride;
+    float* vrow = a.vc + g * a.head_stride + static_cast<size_t>(pos) * a.row_stride;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       krow[lane + 32 * j] = kv[j];
@@ -376,8 +377,8 @@ __device__ void attention_item(const AttnJob& a, int g, int c, float* smem, uint
     for (int d = 0; d < DPL; ++d) qv[hh][d] = qs[hh * HD + lane * DPL + d];
 
   for (int t = t0 + warp; t < t1; t += nw) {
-    const float* krow = a.kc + static_cast<size_t>(t) * a.kvw + g * HD + lane * DPL;
-    const float* vrow = a.vc + static_cast<size_t>(t) * a.kvw + g * HD + lane * DPL;
+    const float* krow = a.kc + g * a.head_stride + static_cast<size_t>(t) * a.row_stride + lane * DPL;
+    const float* vrow = a.vc + g * a.head_stride + static_cast<size_t>(t) * a.row_stride + lane * DPL;
     float kf[DPL], vf[DPL];
     if constexpr (DPL == 4) {
       const float4 k4 = ld_cg4(reinterpret_cast<const float4*>(krow));
