@@ -355,19 +355,6 @@ __device__ __forceinline__ int xpad(int fmt, int e) {
   return fmt == kFmtQ8 ? 20 * (e >> 4) + (e & 15) : 12 * (e >> 3) + (e & 7);
 }
 
-// Sum over the consumer threads with one sync (the scratch alternates halves).
-__device__ __forceinline__ float block_sum_c(Cons& C, float v) {
-  float* red = C.red + 16 * C.rsel;
-  C.rsel ^= 1u;
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  csync();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < kCW; ++w) t += red[w];
-  return t;
-}
-
 // Norm gains a thread needs, loaded before the barrier wait (they are
 // constants, so their latency stays off the critical path).
 struct Gain {
@@ -381,28 +368,39 @@ __device__ __forceinline__ void load_gain(Gain& g, const float* src, int K) {
   }
 }
 
-// xin <- padded(src * rsqrt(mean(src^2) + eps) * g)   ("Eight kernels",
-// rms_norm_row).
-__device__ __forceinline__ void to_xin_norm(Cons& C, const float* src, int K, const Gain& g) {
+// RMSNorm folded into the following matvec ("Eight kernels", rms_norm_row):
+// xin <- padded(src (.) g), and the returned factor 1/sqrt(mean(src^2) + eps)
+// scales every dot product, since W (x/rms (.) g) = (W (x (.) g)) / rms.
+__device__ __forceinline__ float to_xin_norm(Cons& C, const float* src, int K, const Gain& g) {
+  float* red = C.red + 16 * C.rsel;
+  C.rsel ^= 1u;
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxGain; ++j) {
     const int i = threadIdx.x + kCT * j;
-    if (i < K) ss = fmaf(src[i], src[i], ss);
+    if (i < K) {
+      const float v = src[i];
+      ss = fmaf(v, v, ss);
+      C.xin[xpad(C.fmt, i)] = v * g.v[j];
+    }
   }
-  ss = block_sum_c(C, ss);
-  const float inv = rsqrtf(ss / static_cast<float>(K) + C.m.eps);
-#pragma unroll
-  for (int j = 0; j < kMaxGain; ++j) {
-    const int i = threadIdx.x + kCT * j;
-    if (i < K) C.xin[xpad(C.fmt, i)] = src[i] * inv * g.v[j];
-  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   csync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCW; ++w) t += red[w];
+  return rsqrtf(t / static_cast<float>(K) + C.m.eps);
 }
 
-// xin <- padded(src)
-__device__ __forceinline__ void to_xin(Cons& C, const float* src, int K) {
-  for (int i = threadIdx.x; i < K; i += kCT) C.xin[xpad(C.fmt, i)] = src[i];
+// Stage n floats of global memory straight into the padded matvec layout
+// (16-byte pieces stay contiguous inside a chunk).
+__device__ __forceinline__ void stage_xin(Cons& C, const float* src, int n) {
+  for (int i = threadIdx.x; i < n / 4; i += kCT)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(C.xin + xpad(C.fmt, 4 * i))),
+                 "l"(src + 4 * i)
+                 : "memory");
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   csync();
 }
 
@@ -410,24 +408,101 @@ struct MvOut {
   int epi;
   float* y;           // kEpiStore / kEpiArgmax: y[r]; kEpiSwiGLU: y[r/2]; kEpiResid: y[r]
   const float* res;   // kEpiResid: residual source (shared memory), indexed by r
-  float bv;           // running argmax (kEpiArgmax), per epilogue thread
+  float scale;        // multiplies every dot product (1, or 1/rms of a folded RMSNorm)
+  float bv;           // running argmax (kEpiArgmax), per epilogue lane / thread
   int bi;
 };
 
+// Apply the epilogue to row `row` with dot product v (already scaled).
+__device__ __forceinline__ void epi_row(MvOut& o, int row, float v) {
+  if (o.epi == kEpiResid) {
+    o.y[row] = o.res[row] + v;
+  } else {
+    o.y[row] = v;
+    if (o.epi == kEpiArgmax) argmax_merge(o.bv, o.bi, v, row);
+  }
+}
+
+// Partial dot products of rows wa and wb over chunk rounds [i0, i1) of this
+// lane (chunk c = lane + 32 i), two rounds at a time for more independent
+// work in flight.
+template <int FMT>
+__device__ __forceinline__ void dot_rows(const float* xin, const uint8_t* wa, const uint8_t* wb,
+                                         int K, int nchunks, int i0, int i1, float& acc_a,
+                                         float& acc_b) {
+  constexpr int XS = FMT == kFmtQ8 ? 20 : 12;
+  const int lane = threadIdx.x & 31;
+  float a2 = 0.f, b2 = 0.f;
+  int i = i0;
+#pragma unroll 1
+  for (; i + 1 < i1; i += 2) {
+    const int c0 = lane + 32 * i, c1 = c0 + 32;
+    const bool ok1 = c1 < nchunks;  // c0 < nchunks whenever c1 is
+    if (c0 < nchunks) {
+      const int cc1 = ok1 ? c1 : c0;
+      const float4* x0 = reinterpret_cast<const float4*>(xin + XS * c0);
+      const float4* x1 = reinterpret_cast<const float4*>(xin + XS * cc1);
+      const uint4 wa0 = *reinterpret_cast<const uint4*>(wa + 16 * c0);
+      const uint4 wb0 = *reinterpret_cast<const uint4*>(wb + 16 * c0);
+      const uint4 wa1 = *reinterpret_cast<const uint4*>(wa + 16 * cc1);
+      const uint4 wb1 = *reinterpret_cast<const uint4*>(wb + 16 * cc1);
+      if (FMT == kFmtQ8) {
+        const float sa0 = __half2float(*reinterpret_cast<const __half*>(wa + K + 2 * (c0 >> 1)));
+        const float sb0 = __half2float(*reinterpret_cast<const __half*>(wb + K + 2 * (c0 >> 1)));
+        const float sa1 = __half2float(*reinterpret_cast<const __half*>(wa + K + 2 * (cc1 >> 1)));
+        const float sb1 = __half2float(*reinterpret_cast<const __half*>(wb + K + 2 * (cc1 >> 1)));
+        const float da0 = dot16_q8(wa0, x0), db0 = dot16_q8(wb0, x0);
+        const float da1 = dot16_q8(wa1, x1), db1 = dot16_q8(wb1, x1);
+        acc_a = fmaf(sa0, da0, acc_a);
+        acc_b = fmaf(sb0, db0, acc_b);
+        if (ok1) {
+          a2 = fmaf(sa1, da1, a2);
+          b2 = fmaf(sb1, db1, b2);
+        }
+      } else {
+        acc_a += dot8_bf16(wa0, x0);
+        acc_b += dot8_bf16(wb0, x0);
+        if (ok1) {
+          a2 += dot8_bf16(wa1, x1);
+          b2 += dot8_bf16(wb1, x1);
+        }
+      }
+    }
+  }
+  if (i < i1) {
+    const int c = lane + 32 * i;
+    if (c < nchunks) {
+      const float4* xp = reinterpret_cast<const float4*>(xin + XS * c);
+      const uint4 w0 = *reinterpret_cast<const uint4*>(wa + 16 * c);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(wb + 16 * c);
+      if (FMT == kFmtQ8) {
+        const float s0 = __half2float(*reinterpret_cast<const __half*>(wa + K + 2 * (c >> 1)));
+        const float s1 = __half2float(*reinterpret_cast<const __half*>(wb + K + 2 * (c >> 1)));
+        acc_a = fmaf(s0, dot16_q8(w0, xp), acc_a);
+        acc_b = fmaf(s1, dot16_q8(w1, xp), acc_b);
+      } else {
+        acc_a += dot8_bf16(w0, xp);
+        acc_b += dot8_bf16(w1, xp);
+      }
+    }
+  }
+  acc_a += a2;
+  acc_b += b2;
+}
+
 // One phase of matvec rows [r0, r1) streamed through the ring.  Work in a
-// piece is split into tasks of (row pair, K segment); task partial sums go
-// through shared memory and one thread per row applies the epilogue.
+// piece is split into tasks of (row pair, K segment).  When every task owns
+// whole rows (one segment), its warp applies the epilogue itself and moves
+// on to the next piece; otherwise task partial sums go through shared memory
+// and one thread per row applies the epilogue after a consumer sync.
 template <int FMT>
 __device__ void mv_phase(Cons& C, size_t rb, int K, int r0, int r1, MvOut& o) {
   constexpr int EPC = FMT == kFmtQ8 ? 16 : 8;
-  constexpr int XS = FMT == kFmtQ8 ? 20 : 12;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nchunks = K / EPC;
   const int iters = (nchunks + 31) / 32;  // chunk rounds per lane
   const int rpp = rows_per_piece(rb);
   for (int a = r0; a < r1; a += rpp) {
-    float* part = C.red + 64 + kPartFloats * C.psel;  // [tasks][2]
-    C.psel ^= 1u;
     const int n = min(rpp, r1 - a);
     const int pairs = (n + 1) >> 1;
     int nseg = kCW / pairs;
@@ -435,46 +510,42 @@ __device__ void mv_phase(Cons& C, size_t rb, int K, int r0, int r1, MvOut& o) {
     if (nseg > iters) nseg = iters;
     const int tasks = pairs * nseg;
     uint64_t* fb = C.r.full + C.r.n % kSlots;
-    mwait(fb, (C.r.n / kSlots) & 1u, C.err);
     const uint8_t* slot = slot_ptr(C.r);
+    float* part = C.red + 64 + kPartFloats * C.psel;  // [tasks][2] when nseg > 1
+    if (nseg > 1) C.psel ^= 1u;
+    if (warp < tasks) mwait(fb, (C.r.n / kSlots) & 1u, C.err);
     for (int t = warp; t < tasks; t += kCW) {
       const int p = t / nseg, sg = t - p * nseg;
-      const int i0 = iters * sg / nseg, i1 = iters * (sg + 1) / nseg;
       const int ra = 2 * p, rbw = 2 * p + 1;
       const bool has_b = rbw < n;
-      const uint8_t* wa = slot + static_cast<size_t>(ra) * rb;
-      const uint8_t* wb = slot + static_cast<size_t>(has_b ? rbw : ra) * rb;
       float acc_a = 0.f, acc_b = 0.f;
-#pragma unroll 1
-      for (int i = i0; i < i1; ++i) {
-        const int c = lane + 32 * i;
-        if (c < nchunks) {
-          const float4* xp = reinterpret_cast<const float4*>(C.xin + XS * c);
-          const uint4 w0 = *reinterpret_cast<const uint4*>(wa + 16 * c);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(wb + 16 * c);
-          if (FMT == kFmtQ8) {
-            const float s0 = __half2float(*reinterpret_cast<const __half*>(wa + K + 2 * (c >> 1)));
-            const float s1 = __half2float(*reinterpret_cast<const __half*>(wb + K + 2 * (c >> 1)));
-            acc_a = fmaf(s0, dot16_q8(w0, xp), acc_a);
-            acc_b = fmaf(s1, dot16_q8(w1, xp), acc_b);
-          } else {
-            acc_a += dot8_bf16(w0, xp);
-            acc_b += dot8_bf16(w1, xp);
-          }
-        }
-      }
+      dot_rows<FMT>(C.xin, slot + static_cast<size_t>(ra) * rb,
+                    slot + static_cast<size_t>(has_b ? rbw : ra) * rb, K, nchunks,
+                    iters * sg / nseg, iters * (sg + 1) / nseg, acc_a, acc_b);
       acc_a = warp_sum(acc_a);
       acc_b = warp_sum(acc_b);
       if (lane == 0) {
-        part[2 * t] = acc_a;
-        part[2 * t + 1] = acc_b;
+        if (nseg == 1) {
+          acc_a *= o.scale;
+          acc_b *= o.scale;
+          if (o.epi == kEpiSwiGLU) {
+            o.y[(a + ra) >> 1] = silu_mul(acc_a, acc_b);
+          } else {
+            epi_row(o, a + ra, acc_a);
+            if (has_b) epi_row(o, a + rbw, acc_b);
+          }
+        } else {
+          part[2 * t] = acc_a;
+          part[2 * t + 1] = acc_b;
+        }
       }
     }
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(C.r.empty + C.r.n % kSlots)) : "memory");
     ++C.r.n;
+    if (nseg == 1) continue;
     csync();
-    // epilogue: one thread per row (SwiGLU: one per pair)
+    // split-K epilogue: one thread per row (SwiGLU: one per pair)
     if (o.epi == kEpiSwiGLU) {
       for (int p = threadIdx.x; p < pairs; p += kCT) {
         float g = 0.f, u = 0.f;
@@ -482,20 +553,14 @@ __device__ void mv_phase(Cons& C, size_t rb, int K, int r0, int r1, MvOut& o) {
           g += part[2 * (p * nseg + sg)];
           u += part[2 * (p * nseg + sg) + 1];
         }
-        o.y[(a >> 1) + p] = silu_mul(g, u);
+        o.y[(a >> 1) + p] = silu_mul(g * o.scale, u * o.scale);
       }
     } else {
       for (int i = threadIdx.x; i < n; i += kCT) {
         const int p = i >> 1, w = i & 1;
         float v = 0.f;
         for (int sg = 0; sg < nseg; ++sg) v += part[2 * (p * nseg + sg) + w];
-        const int row = a + i;
-        if (o.epi == kEpiResid) {
-          o.y[row] = o.res[row] + v;
-        } else {
-          o.y[row] = v;
-          if (o.epi == kEpiArgmax) argmax_merge(o.bv, o.bi, v, row);
-        }
+        epi_row(o, a + i, v * o.scale);
       }
     }
   }
@@ -785,7 +850,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
         if (!wait()) return;
         stage(C, C.xraw, s.x, m.H);
       }
-      to_xin_norm(C, C.xraw, m.H, gain);
+      o.scale = to_xin_norm(C, C.xraw, m.H, gain);
       o.epi = kEpiStore;
       o.y = s.qkv;
       mv_phase<FMT>(C, m.row_bytes_h, m.H, q0, q1, o);
@@ -804,8 +869,8 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       // ---- O projection + residual ----
       load_gain(gain, L.ffn_norm, m.H);  // for the next phase
       if (!wait()) return;
-      stage(C, C.scr, s.attn, m.qw);
-      to_xin(C, C.scr, m.qw);
+      stage_xin(C, s.attn, m.qw);
+      o.scale = 1.f;
       o.epi = kEpiResid;
       o.y = s.x_mid;
       o.res = C.xraw;
@@ -814,15 +879,15 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       // ---- RMSNorm + gate/up + SwiGLU ----
       if (!wait()) return;
       stage(C, C.xraw, s.x_mid, m.H);
-      to_xin_norm(C, C.xraw, m.H, gain);
+      o.scale = to_xin_norm(C, C.xraw, m.H, gain);
       o.epi = kEpiSwiGLU;
       o.y = s.h;
       mv_phase<FMT>(C, m.row_bytes_h, m.H, g0, g1, o);
       arrive();
       // ---- down projection + residual ----
       if (!wait()) return;
-      stage(C, C.scr, s.h, m.I);
-      to_xin(C, C.scr, m.I);
+      stage_xin(C, s.h, m.I);
+      o.scale = 1.f;
       o.epi = kEpiResid;
       o.y = s.x;
       o.res = C.xraw;
@@ -835,8 +900,8 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       load_gain(gain, m.out_norm, m.H);
       if (!wait()) return;
       stage(C, C.xraw, s.x, m.H);
-      to_xin_norm(C, C.xraw, m.H, gain);
       MvOut o{};
+      o.scale = to_xin_norm(C, C.xraw, m.H, gain);
       o.epi = kEpiArgmax;
       o.y = s.logits;
       o.bv = -INFINITY;
@@ -844,10 +909,11 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       mv_phase<FMT>(C, m.row_bytes_h, m.H, v0, v1, o);
       // block candidate -> global candidates -> the last block picks the winner
       warp_argmax(o.bv, o.bi);
-      int* redi = reinterpret_cast<int*>(C.red + 32);
+      float* redv = C.red + 32;                         // clear of the norm partials
+      int* redi = reinterpret_cast<int*>(C.red + 48);
       const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
       if (lane == 0) {
-        C.red[warp] = o.bv;
+        redv[warp] = o.bv;
         redi[warp] = o.bi;
       }
       csync();
@@ -855,7 +921,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       if (threadIdx.x == 0) {
         float bv = -INFINITY;
         int bi = INT_MAX;
-        for (int w = 0; w < kCW; ++w) argmax_merge(bv, bi, C.red[w], redi[w]);
+        for (int w = 0; w < kCW; ++w) argmax_merge(bv, bi, redv[w], redi[w]);
         s.amax_v[b] = bv;
         s.amax_i[b] = bi;
         __threadfence();
@@ -869,15 +935,16 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
         int bi = INT_MAX;
         for (int k = threadIdx.x; k < nb; k += kCT) argmax_merge(bv, bi, __ldcg(s.amax_v + k), __ldcg(s.amax_i + k));
         warp_argmax(bv, bi);
+        csync();  // every warp has read redv / redi above
         if (lane == 0) {
-          C.red[warp] = bv;
+          redv[warp] = bv;
           redi[warp] = bi;
         }
         csync();
         if (threadIdx.x == 0) {
           float v = -INFINITY;
           int i = INT_MAX;
-          for (int w = 0; w < kCW; ++w) argmax_merge(v, i, C.red[w], redi[w]);
+          for (int w = 0; w < kCW; ++w) argmax_merge(v, i, redv[w], redi[w]);
           int next = i;
           if (i == INT_MAX) {
             atomicOr(C.err, kErrAllNaN);
