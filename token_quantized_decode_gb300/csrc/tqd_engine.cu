@@ -377,8 +377,12 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const int qw = nq * hd, kvw = nkv * hd, wt = cfg->weight_type;
   const int fmt = wt == TQD_WEIGHT_Q8_0 ? kFmtQ8 : kFmtBF16;
   const size_t rbh = row_bytes(wt, H), rbq = row_bytes(wt, qw), rbi = row_bytes(wt, I);
-  // split-K attention chunks: one (kv head, chunk) item per SM
+  // split-K attention chunks: one (kv head, chunk) item per SM, and few
+  // enough that a group's partials (G x chunks x (head_dim + 2) floats) fit
+  // the 24 KB the persistent kernel stages them in
   int nch = m->num_sms / nkv;
+  const int nch_cap = 24576 / (4 * (nq / nkv) * (hd + 2));
+  if (nch > nch_cap) nch = nch_cap;
   if (nch < 1) nch = 1;
 
   // ---- arena layout ----

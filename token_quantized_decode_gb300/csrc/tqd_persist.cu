@@ -513,7 +513,9 @@ __device__ void mv_phase(Cons& C, size_t rb, int K, int r0, int r1, MvOut& o) {
     const uint8_t* slot = slot_ptr(C.r);
     float* part = C.red + 64 + kPartFloats * C.psel;  // [tasks][2] when nseg > 1
     if (nseg > 1) C.psel ^= 1u;
-    if (warp < tasks) mwait(fb, (C.r.n / kSlots) & 1u, C.err);
+    // every warp waits for the piece before releasing it, so no warp can run
+    // ahead and release a later use of the same slot early
+    mwait(fb, (C.r.n / kSlots) & 1u, C.err);
     for (int t = warp; t < tasks; t += kCW) {
       const int p = t / nseg, sg = t - p * nseg;
       const int ra = 2 * p, rbw = 2 * p + 1;
