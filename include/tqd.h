@@ -253,6 +253,28 @@ int32_t tqd_op_silu_mul(const float* g, const float* u, int64_t n, float* out, v
 int32_t tqd_op_argmax(const float* x, int64_t n, int32_t* idx_out, void* scratch, void* stream);
 size_t tqd_argmax_scratch_bytes(void);
 
+/* Allocation-free variant of tqd_op_attention (the pages have no counterpart;
+ * this is an interface for callers that may not allocate device memory while
+ * they run, e.g. a serving loop whose memory budget is fixed at start-up, or a
+ * host thread that must not trigger the device-wide synchronisation that
+ * cudaMalloc / cudaFree can cause).  Same inputs, output and result as
+ * tqd_op_attention; the per-chunk scratch lives in a static device array of
+ * tqd_op_attention_noalloc_max_scratch() bytes (1 MiB) that every device
+ * loading the library holds until the process exits.  No device memory is
+ * allocated by the call.
+ *  - The first call on a device looks up that array's device address (with
+ *    the device current); make that first call before any stream capture.
+ *  - Calls whose tqd_attention_scratch_bytes(...) exceeds the array's size
+ *    return TQD_ERR_BAD_ARG (see tqd_last_error()).
+ *  - Every call on a device shares the array and leaves its contents behind;
+ *    the call clears the arrival counters it needs on `stream` before its
+ *    kernel.  Calls that overlap on the GPU (other streams, or concurrent
+ *    host threads) race on the array and must be serialised by the caller. */
+int32_t tqd_op_attention_noalloc(const float* q, const float* K, const float* V, int32_t S,
+                                 int32_t n_heads, int32_t n_kv, int32_t head_dim,
+                                 int32_t n_chunks, float* out, void* stream);
+size_t tqd_op_attention_noalloc_max_scratch(void);
+
 #ifdef __cplusplus
 }
 #endif

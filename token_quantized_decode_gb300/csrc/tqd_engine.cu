@@ -23,6 +23,12 @@ namespace {
 
 thread_local std::string g_last_error;
 
+}  // namespace
+
+void tqd::set_last_error(const char* msg) { g_last_error = msg; }
+
+namespace {
+
 void set_error(const char* fmt, ...) {
   char buf[1024];
   va_list ap;

@@ -94,4 +94,7 @@ constexpr int kOpArgmaxBlocks = 304;
 
 bool attention_supported(int hd, int group);
 
+// Record the text tqd_last_error() returns on this thread.
+void set_last_error(const char* msg);
+
 }  // namespace tqd

@@ -50,6 +50,19 @@ def tqd_op_attention(q, K, V, S: int, n_heads: int, n_kv: int, head_dim: int, n_
           "tqd_op_attention")
 
 
+def tqd_op_attention_noalloc(q, K, V, S: int, n_heads: int, n_kv: int, head_dim: int, n_chunks: int, out,
+                             stream=None):
+    """tqd_op_attention without caller scratch: the library's static device
+    array holds the partials (allocates nothing per call)."""
+    check(lib().tqd_op_attention_noalloc(q.data_ptr(), K.data_ptr(), V.data_ptr(), S, n_heads, n_kv, head_dim,
+                                         n_chunks, out.data_ptr(), _s(stream)),
+          "tqd_op_attention_noalloc")
+
+
+def tqd_op_attention_noalloc_max_scratch() -> int:
+    return int(lib().tqd_op_attention_noalloc_max_scratch())
+
+
 def tqd_op_silu_mul(g, u, n: int, out, stream=None):
     check(lib().tqd_op_silu_mul(g.data_ptr(), u.data_ptr(), n, out.data_ptr(), _s(stream)), "tqd_op_silu_mul")
 
