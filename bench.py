@@ -61,6 +61,27 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def measured_traffic(tokens_per_launch: float):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "k_persist_qwen3-0.6b_traffic.txt")
+    try:
+        kv = {}
+        for line in open(path):
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+        h = hashlib.sha256()
+        for f in kv["sources"].split():
+            h.update(open(os.path.join(ROOT, "token_quantized_decode_gb300", "csrc", f), "rb").read())
+        if h.hexdigest() != kv["sources_sha256"]:
+            return None
+        return float(kv["dram_bytes_per_token"]) * tokens_per_launch
+    except Exception:
+        return None
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -289,7 +310,10 @@ def run_tqd(args, wl, world, rank, local, pg):
                    "l2": "inputs larger than L2: each token streams %.0f MB vs 129 MB L2" % (mean_step_bytes / 1e6),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
+                     "frac": achieved / hbm,
+                     "traffic": (measured_traffic(tokens / len(ev))
+                                 if schedule == tqd.TQD_SCHED_PERSISTENT and wl.name.startswith("qwen3-0.6b-shape-q8_0-prompt511")
+                                 else None),
                      "kernel": "k_persistent<Q8_0>" if schedule == tqd.TQD_SCHED_PERSISTENT else "whole step",
                      "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
                      "peak_kind": f"{kind} copy bandwidth"},
