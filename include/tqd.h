@@ -178,6 +178,23 @@ int32_t tqd_decode_step(tqd_model* model, int32_t seq, int32_t token, int32_t po
 int32_t tqd_generate(tqd_model* model, int32_t seq, int32_t first_token, int32_t n_steps,
                      int32_t* ids_out);
 
+/* One greedy step for sequences 0 .. n_seq-1 together (n_seq <= 16 and
+ * <= max_batch): sequence b feeds tokens[b] at pos[b] (its next position).
+ * The projections run as tensor-core contractions over the batch (tcgen05,
+ * f32-accurate through exact tf32 splits), attention per sequence.  next_out[b]
+ * receives sequence b's argmax.  Errors: as tqd_decode_step, plus
+ * UNSUPPORTED_CONFIG when the model has no batched step (max_batch == 1).
+ * ("Metal LLM decode", the batched prefill+decode arm: sequences share one
+ * sweep of the weights per step.) */
+int32_t tqd_decode_step_batch(tqd_model* model, int32_t n_seq, const int32_t* tokens,
+                              const int32_t* pos, int32_t* next_out);
+
+/* n_steps chained batched greedy steps for sequences 0 .. n_seq-1, each
+ * starting from first_tokens[b] at its next position; ids_out[i * n_seq + b]
+ * receives step i's id of sequence b. */
+int32_t tqd_generate_batch(tqd_model* model, int32_t n_seq, const int32_t* first_tokens,
+                           int32_t n_steps, int32_t* ids_out);
+
 /* Copy the logits of sequence seq's last step (f32 [vocab]) to host_out.
  * A debugging and parity hook, off the decode path ("One command buffer per
  * token", read_logits). */

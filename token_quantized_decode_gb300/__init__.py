@@ -19,7 +19,8 @@ __all__ = [
     "TQDError", "TQD_SCHED_GRAPH", "TQD_SCHED_PERSISTENT", "TQD_WEIGHT_Q8_0", "TQD_WEIGHT_BF16",
     "make_config", "make_host_weights", "tqd_status_name", "tqd_create", "tqd_destroy", "tqd_reset",
     "tqd_truncate", "tqd_next_pos", "tqd_prefill", "tqd_kv_upload", "tqd_decode_step", "tqd_generate",
-    "tqd_read_logits", "tqd_phase_count", "tqd_step_bytes", "Decoder",
+    "tqd_decode_step_batch", "tqd_generate_batch", "tqd_read_logits", "tqd_phase_count", "tqd_step_bytes",
+    "Decoder",
 ]
 
 _LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "q_norm", "k_norm", "ffn_norm", "w_gate", "w_up",
@@ -142,6 +143,24 @@ def tqd_generate(handle, seq: int, first_token: int, n_steps: int, out=None) -> 
     return ids
 
 
+def tqd_decode_step_batch(handle, tokens, pos) -> np.ndarray:
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    out = np.empty(tokens.size, dtype=np.int32)
+    check(lib().tqd_decode_step_batch(handle, tokens.size, tokens.ctypes.data, pos.ctypes.data, out.ctypes.data),
+          "tqd_decode_step_batch")
+    return out
+
+
+def tqd_generate_batch(handle, first_tokens, n_steps: int) -> np.ndarray:
+    """Returns ids [n_steps, n_seq]."""
+    first = np.ascontiguousarray(first_tokens, dtype=np.int32)
+    out = np.empty((n_steps, first.size), dtype=np.int32)
+    check(lib().tqd_generate_batch(handle, first.size, first.ctypes.data, int(n_steps), out.ctypes.data),
+          "tqd_generate_batch")
+    return out
+
+
 def tqd_read_logits(handle, seq: int, vocab: int, out=None) -> np.ndarray:
     logits = out if out is not None else np.empty(vocab, dtype=np.float32)
     check(lib().tqd_read_logits(handle, seq, logits.ctypes.data), "tqd_read_logits")
@@ -187,6 +206,12 @@ class Decoder:
 
     def generate(self, first_token: int, n_steps: int, seq: int = 0) -> np.ndarray:
         return tqd_generate(self.handle, seq, first_token, n_steps)
+
+    def decode_step_batch(self, tokens, pos) -> np.ndarray:
+        return tqd_decode_step_batch(self.handle, tokens, pos)
+
+    def generate_batch(self, first_tokens, n_steps: int) -> np.ndarray:
+        return tqd_generate_batch(self.handle, first_tokens, n_steps)
 
     def logits(self, seq: int = 0) -> np.ndarray:
         return tqd_read_logits(self.handle, seq, self.cfg.vocab)

@@ -7,6 +7,7 @@
 // sections "Resident state" and "One command buffer").
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -59,13 +60,21 @@ struct tqd_model {
   DevModel dm{};
   std::vector<SeqSlot> seqs;
   std::vector<DevLayer> host_layers;  // host copy of dm.layers (launch arguments)
-  int32_t* h_tokens = nullptr;  // pinned staging [max_seq + 1]
+  int32_t* h_tokens = nullptr;  // pinned staging [max(max_seq + 1, 128)]
   DevState* h_state = nullptr;  // pinned
   bool poisoned = false;
   bool pdl = true;
   int blocks_qkv = 0, blocks_o = 0, blocks_gu = 0, blocks_d = 0, blocks_lm = 0;
   int blocks_persist = 0;
   int64_t weight_bytes = 0;
+  // batched step: activations of up to batch_max() sequences, the device copy
+  // of the sequences' descriptors, one graph per batch size
+  bool batch_ok = false;
+  float *bx = nullptr, *bqkv = nullptr, *battn = nullptr, *bh = nullptr;
+  DevSeq* dseqs = nullptr;
+  uint32_t* bcount = nullptr;
+  int batch_nch = 1;
+  cudaGraphExec_t bgraph[17] = {};
 };
 
 namespace {
@@ -323,6 +332,8 @@ void tqd_destroy(tqd_model* m) {
     if (s.g_full) cudaGraphExecDestroy(s.g_full);
     if (s.g_layers) cudaGraphExecDestroy(s.g_layers);
   }
+  for (cudaGraphExec_t& g : m->bgraph)
+    if (g) cudaGraphExecDestroy(g);
   if (m->arena) cudaFree(m->arena);
   if (m->h_tokens) cudaFreeHost(m->h_tokens);
   if (m->h_state) cudaFreeHost(m->h_state);
@@ -439,6 +450,17 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].acount = take(4);
     so[b].bar = take(sizeof(DevBarrier));
   }
+  // batched-step buffers (only for models holding several sequences)
+  const int bmax = batch_max();
+  size_t o_bx = 0, o_bqkv = 0, o_battn = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0;
+  if (cfg->max_batch > 1) {
+    o_bx = take(4ull * bmax * H);
+    o_bqkv = take(4ull * bmax * (qw + 2 * kvw));
+    o_battn = take(4ull * bmax * qw);
+    o_bh = take(4ull * bmax * I);
+    o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);
+    o_bcount = take(4);
+  }
   m->arena_bytes = off;
   cudaError_t ce = cudaMalloc(&m->arena, m->arena_bytes);
   if (ce != cudaSuccess) {
@@ -448,7 +470,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     tqd_destroy(m);
     return TQD_ERR_OOM;
   }
-  if (cudaMallocHost(&m->h_tokens, 4 * (static_cast<size_t>(S) + 1)) != cudaSuccess ||
+  if (cudaMallocHost(&m->h_tokens, 4 * std::max<size_t>(static_cast<size_t>(S) + 1, 128)) != cudaSuccess ||
       cudaMallocHost(&m->h_state, sizeof(DevState)) != cudaSuccess) {
     cudaGetLastError();
     set_error("pinned host allocation failed");
@@ -579,6 +601,21 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.amax_i = reinterpret_cast<int32_t*>(base + so[b].ai);
     d.amax_count = reinterpret_cast<uint32_t*>(base + so[b].acount);
     d.bar = reinterpret_cast<DevBarrier*>(base + so[b].bar);
+  }
+  if (cfg->max_batch > 1 && batch_supported(dm) && (V + 127) / 128 <= kMaxArgmaxBlocks) {
+    m->bx = reinterpret_cast<float*>(base + o_bx);
+    m->bqkv = reinterpret_cast<float*>(base + o_bqkv);
+    m->battn = reinterpret_cast<float*>(base + o_battn);
+    m->bh = reinterpret_cast<float*>(base + o_bh);
+    m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
+    m->bcount = reinterpret_cast<uint32_t*>(base + o_bcount);
+    std::vector<DevSeq> hs(cfg->max_batch);
+    for (int b = 0; b < cfg->max_batch; ++b) hs[b] = m->seqs[b].d;
+    if ((e = cudaMemcpy(m->dseqs, hs.data(), sizeof(DevSeq) * cfg->max_batch,
+                        cudaMemcpyHostToDevice)) != cudaSuccess ||
+        (e = batch_setup(dm)) != cudaSuccess)
+      return fail(e, "batched-step set-up");
+    m->batch_ok = true;
   }
   m->blocks_qkv = matvec_blocks(fmt, qw + 2 * kvw, H, m->num_sms, 0);
   m->blocks_o = matvec_blocks(fmt, H, qw, m->num_sms, 0);
@@ -759,6 +796,143 @@ int32_t tqd_generate(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_s
   if ((rc = finish(m, s))) return rc;
   s.next_pos = pos + n_steps;
   memcpy(ids_out, m->h_tokens, 4ull * n_steps);
+  return TQD_OK;
+}
+
+namespace {
+
+int32_t check_batch(tqd_model* m, int32_t n_seq) {
+  int32_t rc = check_model(m, 0);
+  if (rc) return rc;
+  if (!m->batch_ok) {
+    set_error("this model has no batched step (max_batch must be > 1 and the shape supported)");
+    return TQD_ERR_UNSUPPORTED_CONFIG;
+  }
+  if (n_seq < 1 || n_seq > batch_max() || n_seq > m->cfg.max_batch) {
+    set_error("n_seq %d outside [1, %d]", n_seq, std::min(batch_max(), m->cfg.max_batch));
+    return TQD_ERR_BAD_ARG;
+  }
+  return TQD_OK;
+}
+
+// Enqueue `steps` batched steps of sequences 0..n-1 (graph captured once per n).
+int32_t run_batch(tqd_model* m, int n, int steps) {
+  cudaGraphExec_t& g = m->bgraph[n];
+  if (!g) {
+    // split-K chunks: about four attention blocks per SM
+    int nch = (4 * m->num_sms + n * m->dm.nkv - 1) / (n * m->dm.nkv);
+    if (nch > m->dm.n_chunks) nch = m->dm.n_chunks;
+    if (nch < 1) nch = 1;
+    m->batch_nch = nch;
+    cudaGraph_t graph = nullptr;
+    CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
+    cudaError_t e = enqueue_batch_step(m->dm, m->host_layers.data(), m->dseqs, n, nch, m->bx, m->bqkv,
+                                       m->battn, m->bh, m->bcount, &m->seqs[0].d.state->err,
+                                       m->stream);
+    cudaError_t e2 = cudaStreamEndCapture(m->stream, &graph);
+    if (e != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      return fail_cuda(m, e, "capture batched step");
+    }
+    if (e2 != cudaSuccess) return fail_cuda(m, e2, "end capture");
+    e = cudaGraphInstantiate(&g, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail_cuda(m, e, "instantiate batched graph");
+  }
+  for (int i = 0; i < steps; ++i) CK(cudaGraphLaunch(g, m->stream), "batched graph launch");
+  return TQD_OK;
+}
+
+// Read back every sequence's state; the first error wins.
+int32_t finish_batch(tqd_model* m, int n) {
+  int32_t first = TQD_OK;
+  for (int b = 0; b < n; ++b) {
+    int32_t rc = finish(m, m->seqs[b]);
+    if (rc && !first) first = rc;
+    if (rc == TQD_ERR_DEVICE_TIMEOUT || rc == TQD_ERR_CUDA) return rc;
+  }
+  return first;
+}
+
+}  // namespace
+
+int32_t tqd_decode_step_batch(tqd_model* m, int32_t n_seq, const int32_t* tokens, const int32_t* pos,
+                              int32_t* next_out) {
+  int32_t rc = check_batch(m, n_seq);
+  if (rc) return rc;
+  if (!tokens || !pos || !next_out) {
+    set_error("tokens, pos and next_out must be non-NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  for (int b = 0; b < n_seq; ++b) {
+    if (tokens[b] < 0 || tokens[b] >= m->cfg.vocab) {
+      set_error("token %d of sequence %d outside the vocabulary", tokens[b], b);
+      return TQD_ERR_BAD_ARG;
+    }
+    if (pos[b] != m->seqs[b].next_pos) {
+      set_error("pos %d of sequence %d is not its next position %d", pos[b], b, m->seqs[b].next_pos);
+      return TQD_ERR_POS_MISMATCH;
+    }
+    if (pos[b] >= m->cfg.max_seq) {
+      set_error("position %d of sequence %d is beyond max_seq %d", pos[b], b, m->cfg.max_seq);
+      return TQD_ERR_CAPACITY;
+    }
+  }
+  for (int b = 0; b < n_seq; ++b) {
+    m->h_tokens[b] = tokens[b];
+    CK(cudaMemcpyAsync(m->seqs[b].d.tokens + pos[b], m->h_tokens + b, 4, cudaMemcpyHostToDevice,
+                       m->stream),
+       "write token");
+  }
+  if ((rc = run_batch(m, n_seq, 1))) return rc;
+  for (int b = 0; b < n_seq; ++b)
+    CK(cudaMemcpyAsync(m->h_tokens + 64 + b, m->seqs[b].d.tokens + pos[b] + 1, 4,
+                       cudaMemcpyDeviceToHost, m->stream),
+       "read next token");
+  if ((rc = finish_batch(m, n_seq))) return rc;
+  for (int b = 0; b < n_seq; ++b) {
+    m->seqs[b].next_pos = pos[b] + 1;
+    next_out[b] = m->h_tokens[64 + b];
+  }
+  return TQD_OK;
+}
+
+int32_t tqd_generate_batch(tqd_model* m, int32_t n_seq, const int32_t* first_tokens, int32_t n_steps,
+                           int32_t* ids_out) {
+  int32_t rc = check_batch(m, n_seq);
+  if (rc) return rc;
+  if (!first_tokens || !ids_out || n_steps <= 0) {
+    set_error("generate_batch needs first_tokens, ids_out and n_steps > 0");
+    return TQD_ERR_BAD_ARG;
+  }
+  for (int b = 0; b < n_seq; ++b) {
+    if (first_tokens[b] < 0 || first_tokens[b] >= m->cfg.vocab) {
+      set_error("first token of sequence %d outside the vocabulary", b);
+      return TQD_ERR_BAD_ARG;
+    }
+    if (static_cast<int64_t>(m->seqs[b].next_pos) + n_steps > m->cfg.max_seq) {
+      set_error("%d steps from position %d of sequence %d exceed max_seq %d", n_steps,
+                m->seqs[b].next_pos, b, m->cfg.max_seq);
+      return TQD_ERR_CAPACITY;
+    }
+  }
+  for (int b = 0; b < n_seq; ++b) {
+    m->h_tokens[b] = first_tokens[b];
+    CK(cudaMemcpyAsync(m->seqs[b].d.tokens + m->seqs[b].next_pos, m->h_tokens + b, 4,
+                       cudaMemcpyHostToDevice, m->stream),
+       "write token");
+  }
+  if ((rc = run_batch(m, n_seq, n_steps))) return rc;
+  CK(cudaStreamSynchronize(m->stream), "synchronize");
+  for (int b = 0; b < n_seq; ++b) {
+    CK(cudaMemcpyAsync(m->h_tokens, m->seqs[b].d.tokens + m->seqs[b].next_pos + 1, 4ull * n_steps,
+                       cudaMemcpyDeviceToHost, m->stream),
+       "read tokens");
+    CK(cudaStreamSynchronize(m->stream), "synchronize");
+    for (int i = 0; i < n_steps; ++i) ids_out[static_cast<size_t>(i) * n_seq + b] = m->h_tokens[i];
+  }
+  if ((rc = finish_batch(m, n_seq))) return rc;
+  for (int b = 0; b < n_seq; ++b) m->seqs[b].next_pos += n_steps;
   return TQD_OK;
 }
 
