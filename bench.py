@@ -35,6 +35,14 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "qwen3_0.6b"
 
 
+def metric_for(wl) -> str:
+    """The headline metric on the default workload; the other workloads
+    (parity cases, measured on request) say which workload they are."""
+    if wl.name == synth.WORKLOADS[DEFAULT_WORKLOAD].name:
+        return METRIC
+    return f"decode tokens/sec, all sequences ({wl.name}) and % of HBM roofline"
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -215,7 +223,7 @@ def run_reference(args, wl, world, rank):
     sample = (f"{n} oracle decode steps at positions {wl.prompt_len}..{wl.prompt_len + n - 1} after a "
               f"seeded stand-in KV history of {wl.prompt_len} rows (no oracle prefill)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric_for(wl), "value": tps, "unit": UNIT, "n_gpus": world,
         "steps": n, "warmup": args.warmup, "ms_per_step": 1000.0 * el / n, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "prompt_len": wl.prompt_len, "batch": wl.batch},
@@ -233,30 +241,48 @@ def run_tqd(args, wl, world, rank, local, pg):
     stream = torch.cuda.Stream()
     cfg = wl.model
     model = synth.make_model(cfg, wl.model_seed)
-    ids = synth.prompt(wl)
-    P, D = wl.prompt_len, wl.decode_steps
+    P, D, B = wl.prompt_len, wl.decode_steps, wl.batch
     schedule = tqd.TQD_SCHED_PERSISTENT if args.schedule == "persistent" else tqd.TQD_SCHED_GRAPH
-    dec = tqd.Decoder(model, P + D, 1, schedule, stream=stream)
+    dec = tqd.Decoder(model, P + D, B, schedule, stream=stream)
     del model
-    if args.kv_source == "prefill":
-        first = dec.prefill(ids)
-    else:
-        k, v = synth.kv_fill(cfg, 7, 0, P, -1.0, 1.0)
-        dec.kv_upload(k, v)
-        del k, v
-        first = int(ids[-1])
+    firsts = []
+    for b in range(B):
+        ids = synth.prompt(wl, seq=b)
+        if args.kv_source == "prefill":
+            firsts.append(dec.prefill(ids, seq=b))
+        else:
+            k, v = synth.kv_fill(cfg, 7, b, P, -1.0, 1.0)
+            dec.kv_upload(k, v, seq=b)
+            del k, v
+            firsts.append(int(ids[-1]))
+    first = firsts[0]
+    kv_pos = 4 * cfg.kv_width * 2 * cfg.n_layers          # K and V bytes of one position, all layers
+    w_and_row = dec.step_bytes(0) - 2 * kv_pos              # weights + one embedding row
+    emb_row = cfg.hidden * 17 // 16 if cfg.weight_type == "q8_0" else 2 * cfg.hidden
 
-    def windows(n_tokens):
-        out, left = [], n_tokens
+    def step_bytes(p):
+        """Algorithmic bytes of one step at position p for all B sequences:
+        weights once, one embedding row and (p + 2) K/V positions per sequence."""
+        return w_and_row + (B - 1) * emb_row + B * kv_pos * (p + 2)
+
+    def windows(n_steps):
+        out, left = [], n_steps
         while left > 0:
             out.append(min(left, D))
             left -= out[-1]
         return out
 
-    # warm-up
-    for n in windows(args.warmup):
-        dec.truncate(P)
-        dec.generate(first, n)
+    def run_window(n):
+        for b in range(B):
+            dec.truncate(P, seq=b)
+        if B == 1:
+            dec.generate(first, n)
+        else:
+            dec.generate_batch(np.array(firsts), n)
+
+    steps_timed = max(1, args.steps // B)   # --steps counts tokens (all sequences)
+    for n in windows(max(1, args.warmup // B)):
+        run_window(n)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -265,61 +291,81 @@ def run_tqd(args, wl, world, rank, local, pg):
     torch.cuda.synchronize()
     total_bytes = 0
     launches = 0
-    for n in windows(args.steps):
-        dec.truncate(P)
+    for n in windows(steps_timed):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for b in range(B):
+            dec.truncate(P, seq=b)
         s.record(stream)
-        dec.generate(first, n)
+        if B == 1:
+            dec.generate(first, n)
+        else:
+            dec.generate_batch(np.array(firsts), n)
         e.record(stream)
         ev.append((s, e, n))
-        total_bytes += sum(dec.step_bytes(p) for p in range(P, P + n))
-        launches += 1 if schedule == tqd.TQD_SCHED_PERSISTENT else n * dec.phase_count
+        total_bytes += sum(step_bytes(p) for p in range(P, P + n))
+        if B > 1:
+            launches += n * (1 + 5 * cfg.n_layers + 1)
+        else:
+            launches += 1 if schedule == tqd.TQD_SCHED_PERSISTENT else n * dec.phase_count
     torch.cuda.synchronize()
     barrier(pg)
     clocks = sampler.stop()
     t_ms = sum(s.elapsed_time(e) for s, e, _ in ev)
-    tokens = sum(n for _, _, n in ev)
+    steps = sum(n for _, _, n in ev)
+    tokens = steps * B
     t_max = max_over_ranks(pg, t_ms)
     all_tokens = sum_over_ranks(pg, tokens)
     value = all_tokens / (t_max / 1000.0)
     per_launch_bytes = total_bytes / len(ev)
     per_launch_ms = t_ms / len(ev)
 
-    # end to end through the C ABI: one tqd_decode_step per token, host token
-    # in, host token out, the host round trip inside the timed region
-    dec.truncate(P)
+    # end to end through the C ABI: one decode call per step, host tokens in,
+    # host tokens out, the host round trip inside the timed region
+    for b in range(B):
+        dec.truncate(P, seq=b)
     torch.cuda.synchronize()
-    tok, pos = first, P
+    toks, pos = list(firsts), P
     n_e2e = min(args.e2e_steps, D)
     t0 = time.perf_counter()
     for _ in range(n_e2e):
-        tok = dec.decode_step(tok, pos)
+        if B == 1:
+            toks = [dec.decode_step(toks[0], pos)]
+        else:
+            toks = list(dec.decode_step_batch(np.array(toks), np.full(B, pos)))
         pos += 1
     e2e_s = time.perf_counter() - t0
-    e2e_val = sum_over_ranks(pg, n_e2e) / max_over_ranks(pg, e2e_s)
+    e2e_val = sum_over_ranks(pg, n_e2e * B) / max_over_ranks(pg, e2e_s)
 
     hbm, kind = peaks()
     achieved = per_launch_bytes / (per_launch_ms / 1000.0) / 1e9
-    mean_step_bytes = total_bytes / tokens
+    mean_step_bytes = total_bytes / steps
+    persistent_b1 = B == 1 and schedule == tqd.TQD_SCHED_PERSISTENT
+    if persistent_b1:
+        kernel = "k_persist<%s>" % ("Q8_0" if cfg.weight_type == "q8_0" else "bf16")
+    elif B > 1:
+        kernel = "whole batched step (graph: tcgen05 matmuls + streaming attention)"
+    else:
+        kernel = "whole step (graph schedule)"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": tokens,
-        "warmup": args.warmup, "ms_per_step": t_max / tokens, "higher_is_better": True, "scaling": "weak",
+        "metric": metric_for(wl), "value": value, "unit": UNIT, "n_gpus": world, "steps": tokens,
+        "warmup": args.warmup, "ms_per_step": t_max / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "prompt_len": P, "decode_positions": f"{P}..{P + D - 1}",
-                   "batch": wl.batch, "schedule": args.schedule, "weights": "Q8_0 (34-byte blocks), resident",
-                   "l2": "inputs larger than L2: each token streams %.0f MB vs 129 MB L2" % (mean_step_bytes / 1e6),
+                   "batch": B, "schedule": args.schedule if B == 1 else "batched graph",
+                   "weights": ("Q8_0 (34-byte blocks)" if cfg.weight_type == "q8_0" else "bf16") + ", resident",
+                   "kv_history": args.kv_source,
+                   "l2": "inputs larger than L2: each step streams %.0f MB vs 129 MB L2" % (mean_step_bytes / 1e6),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm,
-                     "traffic": (measured_traffic(tokens / len(ev))
-                                 if schedule == tqd.TQD_SCHED_PERSISTENT and wl.name.startswith("qwen3-0.6b-shape-q8_0-prompt511")
+                     "traffic": (measured_traffic(steps / len(ev))
+                                 if persistent_b1 and wl.name.startswith("qwen3-0.6b-shape-q8_0-prompt511")
                                  else None),
-                     "kernel": "k_persistent<Q8_0>" if schedule == tqd.TQD_SCHED_PERSISTENT else "whole step",
-                     "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
+                     "kernel": kernel, "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
                      "peak_kind": f"{kind} copy bandwidth"},
-        "step_roofline_frac": (mean_step_bytes / (hbm * 1e9)) / (t_max / tokens / 1000.0),
-        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4 + 16,
-                "api": "tqd_decode_step per token (host token in, host token out)"},
+        "step_roofline_frac": (mean_step_bytes / (hbm * 1e9)) / (t_max / steps / 1000.0),
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4 * B, "d2h_bytes_per_step": (4 + 16) * B,
+                "api": "tqd_decode_step per token" if B == 1 else "tqd_decode_step_batch per step"},
         "gpu_launches": launches,
         "clocks": clocks,
     }
