@@ -30,6 +30,9 @@ constexpr int kSlots = 4;
 constexpr int kPartFloats = 320;        // per-task partial sums of one ring piece
 constexpr int kRedFloats = 64 + 2 * kPartFloats;
 constexpr int kMaxGain = 4;             // norm gains held per thread (H <= 4 * kCT)
+// Error bits that end every block's waits; the others (a bad token id, every
+// logit NaN, capacity) are reported to the host without stopping the launch.
+constexpr uint32_t kFatal = kErrGridBarrier | kErrMbarrier;
 
 // ---------------------------------------------------------------- layout
 struct PLayout {
@@ -91,14 +94,14 @@ __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
 }
 
 // mbarrier wait that gives up after kWaitLimitNs or as soon as another thread
-// has reported an error.
+// has reported a fatal error.
 __device__ __forceinline__ bool mwait(uint64_t* bar, uint32_t parity, uint32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   uint32_t spins = 0;
   while (!mbar_try_wait(bar, parity)) {
     if ((++spins & 63u) == 0) {
-      if (ld_volatile_u32(err) != 0) return false;
+      if (ld_volatile_u32(err) & kFatal) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         atomicOr(err, kErrMbarrier);
         return false;
@@ -124,15 +127,15 @@ __device__ __forceinline__ void gb_arrive(DevBarrier* b) {
   if (threadIdx.x == 0) red_release_add_u64(&b->count, 1ull);
 }
 
-// Returns false on every consumer thread if the wait failed (timeout or an
-// error reported elsewhere).
+// Returns false on every consumer thread if the wait failed (timeout or a
+// fatal error reported elsewhere).
 __device__ __forceinline__ bool gb_wait(DevBarrier* b, unsigned long long target, uint32_t* err) {
   bool fail = false;
   if (threadIdx.x == 0) {
     if (ld_acquire_u64(&b->count) < target) {
       const uint64_t t0 = global_timer_ns();
       while (ld_acquire_u64(&b->count) < target) {
-        if (ld_volatile_u32(err) != 0) {
+        if (ld_volatile_u32(err) & kFatal) {
           fail = true;
           break;
         }
