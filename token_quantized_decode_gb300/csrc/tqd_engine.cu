@@ -73,6 +73,7 @@ struct tqd_model {
   float *bx = nullptr, *bqkv = nullptr, *battn = nullptr, *bh = nullptr;
   DevSeq* dseqs = nullptr;
   uint32_t* bcount = nullptr;
+  float* bss = nullptr;
   int batch_nch = 1;
   cudaGraphExec_t bgraph[17] = {};
 };
@@ -452,7 +453,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   }
   // batched-step buffers (only for models holding several sequences)
   const int bmax = batch_max();
-  size_t o_bx = 0, o_bqkv = 0, o_battn = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0;
+  size_t o_bx = 0, o_bqkv = 0, o_battn = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0;
   if (cfg->max_batch > 1) {
     o_bx = take(4ull * bmax * H);
     o_bqkv = take(4ull * bmax * (qw + 2 * kvw));
@@ -460,6 +461,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     o_bh = take(4ull * bmax * I);
     o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);
     o_bcount = take(4);
+    o_bss = take(4ull * 2 * batch_ss_slots(H) * bmax);
   }
   m->arena_bytes = off;
   cudaError_t ce = cudaMalloc(&m->arena, m->arena_bytes);
@@ -609,6 +611,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     m->bh = reinterpret_cast<float*>(base + o_bh);
     m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
     m->bcount = reinterpret_cast<uint32_t*>(base + o_bcount);
+    m->bss = reinterpret_cast<float*>(base + o_bss);
     std::vector<DevSeq> hs(cfg->max_batch);
     for (int b = 0; b < cfg->max_batch; ++b) hs[b] = m->seqs[b].d;
     if ((e = cudaMemcpy(m->dseqs, hs.data(), sizeof(DevSeq) * cfg->max_batch,
@@ -827,7 +830,7 @@ int32_t run_batch(tqd_model* m, int n, int steps) {
     cudaGraph_t graph = nullptr;
     CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
     cudaError_t e = enqueue_batch_step(m->dm, m->host_layers.data(), m->dseqs, n, nch, m->bx, m->bqkv,
-                                       m->battn, m->bh, m->bcount, &m->seqs[0].d.state->err,
+                                       m->battn, m->bh, m->bss, m->bcount, &m->seqs[0].d.state->err,
                                        m->stream);
     cudaError_t e2 = cudaStreamEndCapture(m->stream, &graph);
     if (e != cudaSuccess) {

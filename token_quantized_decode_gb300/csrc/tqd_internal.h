@@ -97,10 +97,11 @@ bool attention_supported(int hd, int group);
 // Batched step (tqd_batch.cu): up to batch_max() sequences per step, tcgen05
 // contractions for the projections, streaming split-K attention.
 int batch_max();
+int batch_ss_slots(int H);  // partial sums of squares per activation ([slots][batch_max()])
 bool batch_supported(const DevModel& m);
 cudaError_t batch_setup(const DevModel& m);
 cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const DevSeq* seqs,
-                               int n, int nch, float* X, float* QKV, float* ATTN, float* H,
+                               int n, int nch, float* X, float* QKV, float* ATTN, float* H, float* SS,
                                uint32_t* count, uint32_t* err, cudaStream_t st);
 
 // Record the text tqd_last_error() returns on this thread.
