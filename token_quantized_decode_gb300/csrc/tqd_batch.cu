@@ -13,6 +13,7 @@
 // What is computed is the decode step of the inferno.rs blog, "IV.4: One
 // command buffer per token", for several sequences sharing one sweep of the
 // weights ("Metal LLM decode", the batched prefill+decode arm).
+#include <algorithm>
 #include <climits>
 
 #include "tqd_internal.h"
@@ -35,22 +36,34 @@ namespace {
 //       bits, so the products are exact and the sums are f32 sums.
 constexpr int kMmThreads = 128;        // 4 warps; thread t owns weight row t of the tile
 constexpr int kTcM = 128;              // weight rows per tile (MMA M)
-constexpr int kTcN = 16;               // batch columns (MMA N)
-constexpr int kSubK = 64;              // K elements per MMA sub-chunk
+constexpr int kTcN = 16;               // batch rows
+constexpr int kTcN3 = 3 * kTcN;        // MMA N: the three bf16 parts of every batch row
+constexpr int kSubK = 64;              // K elements per A / B sub-chunk
 constexpr int kPassBytes = 128;        // weight bytes per row per pass (Q8_0: 128 K, bf16: 64 K)
-constexpr int kRawStride = kPassBytes + 16;  // padded row: conflict-free 16-byte reads
-constexpr int kRawStages = 2;
-constexpr uint32_t kRawBytes = kTcM * kRawStride;
+constexpr uint32_t kRawBytes = kTcM * kPassBytes;    // one raw stage; 16-byte chunks XOR-swizzled per row
 constexpr uint32_t kABytes = kTcM * kSubK * 2;       // one bf16 A sub-chunk
+constexpr uint32_t kAPassBytes = 2 * kABytes;        // A of one pass (up to 128 K)
 constexpr uint32_t kBPartBytes = kTcN * kSubK * 2;   // one bf16 part of B
-constexpr uint32_t kBBytes = 3 * kBPartBytes;
-constexpr int kRedStride = kTcN + 1;
-constexpr uint32_t kOffA = kRawStages * kRawBytes;
-constexpr uint32_t kOffB = kOffA + 2 * kABytes;
-constexpr uint32_t kOffRed = kOffB + 2 * kBBytes;
-constexpr uint32_t kMmSmem = kOffRed + kTcM * kRedStride * 4;
-constexpr uint32_t kTmemCols = 128;    // two passes x four blocks x 16 columns
+constexpr uint32_t kBBytes = 3 * kBPartBytes;        // one sub-chunk of B: N = 48 rows
+constexpr uint32_t kRecvBytes = kTcM * kTcN * 4;     // cluster partials received: [rank][row][16]
+constexpr uint32_t kPassCols = 4 * kTcN3;            // tensor-memory columns of one pass (four blocks)
 constexpr int kMaxCluster = 8;
+// Split projections (one tile per CTA, two CTAs per SM): B for up to 384
+// columns, one pass of A and of tensor memory at a time.  lm_head (one CTA
+// per SM looping over tiles): B for all of H <= 1024, deeper weight
+// staging, and double-buffered A and tensor memory so one pass's read-out
+// overlaps the next pass's MMAs.
+template <int STAGES, int MAXSUB, bool DBL>
+struct MmCfg {
+  static constexpr uint32_t a = STAGES * kRawBytes;
+  static constexpr uint32_t b = a + (DBL ? 2 : 1) * kAPassBytes;
+  static constexpr uint32_t recv = b + MAXSUB * kBBytes;
+  static constexpr uint32_t total = recv + kRecvBytes;
+  static constexpr uint32_t tmem = DBL ? 512 : 256;
+};
+using SplitCfg = MmCfg<2, 6, false>;
+using HeadCfg = MmCfg<3, 16, true>;
+constexpr int kSplitMaxK = 6 * kSubK, kHeadMaxK = 16 * kSubK;
 
 // Shared-memory matrix descriptor, K-major without swizzle: core matrices of
 // 8 rows x 16 bytes; lbo = byte step between core matrices along K, sbo =
@@ -74,7 +87,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t dt, uint64_t ad, uint64_t bd, 
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dt),
-      "l"(ad), "l"(bd), "r"(idesc_bf16(kTcM, kTcN)), "r"(acc)
+      "l"(ad), "l"(bd), "r"(idesc_bf16(kTcM, kTcN3)), "r"(acc)
       : "memory");
 }
 
@@ -127,26 +140,32 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-// A float in the shared memory of CTA `cta` of the cluster, at the offset of p.
-__device__ __forceinline__ float ld_dsmem(const float* p, uint32_t cta) {
-  uint32_t a;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(cta));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t addr, float (&v)[16]) {
-  uint32_t r[16];
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(addr)
       : "memory");
+}
+// The 48 columns of one block (three parts x 16 batch rows), summed per row.
+__device__ __forceinline__ void tmem_block_sum(uint32_t addr, float (&v)[16]) {
+  uint32_t r0[16], r1[16], r2[16];
+  tmem_ld16(addr, r0);
+  tmem_ld16(addr + 16, r1);
+  tmem_ld16(addr + 32, r2);
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) v[i] = (__uint_as_float(r0[i]) + __uint_as_float(r1[i])) + __uint_as_float(r2[i]);
+}
+__device__ __forceinline__ void st_dsmem4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t mapa_u32(const void* p, uint32_t cta) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(cta));
+  return a;
 }
 
 struct MmArgs {
@@ -170,243 +189,289 @@ struct MmArgs {
   int max_seq;
 };
 
+// Thread t of the CTA dequantises weight row t of the current tile and owns
+// tensor-memory lane t.  Projections split over a cluster run one tile per
+// CTA; the lm_head (cs == 1) runs one CTA per SM over tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ..., reading out one pass while the next pass's
+// MMAs run.
+template <class CFG>
 __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
+  constexpr bool DBL = CFG::tmem == 512;
+  constexpr int STAGES = CFG::a / kRawBytes;
   extern __shared__ __align__(1024) unsigned char sm[];
-  __shared__ __align__(8) uint64_t bars[4];  // [0..1] sub-chunk buffers free, [2..3] a pass's sums ready
+  __shared__ __align__(8) uint64_t bars[2];  // a pass's MMAs are complete (by pass parity)
   __shared__ uint32_t tmem_base;
   __shared__ float inv_rms[kTcN];
   __shared__ float wred_v[4][kTcN];
   __shared__ int wred_i[4][kTcN];
   __shared__ uint32_t s_last;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int rank = static_cast<int>(cluster_rank()), tile = blockIdx.x / a.cs;
-  const int row0 = tile * kTcM, row = row0 + t;
-  const bool row_ok = row < a.rows;
+  const int rank = static_cast<int>(cluster_rank());
   const bool q8 = a.fmt == kFmtQ8;
   const int KR = a.K / a.cs, kc0 = rank * KR;
   const int PK = q8 ? kPassBytes : kPassBytes / 2;  // K per pass
   const int npass = (KR + PK - 1) / PK;
-  // weight bytes of pass p for all 128 rows -> raw stage p % kRawStages
-  auto issue_raw = [&](int p) {
-    const int k0 = kc0 + p * PK, pk = min(PK, kc0 + KR - k0);
+  const int tiles = (a.rows + kTcM - 1) / kTcM;
+  const int tile0 = a.cs > 1 ? static_cast<int>(blockIdx.x) / a.cs : static_cast<int>(blockIdx.x);
+  const int tstride = a.cs > 1 ? tiles : static_cast<int>(gridDim.x);
+  const int ntile = tile0 < tiles ? (tiles - 1 - tile0) / tstride + 1 : 0;
+  const int total = ntile * npass;  // passes of this CTA, over all its tiles
+  auto pass_tile = [&](int g) { return tile0 + (g / npass) * tstride; };
+  // weight quants of pass g for all 128 rows -> raw stage g % STAGES
+  auto issue_raw = [&](int g) {
+    const int row0 = pass_tile(g) * kTcM;
+    const int k0 = kc0 + (g % npass) * PK, pk = min(PK, kc0 + KR - k0);
     const int chunks = (q8 ? pk : 2 * pk) / 16;
-    unsigned char* dst = sm + (p % kRawStages) * kRawBytes;
+    unsigned char* dst = sm + (g % STAGES) * kRawBytes;
     for (int c = t; c < kTcM * 8; c += kMmThreads) {
       const int r = c >> 3, ch = c & 7;
       if (ch < chunks) {
         const bool ok = row0 + r < a.rows;
         const uint8_t* src = a.W + static_cast<size_t>(ok ? row0 + r : 0) * a.rb + (q8 ? k0 : 2 * k0) + ch * 16;
-        cp_async16(dst + r * kRawStride + ch * 16, src, ok);
+        cp_async16(dst + r * kPassBytes + ((ch ^ (r & 7)) << 4), src, ok);
       }
     }
     cp_async_commit();
   };
+  // f16 scale bits of this thread's row for the blocks of pass g
+  auto load_scales = [&](int g, uint16_t (&sb)[4]) {
+    const int row = pass_tile(g) * kTcM + t;
+    const int k0 = kc0 + (g % npass) * PK, nblk = min(PK, kc0 + KR - k0) / 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      sb[i] = (q8 && g < total && row < a.rows && i < nblk)
+                  ? ld_weights_u16(a.W + static_cast<size_t>(row) * a.rb + a.K + 2 * (k0 / 32 + i))
+                  : static_cast<uint16_t>(0);
+  };
   if (t == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
     fence_mbar_init();
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(&tmem_base)), "n"(kTmemCols)
+                     smem_addr(&tmem_base)), "n"(CFG::tmem)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // weights never depend on earlier kernels: their loads start before the wait
-  issue_raw(0);
-  if (npass > 1) issue_raw(1);
+  for (int g = 0; g < STAGES - 1; ++g) {
+    if (g < total) issue_raw(g);
+    else cp_async_commit();  // empty groups keep the group count uniform
+  }
+  uint16_t sc_next[4];
+  load_scales(0, sc_next);
   pdl_wait();
   pdl_launch_dependents();
-  if (t < kTcN) {
-    float r = 1.f;
-    if (a.gain) {
-      float ss = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < a.nss; ++i) ss += __ldcg(a.ss + i * kTcN + t);
-      r = rsqrtf(ss / static_cast<float>(a.K) + a.eps);
+  // inputs of the previous kernel: the RMSNorm sums of squares and B for the
+  // CTA's whole K range (16 batch rows x KR activations times the gain, three
+  // bf16 parts per sub-chunk: rows 0-15, 16-31, 32-47 of the N = 48 operand)
+  {
+    float ss = 0.f;
+    if (a.gain)
+      for (int i = t; i < a.nss * kTcN; i += kMmThreads) ss += __ldcg(a.ss + i);  // sequence i % 16 = t % 16
+    const int nsubs = (KR + kSubK - 1) / kSubK;
+    const int b = t >> 3, k8 = (t & 7) * 8;
+    for (int s0 = 0; s0 < nsubs; s0 += 4) {
+      float4 xv[4][2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xv[i][0] = xv[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int sidx = s0 + i;
+        if (sidx < nsubs && b < a.n && k8 < min(kSubK, KR - sidx * kSubK)) {
+          const float* src = a.X + static_cast<size_t>(b) * a.ldx + kc0 + sidx * kSubK + k8;
+          xv[i][0] = __ldcg(reinterpret_cast<const float4*>(src));
+          xv[i][1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+          if (a.gain) {
+            const float* gp = a.gain + kc0 + sidx * kSubK + k8;
+            const float4 g0 = __ldg(reinterpret_cast<const float4*>(gp));
+            const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp + 4));
+            xv[i][0].x *= g0.x; xv[i][0].y *= g0.y; xv[i][0].z *= g0.z; xv[i][0].w *= g0.w;
+            xv[i][1].x *= g1.x; xv[i][1].y *= g1.y; xv[i][1].z *= g1.z; xv[i][1].w *= g1.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int sidx = s0 + i;
+        if (sidx >= nsubs) break;
+        const float x[8] = {xv[i][0].x, xv[i][0].y, xv[i][0].z, xv[i][0].w,
+                            xv[i][1].x, xv[i][1].y, xv[i][1].z, xv[i][1].w};
+        uint32_t p1[8], p2[8], p3[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split3_bf16(x[e], p1[e], p2[e], p3[e]);
+        unsigned char* B = sm + CFG::b + sidx * kBBytes + core_off16(b, k8);
+        *reinterpret_cast<uint4*>(B) =
+            make_uint4(p1[0] | (p1[1] << 16), p1[2] | (p1[3] << 16), p1[4] | (p1[5] << 16), p1[6] | (p1[7] << 16));
+        *reinterpret_cast<uint4*>(B + kBPartBytes) =
+            make_uint4(p2[0] | (p2[1] << 16), p2[2] | (p2[3] << 16), p2[4] | (p2[5] << 16), p2[6] | (p2[7] << 16));
+        *reinterpret_cast<uint4*>(B + 2 * kBPartBytes) =
+            make_uint4(p3[0] | (p3[1] << 16), p3[2] | (p3[3] << 16), p3[4] | (p3[5] << 16), p3[6] | (p3[7] << 16));
+      }
     }
-    inv_rms[t] = r;
+    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 16);
+    if (lane < kTcN) wred_v[warp][lane] = ss;
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (t < kTcN)
+    inv_rms[t] = a.gain ? rsqrtf((wred_v[0][t] + wred_v[1][t] + wred_v[2][t] + wred_v[3][t]) / static_cast<float>(a.K) +
+                                 a.eps)
+                        : 1.f;
   const uint32_t dt = tmem_base;
   const uint32_t lane_addr = dt + (static_cast<uint32_t>(warp * 32) << 16);
   float acc[kTcN];
 #pragma unroll
   for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
   float s_cur[4], s_prev[4];
-  uint32_t ph[4] = {0u, 0u, 0u, 0u};
+  uint32_t ph[2] = {0u, 0u};
   bool ok = true;
-  int sub = 0, nblk_prev = 0;
+  int nblk_prev = 0;
+  const int b_ep = t & (kTcN - 1);  // the sequence this thread's epilogue items belong to
+  float ssum = 0.f, bv = -INFINITY;
+  int bi = INT_MAX;
+  float* recv = reinterpret_cast<float*>(sm + CFG::recv);
   // read out pass q: scale each block's column sums and add them up
   auto readout = [&](int q, const float (&sc)[4], int nblk) {
-    if (!mbar_wait_bounded(&bars[2 + (q & 1)], ph[2 + (q & 1)], a.err)) ok = false;
-    ph[2 + (q & 1)] ^= 1u;
+    if (!mbar_wait_bounded(&bars[q & 1], ph[q & 1], a.err)) ok = false;
+    ph[q & 1] ^= 1u;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t base = lane_addr + (DBL ? (q & 1) * 256 : 0);
     for (int blk = 0; blk < nblk; ++blk) {
       float v[16];
-      tmem_ld16(lane_addr + (q & 1) * 64 + blk * 16, v);
+      tmem_block_sum(base + blk * kTcN3, v);
 #pragma unroll
       for (int b = 0; b < kTcN; ++b) acc[b] = fmaf(sc[blk], v[b], acc[b]);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   };
-  for (int p = 0; p < npass; ++p) {
+  // reduce one tile's sums over the cluster (each CTA pushes its partials of
+  // the rows another CTA owns into that CTA's shared memory) and apply the
+  // epilogue; thread t handles row pairs (2m, 2m+1) of the rows this CTA owns
+  // for sequence t % 16, summing the partials in rank order
+  auto epilogue = [&](int tile, bool more) {
+    const int rpc = kTcM / a.cs, row0 = tile * kTcM;
+    {
+      const int q = t / rpc, lr = t - q * rpc;
+      const uint32_t dst = mapa_u32(recv + (rank * rpc + lr) * kTcN, static_cast<uint32_t>(q));
+#pragma unroll
+      for (int i = 0; i < kTcN / 4; ++i)
+        st_dsmem4(dst + 16 * i, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+#pragma unroll
+      for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
+    }
+    cluster_sync();
+    const float sc = inv_rms[b_ep];
+    for (int idx = t; idx < rpc * (kTcN / 2); idx += kMmThreads) {
+      const int lr = 2 * (idx / kTcN);
+      float v0 = 0.f, v1 = 0.f;
+      for (int q = 0; q < a.cs; ++q) {
+        v0 += recv[(q * rpc + lr) * kTcN + b_ep];
+        v1 += recv[(q * rpc + lr + 1) * kTcN + b_ep];
+      }
+      v0 *= sc;
+      v1 *= sc;
+      const int r0 = row0 + rank * rpc + lr, r1 = r0 + 1;
+      if (b_ep >= a.n || r0 >= a.rows) continue;
+      const bool ok1 = r1 < a.rows;
+      if (a.epi == kEpiSwiGLU) {
+        a.Y[static_cast<size_t>(b_ep) * a.ldy + (r0 >> 1)] = silu_mul(v0, v1);
+      } else if (a.epi == kEpiArgmax) {
+        float* lg = a.seqs[b_ep].logits;
+        lg[r0] = v0;
+        argmax_merge(bv, bi, v0, r0);
+        if (ok1) {
+          lg[r1] = v1;
+          argmax_merge(bv, bi, v1, r1);
+        }
+      } else {
+        float* y = a.Y + static_cast<size_t>(b_ep) * a.ldy;
+        if (a.epi == kEpiResid) {
+          v0 += y[r0];
+          if (ok1) v1 += y[r1];
+          ssum = fmaf(v0, v0, ssum);
+          if (ok1) ssum = fmaf(v1, v1, ssum);
+        }
+        y[r0] = v0;
+        if (ok1) y[r1] = v1;
+      }
+    }
+    if (more) cluster_sync();  // this tile's partials are read before the next tile's arrive
+  };
+  for (int g = 0; g < total; ++g) {
+    const int p = g % npass;
     const int k0 = kc0 + p * PK, pk = min(PK, kc0 + KR - k0);
     const int nblk = pk / 32;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      s_cur[i] = 1.f;
-      if (q8) {
-        s_cur[i] = 0.f;
-        if (row_ok && i < nblk)
-          s_cur[i] = __half2float(__ushort_as_half(ld_weights_u16(a.W + static_cast<size_t>(row) * a.rb + a.K +
-                                                                   2 * (k0 / 32 + i))));
-      }
-    }
-    if (p + 1 < npass) cp_async_wait<1>();
-    else cp_async_wait<0>();
+    for (int i = 0; i < 4; ++i) s_cur[i] = q8 ? __half2float(__ushort_as_half(sc_next[i])) : 1.f;
+    load_scales(g + 1, sc_next);
+    // keep STAGES - 1 passes in flight ahead of this one
+    if (g + STAGES - 1 < total) issue_raw(g + STAGES - 1);
+    else cp_async_commit();
+    cp_async_wait<STAGES - 1>();
     __syncthreads();
-    const unsigned char* raw = sm + (p % kRawStages) * kRawBytes + t * kRawStride;
-    const int nsub = (pk + kSubK - 1) / kSubK;
-    for (int j = 0; j < nsub; ++j, ++sub) {
-      const int u = sub & 1;
-      const int sk = min(kSubK, pk - j * kSubK);  // 64 or 32
-      if (sub >= 2) {
-        if (!mbar_wait_bounded(&bars[u], ph[u], a.err)) ok = false;
-        ph[u] ^= 1u;
-      }
-      unsigned char* A = sm + kOffA + u * kABytes;
-      unsigned char* B = sm + kOffB + u * kBBytes;
-      {  // B: 16 batch rows x sk activations (times the gain), three bf16 parts
-        const int b = t >> 3, k8 = (t & 7) * 8;
-        if (k8 < sk) {
-          const int kg = k0 + j * kSubK + k8;
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
-          if (b < a.n) {
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(a.X + static_cast<size_t>(b) * a.ldx + kg));
-            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(a.X + static_cast<size_t>(b) * a.ldx + kg + 4));
-            x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-            x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
-            if (a.gain) {
-              const float4 g0 = __ldg(reinterpret_cast<const float4*>(a.gain + kg));
-              const float4 g1 = __ldg(reinterpret_cast<const float4*>(a.gain + kg + 4));
-              x[0] *= g0.x; x[1] *= g0.y; x[2] *= g0.z; x[3] *= g0.w;
-              x[4] *= g1.x; x[5] *= g1.y; x[6] *= g1.z; x[7] *= g1.w;
-            }
-          }
-          uint32_t p1[8], p2[8], p3[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) split3_bf16(x[e], p1[e], p2[e], p3[e]);
-          const uint32_t off = core_off16(b, k8);
-          *reinterpret_cast<uint4*>(B + off) =
-              make_uint4(p1[0] | (p1[1] << 16), p1[2] | (p1[3] << 16), p1[4] | (p1[5] << 16), p1[6] | (p1[7] << 16));
-          *reinterpret_cast<uint4*>(B + kBPartBytes + off) =
-              make_uint4(p2[0] | (p2[1] << 16), p2[2] | (p2[3] << 16), p2[4] | (p2[5] << 16), p2[6] | (p2[7] << 16));
-          *reinterpret_cast<uint4*>(B + 2 * kBPartBytes + off) =
-              make_uint4(p3[0] | (p3[1] << 16), p3[2] | (p3[3] << 16), p3[4] | (p3[5] << 16), p3[6] | (p3[7] << 16));
-        }
-      }
-      // A: this thread's row of the sub-chunk as bf16
-      if (q8) {
-        for (int v = 0; v < sk / 16; ++v) {
-          const uint4 w = *reinterpret_cast<const uint4*>(raw + j * kSubK + v * 16);
-          uint32_t o[8];
-          i8x4_to_bf16x4(w.x, o[0], o[1]);
-          i8x4_to_bf16x4(w.y, o[2], o[3]);
-          i8x4_to_bf16x4(w.z, o[4], o[5]);
-          i8x4_to_bf16x4(w.w, o[6], o[7]);
-          *reinterpret_cast<uint4*>(A + core_off16(t, v * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(A + core_off16(t, v * 16 + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-      } else {
-        for (int v = 0; v < sk / 8; ++v)
-          *reinterpret_cast<uint4*>(A + core_off16(t, v * 8)) =
-              *reinterpret_cast<const uint4*>(raw + 2 * j * kSubK + v * 16);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncthreads();
-      if (t == 0) {
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t col0 = (p & 1) * 64;
-        for (int bk = 0; bk < sk / 32; ++bk) {
-          const uint32_t d = dt + col0 + (j * 2 + bk) * 16;
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint32_t koff = (bk * 2 + ks) * 256;  // 16 K = two core matrices
-            const uint64_t ad = smem_desc(A + koff, 128, (kSubK / 8) * 128);
-#pragma unroll
-            for (int pt = 0; pt < 3; ++pt)
-              mma_bf16(d, ad, smem_desc(B + pt * kBPartBytes + koff, 128, (kSubK / 8) * 128),
-                       (ks | pt) ? 1u : 0u);
-          }
-        }
-        mma_commit(&bars[u]);
-        if (j == nsub - 1) mma_commit(&bars[2 + (p & 1)]);
-      }
+    if (!DBL && g > 0) {  // one buffer: read the previous pass out before its A and columns are reused
+      readout(g - 1, s_prev, nblk_prev);
+      if ((g - 1) % npass == npass - 1) epilogue(pass_tile(g - 1), true);
     }
-    // every thread is past its last read of this raw stage: refill it
-    if (p + kRawStages < npass) issue_raw(p + kRawStages);
-    if (p > 0) readout(p - 1, s_prev, nblk_prev);
+    // A: this thread's row of the pass as bf16, both sub-chunks
+    const unsigned char* raw = sm + (g % STAGES) * kRawBytes + t * kPassBytes;
+    unsigned char* A = sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
+    if (q8) {
+      for (int ch = 0; ch < pk / 16; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + ((ch ^ (t & 7)) << 4));
+        uint32_t o[8];
+        i8x4_to_bf16x4(w.x, o[0], o[1]);
+        i8x4_to_bf16x4(w.y, o[2], o[3]);
+        i8x4_to_bf16x4(w.z, o[4], o[5]);
+        i8x4_to_bf16x4(w.w, o[6], o[7]);
+        unsigned char* As = A + (ch >> 2) * kABytes;
+        const int kk = (ch & 3) * 16;
+        *reinterpret_cast<uint4*>(As + core_off16(t, kk)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(As + core_off16(t, kk + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    } else {
+      for (int ch = 0; ch < pk / 8; ++ch)
+        *reinterpret_cast<uint4*>(A + core_off16(t, ch * 8)) =
+            *reinterpret_cast<const uint4*>(raw + ((ch ^ (t & 7)) << 4));
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (t == 0) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const unsigned char* Bp = sm + CFG::b + ((k0 - kc0) / kSubK) * kBBytes;
+      const uint32_t col0 = DBL ? (g & 1) * 256 : 0;
+      for (int blk = 0; blk < nblk; ++blk) {
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          const uint32_t koff = (blk >> 1) * kABytes + ((blk & 1) * 2 + ks) * 256;  // 16 K = two core matrices
+          const uint32_t boff = (blk >> 1) * kBBytes + ((blk & 1) * 2 + ks) * 256;
+          mma_bf16(dt + col0 + blk * kTcN3, smem_desc(A + koff, 128, (kSubK / 8) * 128),
+                   smem_desc(Bp + boff, 128, (kSubK / 8) * 128), ks ? 1u : 0u);
+        }
+      }
+      mma_commit(&bars[g & 1]);
+    }
+    if (DBL && g > 0) {
+      readout(g - 1, s_prev, nblk_prev);
+      if ((g - 1) % npass == npass - 1) epilogue(pass_tile(g - 1), true);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) s_prev[i] = s_cur[i];
     nblk_prev = nblk;
   }
-  readout(npass - 1, s_prev, nblk_prev);
+  if (total > 0) {
+    readout(total - 1, s_prev, nblk_prev);
+    epilogue(pass_tile(total - 1), false);
+  }
+  cp_async_wait<0>();
   __syncthreads();
   if (warp == 0) {  // the tensor memory is released on every path
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(dt), "n"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(dt), "n"(CFG::tmem) : "memory");
   }
   (void)ok;  // a timed-out wait has set the error word; the host reports it
-  // cluster reduction of the K partials, then the epilogue; thread t handles
-  // row pairs (2m, 2m+1) of this CTA's share of the tile for sequence t % 16
-  float* red = reinterpret_cast<float*>(sm + kOffRed);
-#pragma unroll
-  for (int b = 0; b < kTcN; ++b) red[t * kRedStride + b] = acc[b];
-  cluster_sync();
-  const int rpc = kTcM / a.cs;
-  const int b = t & (kTcN - 1);
-  const float sc = inv_rms[b];
-  float ssum = 0.f, bv = -INFINITY;
-  int bi = INT_MAX;
-  for (int idx = t; idx < rpc * (kTcN / 2); idx += kMmThreads) {
-    const int lr = rank * rpc + 2 * (idx / kTcN);
-    float v0 = 0.f, v1 = 0.f;
-    for (int q = 0; q < a.cs; ++q) {
-      v0 += ld_dsmem(red + lr * kRedStride + b, static_cast<uint32_t>(q));
-      v1 += ld_dsmem(red + (lr + 1) * kRedStride + b, static_cast<uint32_t>(q));
-    }
-    v0 *= sc;
-    v1 *= sc;
-    const int r0 = row0 + lr, r1 = r0 + 1;
-    if (b >= a.n || r0 >= a.rows) continue;
-    const bool ok1 = r1 < a.rows;
-    if (a.epi == kEpiSwiGLU) {
-      a.Y[static_cast<size_t>(b) * a.ldy + (r0 >> 1)] = silu_mul(v0, v1);
-    } else if (a.epi == kEpiArgmax) {
-      float* lg = a.seqs[b].logits;
-      lg[r0] = v0;
-      argmax_merge(bv, bi, v0, r0);
-      if (ok1) {
-        lg[r1] = v1;
-        argmax_merge(bv, bi, v1, r1);
-      }
-    } else {
-      float* y = a.Y + static_cast<size_t>(b) * a.ldy;
-      if (a.epi == kEpiResid) {
-        v0 += y[r0];
-        if (ok1) v1 += y[r1];
-        ssum = fmaf(v0, v0, ssum);
-        if (ok1) ssum = fmaf(v1, v1, ssum);
-      }
-      y[r0] = v0;
-      if (ok1) y[r1] = v1;
-    }
-  }
-  cluster_sync();  // the cluster's partials are no longer read
   if (a.epi == kEpiResid && a.ss_out) {
     ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, 16);
     if (lane < kTcN) wred_v[warp][lane] = ssum;
@@ -761,14 +826,18 @@ int batch_ss_slots(int H) { return ((H + kTcM - 1) / kTcM) * kMaxCluster; }
 
 bool batch_supported(const DevModel& m) {
   const int G = m.nq / m.nkv;
-  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && m.H % 64 == 0 && m.qw % 64 == 0 &&
-         m.I % 64 == 0 && attn_batch_smem(m) <= 227 * 1024;
+  auto split_ok = [](int K) { return K % 64 == 0 && K / mm_cluster(K) <= kSplitMaxK; };
+  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && split_ok(m.H) && split_ok(m.qw) &&
+         split_ok(m.I) && m.H <= kHeadMaxK && attn_batch_smem(m) <= 227 * 1024;
 }
 
 cudaError_t batch_setup(const DevModel& m) {
-  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16),
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<SplitCfg>),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kMmSmem));
+                                       static_cast<int>(SplitCfg::total));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<HeadCfg>),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(HeadCfg::total));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_attn_batch),
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -812,6 +881,10 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
   cudaLaunchConfig_t ce = config(n, 256, 0, 1);
   cudaError_t e = cudaLaunchKernelEx(&ce, k_embed_batch, m, seqs, n, X, ss_x, nss_x);
   if (e != cudaSuccess) return e;
+  int dev = 0, num_sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
   auto mm = [&](const uint8_t* W, size_t rb, int K, int rows, const float* Xin, int ldx, const float* gain,
                 const float* ss, int nss, int epi, float* Y, int ldy, float* ss_out, bool split) {
     MmArgs a{};
@@ -821,8 +894,12 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
     a.epi = epi; a.Y = Y; a.ldy = ldy; a.ss_out = ss_out;
     a.seqs = seqs; a.count = count; a.err = err; a.max_seq = m.max_seq;
     const int tiles = (rows + kTcM - 1) / kTcM;
-    cudaLaunchConfig_t c = config(tiles * a.cs, kMmThreads, kMmSmem, a.cs);
-    return cudaLaunchKernelEx(&c, k_mm16, a);
+    if (split) {
+      cudaLaunchConfig_t c = config(tiles * a.cs, kMmThreads, SplitCfg::total, a.cs);
+      return cudaLaunchKernelEx(&c, k_mm16<SplitCfg>, a);
+    }
+    cudaLaunchConfig_t c = config(std::min(tiles, num_sms), kMmThreads, HeadCfg::total, 1);
+    return cudaLaunchKernelEx(&c, k_mm16<HeadCfg>, a);
   };
   const int lqkv = m.qw + 2 * m.kvw;
   for (int l = 0; l < m.n_layers; ++l) {
