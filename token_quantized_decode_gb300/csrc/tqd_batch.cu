@@ -598,7 +598,7 @@ __device__ __forceinline__ void async() { asm volatile("bar.sync 1, %0;" ::"n"(k
 template <int HD, int G>
 __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, int g, int c, int nch,
                                 const float* qkv, float* attn, unsigned char* sm) {
-  constexpr int NJ = HD / 32, DPL = HD / 32;
+  constexpr int NJ = HD / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kASlots * kASlotBytes);
   uint64_t* empty = full + kASlots;
@@ -662,41 +662,66 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
     }
   }
   async();
-  float qv[G][DPL], mm[G], ll[G], oo[G][DPL];
+  // Each warp takes four rows per step, eight lanes per row: lane (rg, g8)
+  // holds elements 32i + 4 g8 + {0..3} (i < HD/32) of its row, so a group's
+  // 16-byte reads are contiguous and a score needs a 3-step shuffle.  Every
+  // group keeps its own online-softmax state over the rows it saw; the four
+  // groups are merged at the end.
+  constexpr int NC4 = HD / 32;        // float4 chunks per lane
+  const int rg = lane >> 3, g8 = lane & 7;
+  float4 qv[G][NC4], oo[G][NC4];
+  float mm[G], ll[G];
 #pragma unroll
   for (int hh = 0; hh < G; ++hh) {
     mm[hh] = -INFINITY;
     ll[hh] = 0.f;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      qv[hh][e] = qs[hh * HD + lane * DPL + e];
-      oo[hh][e] = 0.f;
+    for (int i = 0; i < NC4; ++i) {
+      qv[hh][i] = *reinterpret_cast<const float4*>(qs + hh * HD + 32 * i + 4 * g8);
+      oo[hh][i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  auto row_update = [&](const float* kr, const float* vr) {
-    float kf[DPL], vf[DPL];
+  // one row for this lane's group (all 32 lanes call it; `valid` masks the update)
+  auto row_update = [&](const float* kr, const float* vr, bool valid) {
+    float4 kf[NC4];
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      kf[e] = kr[lane * DPL + e];
-      vf[e] = vr[lane * DPL + e];
-    }
+    for (int i = 0; i < NC4; ++i) kf[i] = *reinterpret_cast<const float4*>(kr + 32 * i + 4 * g8);
+    float sc[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
       float d = 0.f;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) d = fmaf(qv[hh][e], kf[e], d);
-      const float sc = warp_sum(d) * m.attn_scale;
-      if (sc > mm[hh]) {
-        const float corr = expf(mm[hh] - sc);
-        mm[hh] = sc;
-        ll[hh] = ll[hh] * corr + 1.f;
+      for (int i = 0; i < NC4; ++i) {
+        d = fmaf(qv[hh][i].x, kf[i].x, d);
+        d = fmaf(qv[hh][i].y, kf[i].y, d);
+        d = fmaf(qv[hh][i].z, kf[i].z, d);
+        d = fmaf(qv[hh][i].w, kf[i].w, d);
+      }
+      d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
+      d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
+      d += __shfl_xor_sync(0xFFFFFFFFu, d, 4);
+      sc[hh] = d * m.attn_scale;
+    }
+    if (!valid) return;
+    float4 vf[NC4];
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) oo[hh][e] = fmaf(oo[hh][e], corr, vf[e]);
+    for (int i = 0; i < NC4; ++i) vf[i] = *reinterpret_cast<const float4*>(vr + 32 * i + 4 * g8);
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      float corr = 1.f, p = 1.f;
+      if (sc[hh] > mm[hh]) {
+        corr = expf(mm[hh] - sc[hh]);
+        mm[hh] = sc[hh];
       } else {
-        const float p = expf(sc - mm[hh]);
-        ll[hh] += p;
+        p = expf(sc[hh] - mm[hh]);
+      }
+      ll[hh] = fmaf(ll[hh], corr, p);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) oo[hh][e] = fmaf(p, vf[e], oo[hh][e]);
+      for (int i = 0; i < NC4; ++i) {
+        oo[hh][i].x = fmaf(p, vf[i].x, oo[hh][i].x * corr);
+        oo[hh][i].y = fmaf(p, vf[i].y, oo[hh][i].y * corr);
+        oo[hh][i].z = fmaf(p, vf[i].z, oo[hh][i].z * corr);
+        oo[hh][i].w = fmaf(p, vf[i].w, oo[hh][i].w * corr);
       }
     }
   };
@@ -707,24 +732,53 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
     mbar_wait_bounded(full + slot, (n / kASlots) & 1u, err);
     const float* Ks = reinterpret_cast<const float*>(sm + slot * kASlotBytes);
     const float* Vs = Ks + static_cast<size_t>(rpp) * HD;
-    for (int r = warp; r < cnt; r += kAW) row_update(Ks + r * HD, Vs + r * HD);
+    for (int r0 = 4 * warp; r0 < cnt; r0 += 4 * kAW) {
+      const int r = min(r0 + rg, cnt - 1);
+      row_update(Ks + r * HD, Vs + r * HD, r0 + rg < cnt);
+    }
     __syncwarp();
     if (lane == 0)
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(empty + slot)) : "memory");
   }
-  if (has_new && warp == ((tc - t0) % kAW)) row_update(knew, vnew);
-  const int stride = HD + 2;
+  if (has_new && warp == kAW - 1) row_update(knew, vnew, rg == 0);
+  // merge the four groups of the warp (lanes g8, g8+8, g8+16, g8+24 hold the
+  // same elements), then publish the warp's state
 #pragma unroll
   for (int hh = 0; hh < G; ++hh) {
-    float* w = wst + (warp * G + hh) * stride;
+    float M = mm[hh];
+    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 8));
+    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, 16));
+    const float f = M == -INFINITY ? 0.f : expf(mm[hh] - M);
+    float l = ll[hh] * f;
+    l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
+    l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+    float* w = wst + (warp * G + hh) * (HD + 2);
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) w[lane * DPL + e] = oo[hh][e];
+    for (int i = 0; i < NC4; ++i) {
+      float4 o = oo[hh][i];
+      o.x *= f; o.y *= f; o.z *= f; o.w *= f;
+      o.x += __shfl_xor_sync(0xFFFFFFFFu, o.x, 8);
+      o.y += __shfl_xor_sync(0xFFFFFFFFu, o.y, 8);
+      o.z += __shfl_xor_sync(0xFFFFFFFFu, o.z, 8);
+      o.w += __shfl_xor_sync(0xFFFFFFFFu, o.w, 8);
+      o.x += __shfl_xor_sync(0xFFFFFFFFu, o.x, 16);
+      o.y += __shfl_xor_sync(0xFFFFFFFFu, o.y, 16);
+      o.z += __shfl_xor_sync(0xFFFFFFFFu, o.z, 16);
+      o.w += __shfl_xor_sync(0xFFFFFFFFu, o.w, 16);
+      if (rg == 0) {
+        w[32 * i + 4 * g8] = o.x;
+        w[32 * i + 4 * g8 + 1] = o.y;
+        w[32 * i + 4 * g8 + 2] = o.z;
+        w[32 * i + 4 * g8 + 3] = o.w;
+      }
+    }
     if (lane == 0) {
-      w[HD] = mm[hh];
-      w[HD + 1] = ll[hh];
+      w[HD] = M;
+      w[HD + 1] = l;
     }
   }
   async();
+  const int stride = HD + 2;
   for (int idx = threadIdx.x; idx < G * HD; idx += kAT) {
     const int hh = idx / HD, d = idx - hh * HD;
     float M = -INFINITY;
@@ -775,7 +829,8 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
   if (threadIdx.x == 0) s.attn_count[g] = 0u;
 }
 
-__global__ void __launch_bounds__(kAT + 32, 1)
+template <int HD, int G>
+__global__ void __launch_bounds__(kAT + 32, 2)
     k_attn_batch(DevModel m, const DevSeq* seqs, int layer, int nch, const float* QKV, float* ATTN) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int per_seq = m.nkv * nch;
@@ -794,21 +849,25 @@ __global__ void __launch_bounds__(kAT + 32, 1)
   if (s.state->pos >= static_cast<uint32_t>(m.max_seq)) return;
   const float* qkv = QKV + static_cast<size_t>(b) * (m.qw + 2 * m.kvw);
   float* attn = ATTN + static_cast<size_t>(b) * m.qw;
+  attn_batch_item<HD, G>(m, s, layer, g, c, nch, qkv, attn, sm);
+}
+
+// The attention kernel instantiated for the model's head_dim and group size.
+const void* attn_batch_fn(const DevModel& m) {
   const int G = m.nq / m.nkv;
   if (m.hd == 128) {
     switch (G) {
-      case 1: attn_batch_item<128, 1>(m, s, layer, g, c, nch, qkv, attn, sm); break;
-      case 2: attn_batch_item<128, 2>(m, s, layer, g, c, nch, qkv, attn, sm); break;
-      case 3: attn_batch_item<128, 3>(m, s, layer, g, c, nch, qkv, attn, sm); break;
-      default: attn_batch_item<128, 4>(m, s, layer, g, c, nch, qkv, attn, sm); break;
+      case 1: return reinterpret_cast<const void*>(&k_attn_batch<128, 1>);
+      case 2: return reinterpret_cast<const void*>(&k_attn_batch<128, 2>);
+      case 3: return reinterpret_cast<const void*>(&k_attn_batch<128, 3>);
+      default: return reinterpret_cast<const void*>(&k_attn_batch<128, 4>);
     }
-  } else {
-    switch (G) {
-      case 1: attn_batch_item<64, 1>(m, s, layer, g, c, nch, qkv, attn, sm); break;
-      case 2: attn_batch_item<64, 2>(m, s, layer, g, c, nch, qkv, attn, sm); break;
-      case 3: attn_batch_item<64, 3>(m, s, layer, g, c, nch, qkv, attn, sm); break;
-      default: attn_batch_item<64, 4>(m, s, layer, g, c, nch, qkv, attn, sm); break;
-    }
+  }
+  switch (G) {
+    case 1: return reinterpret_cast<const void*>(&k_attn_batch<64, 1>);
+    case 2: return reinterpret_cast<const void*>(&k_attn_batch<64, 2>);
+    case 3: return reinterpret_cast<const void*>(&k_attn_batch<64, 3>);
+    default: return reinterpret_cast<const void*>(&k_attn_batch<64, 4>);
   }
 }
 
@@ -839,8 +898,7 @@ cudaError_t batch_setup(const DevModel& m) {
   e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<HeadCfg>),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(HeadCfg::total));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_attn_batch),
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(attn_batch_fn(m), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(attn_batch_smem(m)));
 }
 
@@ -902,15 +960,22 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
     return cudaLaunchKernelEx(&c, k_mm16<HeadCfg>, a);
   };
   const int lqkv = m.qw + 2 * m.kvw;
+  const void* attn_fn = attn_batch_fn(m);
   for (int l = 0; l < m.n_layers; ++l) {
     const DevLayer& L = host_layers[l];
     if ((e = mm(L.wqkv, m.row_bytes_h, m.H, lqkv, X, m.H, L.attn_norm, ss_x, nss_x, kEpiStore, QKV, lqkv,
                 nullptr, true)) != cudaSuccess)
       return e;
     cudaLaunchConfig_t ca = config(n * m.nkv * nch, kAT + 32, attn_batch_smem(m), 1);
-    if ((e = cudaLaunchKernelEx(&ca, k_attn_batch, m, seqs, l, nch, static_cast<const float*>(QKV), ATTN)) !=
-        cudaSuccess)
-      return e;
+    {
+      DevModel mm_ = m;
+      const DevSeq* sq = seqs;
+      int layer = l, nc = nch;
+      const float* q = QKV;
+      float* o = ATTN;
+      void* args[] = {&mm_, &sq, &layer, &nc, &q, &o};
+      if ((e = cudaLaunchKernelExC(&ca, attn_fn, args)) != cudaSuccess) return e;
+    }
     if ((e = mm(L.wo, m.row_bytes_qw, m.qw, m.H, ATTN, m.qw, nullptr, nullptr, 0, kEpiResid, X, m.H, ss_mid,
                 true)) != cudaSuccess)
       return e;
