@@ -822,8 +822,9 @@ int32_t check_batch(tqd_model* m, int32_t n_seq) {
 int32_t run_batch(tqd_model* m, int n, int steps) {
   cudaGraphExec_t& g = m->bgraph[n];
   if (!g) {
-    // split-K chunks: about four attention blocks per SM
-    int nch = (4 * m->num_sms + n * m->dm.nkv - 1) / (n * m->dm.nkv);
+    // split-K chunks: as many as keep every (sequence, kv head, chunk) block
+    // in one wave at two blocks per SM (a partial last wave would run alone)
+    int nch = 2 * m->num_sms / (n * m->dm.nkv);
     if (nch > m->dm.n_chunks) nch = m->dm.n_chunks;
     if (nch < 1) nch = 1;
     m->batch_nch = nch;
