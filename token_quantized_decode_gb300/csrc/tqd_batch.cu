@@ -261,6 +261,126 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   }
   uint16_t sc_next[4];
   load_scales(0, sc_next);
+  float sc[2][4];   // scales of the passes in flight, by pass parity
+  int nbk[2] = {0, 0};
+  float acc[kTcN];
+#pragma unroll
+  for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
+  uint32_t ph[2] = {0u, 0u};
+  bool ok = true;
+  const int b_ep = t & (kTcN - 1);  // the sequence this thread's epilogue items belong to
+  float ssum = 0.f, bv = -INFINITY;
+  int bi = INT_MAX;
+  float* recv = reinterpret_cast<float*>(sm + CFG::recv);
+  uint32_t lane_addr = 0;
+  // read out pass q: scale each block's column sums and add them up
+  auto readout = [&](int q) {
+    if (!mbar_wait_bounded(&bars[q & 1], ph[q & 1], a.err)) ok = false;
+    ph[q & 1] ^= 1u;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t base = lane_addr + (DBL ? (q & 1) * 256 : 0);
+    for (int blk = 0; blk < nbk[q & 1]; ++blk) {
+      float v[16];
+      tmem_block_sum(base + blk * kTcN3, v);
+#pragma unroll
+      for (int b = 0; b < kTcN; ++b) acc[b] = fmaf(sc[q & 1][blk], v[b], acc[b]);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  };
+  // reduce one tile's sums over the cluster (each CTA pushes its partials of
+  // the rows another CTA owns into that CTA's shared memory) and apply the
+  // epilogue; thread t handles row pairs (2m, 2m+1) of the rows this CTA owns
+  // for sequence t % 16, summing the partials in rank order
+  auto epilogue = [&](int tile, bool more) {
+    const int rpc = kTcM / a.cs, row0 = tile * kTcM;
+    {
+      const int q = t / rpc, lr = t - q * rpc;
+      const uint32_t dst = mapa_u32(recv + (rank * rpc + lr) * kTcN, static_cast<uint32_t>(q));
+#pragma unroll
+      for (int i = 0; i < kTcN / 4; ++i)
+        st_dsmem4(dst + 16 * i, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+#pragma unroll
+      for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
+    }
+    cluster_sync();
+    const float scl = inv_rms[b_ep];
+    for (int idx = t; idx < rpc * (kTcN / 2); idx += kMmThreads) {
+      const int lr = 2 * (idx / kTcN);
+      float v0 = 0.f, v1 = 0.f;
+      for (int q = 0; q < a.cs; ++q) {
+        v0 += recv[(q * rpc + lr) * kTcN + b_ep];
+        v1 += recv[(q * rpc + lr + 1) * kTcN + b_ep];
+      }
+      v0 *= scl;
+      v1 *= scl;
+      const int r0 = row0 + rank * rpc + lr, r1 = r0 + 1;
+      if (b_ep >= a.n || r0 >= a.rows) continue;
+      const bool ok1 = r1 < a.rows;
+      if (a.epi == kEpiSwiGLU) {
+        a.Y[static_cast<size_t>(b_ep) * a.ldy + (r0 >> 1)] = silu_mul(v0, v1);
+      } else if (a.epi == kEpiArgmax) {
+        float* lg = a.seqs[b_ep].logits;
+        lg[r0] = v0;
+        argmax_merge(bv, bi, v0, r0);
+        if (ok1) {
+          lg[r1] = v1;
+          argmax_merge(bv, bi, v1, r1);
+        }
+      } else {
+        float* y = a.Y + static_cast<size_t>(b_ep) * a.ldy;
+        if (a.epi == kEpiResid) {
+          v0 += y[r0];
+          if (ok1) v1 += y[r1];
+          ssum = fmaf(v0, v0, ssum);
+          if (ok1) ssum = fmaf(v1, v1, ssum);
+        }
+        y[r0] = v0;
+        if (ok1) y[r1] = v1;
+      }
+    }
+    if (more) cluster_sync();  // this tile's partials are read before the next tile's arrive
+  };
+  // wait for pass g's weights and dequantise them into A (this thread's row,
+  // both sub-chunks); with one A / tensor-memory buffer the previous pass is
+  // read out first
+  auto load_pass = [&](int g) {
+    const int k0 = kc0 + (g % npass) * PK, pk = min(PK, kc0 + KR - k0);
+    nbk[g & 1] = pk / 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[g & 1][i] = q8 ? __half2float(__ushort_as_half(sc_next[i])) : 1.f;
+    load_scales(g + 1, sc_next);
+    // keep STAGES - 1 passes in flight ahead of this one
+    if (g + STAGES - 1 < total) issue_raw(g + STAGES - 1);
+    else cp_async_commit();
+    cp_async_wait<STAGES - 1>();
+    __syncthreads();
+    if (!DBL && g > 0) {
+      readout(g - 1);
+      if ((g - 1) % npass == npass - 1) epilogue(pass_tile(g - 1), true);
+    }
+    const unsigned char* raw = sm + (g % STAGES) * kRawBytes + t * kPassBytes;
+    unsigned char* A = sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
+    if (q8) {
+      for (int ch = 0; ch < pk / 16; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + ((ch ^ (t & 7)) << 4));
+        uint32_t o[8];
+        i8x4_to_bf16x4(w.x, o[0], o[1]);
+        i8x4_to_bf16x4(w.y, o[2], o[3]);
+        i8x4_to_bf16x4(w.z, o[4], o[5]);
+        i8x4_to_bf16x4(w.w, o[6], o[7]);
+        unsigned char* As = A + (ch >> 2) * kABytes;
+        const int kk = (ch & 3) * 16;
+        *reinterpret_cast<uint4*>(As + core_off16(t, kk)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(As + core_off16(t, kk + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    } else {
+      for (int ch = 0; ch < pk / 8; ++ch)
+        *reinterpret_cast<uint4*>(A + core_off16(t, ch * 8)) =
+            *reinterpret_cast<const uint4*>(raw + ((ch ^ (t & 7)) << 4));
+    }
+  };
+  // the first pass's weights are dequantised before the wait as well
+  if (total > 0) load_pass(0);
   pdl_wait();
   pdl_launch_dependents();
   // inputs of the previous kernel: the RMSNorm sums of squares and B for the
@@ -320,129 +440,18 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
                                  a.eps)
                         : 1.f;
   const uint32_t dt = tmem_base;
-  const uint32_t lane_addr = dt + (static_cast<uint32_t>(warp * 32) << 16);
-  float acc[kTcN];
-#pragma unroll
-  for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
-  float s_cur[4], s_prev[4];
-  uint32_t ph[2] = {0u, 0u};
-  bool ok = true;
-  int nblk_prev = 0;
-  const int b_ep = t & (kTcN - 1);  // the sequence this thread's epilogue items belong to
-  float ssum = 0.f, bv = -INFINITY;
-  int bi = INT_MAX;
-  float* recv = reinterpret_cast<float*>(sm + CFG::recv);
-  // read out pass q: scale each block's column sums and add them up
-  auto readout = [&](int q, const float (&sc)[4], int nblk) {
-    if (!mbar_wait_bounded(&bars[q & 1], ph[q & 1], a.err)) ok = false;
-    ph[q & 1] ^= 1u;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t base = lane_addr + (DBL ? (q & 1) * 256 : 0);
-    for (int blk = 0; blk < nblk; ++blk) {
-      float v[16];
-      tmem_block_sum(base + blk * kTcN3, v);
-#pragma unroll
-      for (int b = 0; b < kTcN; ++b) acc[b] = fmaf(sc[blk], v[b], acc[b]);
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  };
-  // reduce one tile's sums over the cluster (each CTA pushes its partials of
-  // the rows another CTA owns into that CTA's shared memory) and apply the
-  // epilogue; thread t handles row pairs (2m, 2m+1) of the rows this CTA owns
-  // for sequence t % 16, summing the partials in rank order
-  auto epilogue = [&](int tile, bool more) {
-    const int rpc = kTcM / a.cs, row0 = tile * kTcM;
-    {
-      const int q = t / rpc, lr = t - q * rpc;
-      const uint32_t dst = mapa_u32(recv + (rank * rpc + lr) * kTcN, static_cast<uint32_t>(q));
-#pragma unroll
-      for (int i = 0; i < kTcN / 4; ++i)
-        st_dsmem4(dst + 16 * i, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-#pragma unroll
-      for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
-    }
-    cluster_sync();
-    const float sc = inv_rms[b_ep];
-    for (int idx = t; idx < rpc * (kTcN / 2); idx += kMmThreads) {
-      const int lr = 2 * (idx / kTcN);
-      float v0 = 0.f, v1 = 0.f;
-      for (int q = 0; q < a.cs; ++q) {
-        v0 += recv[(q * rpc + lr) * kTcN + b_ep];
-        v1 += recv[(q * rpc + lr + 1) * kTcN + b_ep];
-      }
-      v0 *= sc;
-      v1 *= sc;
-      const int r0 = row0 + rank * rpc + lr, r1 = r0 + 1;
-      if (b_ep >= a.n || r0 >= a.rows) continue;
-      const bool ok1 = r1 < a.rows;
-      if (a.epi == kEpiSwiGLU) {
-        a.Y[static_cast<size_t>(b_ep) * a.ldy + (r0 >> 1)] = silu_mul(v0, v1);
-      } else if (a.epi == kEpiArgmax) {
-        float* lg = a.seqs[b_ep].logits;
-        lg[r0] = v0;
-        argmax_merge(bv, bi, v0, r0);
-        if (ok1) {
-          lg[r1] = v1;
-          argmax_merge(bv, bi, v1, r1);
-        }
-      } else {
-        float* y = a.Y + static_cast<size_t>(b_ep) * a.ldy;
-        if (a.epi == kEpiResid) {
-          v0 += y[r0];
-          if (ok1) v1 += y[r1];
-          ssum = fmaf(v0, v0, ssum);
-          if (ok1) ssum = fmaf(v1, v1, ssum);
-        }
-        y[r0] = v0;
-        if (ok1) y[r1] = v1;
-      }
-    }
-    if (more) cluster_sync();  // this tile's partials are read before the next tile's arrive
-  };
+  lane_addr = dt + (static_cast<uint32_t>(warp * 32) << 16);
   for (int g = 0; g < total; ++g) {
-    const int p = g % npass;
-    const int k0 = kc0 + p * PK, pk = min(PK, kc0 + KR - k0);
-    const int nblk = pk / 32;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s_cur[i] = q8 ? __half2float(__ushort_as_half(sc_next[i])) : 1.f;
-    load_scales(g + 1, sc_next);
-    // keep STAGES - 1 passes in flight ahead of this one
-    if (g + STAGES - 1 < total) issue_raw(g + STAGES - 1);
-    else cp_async_commit();
-    cp_async_wait<STAGES - 1>();
-    __syncthreads();
-    if (!DBL && g > 0) {  // one buffer: read the previous pass out before its A and columns are reused
-      readout(g - 1, s_prev, nblk_prev);
-      if ((g - 1) % npass == npass - 1) epilogue(pass_tile(g - 1), true);
-    }
-    // A: this thread's row of the pass as bf16, both sub-chunks
-    const unsigned char* raw = sm + (g % STAGES) * kRawBytes + t * kPassBytes;
-    unsigned char* A = sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
-    if (q8) {
-      for (int ch = 0; ch < pk / 16; ++ch) {
-        const uint4 w = *reinterpret_cast<const uint4*>(raw + ((ch ^ (t & 7)) << 4));
-        uint32_t o[8];
-        i8x4_to_bf16x4(w.x, o[0], o[1]);
-        i8x4_to_bf16x4(w.y, o[2], o[3]);
-        i8x4_to_bf16x4(w.z, o[4], o[5]);
-        i8x4_to_bf16x4(w.w, o[6], o[7]);
-        unsigned char* As = A + (ch >> 2) * kABytes;
-        const int kk = (ch & 3) * 16;
-        *reinterpret_cast<uint4*>(As + core_off16(t, kk)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(As + core_off16(t, kk + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
-      }
-    } else {
-      for (int ch = 0; ch < pk / 8; ++ch)
-        *reinterpret_cast<uint4*>(A + core_off16(t, ch * 8)) =
-            *reinterpret_cast<const uint4*>(raw + ((ch ^ (t & 7)) << 4));
-    }
+    if (g > 0) load_pass(g);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     if (t == 0) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int k0 = kc0 + (g % npass) * PK;
+      unsigned char* A = sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
       const unsigned char* Bp = sm + CFG::b + ((k0 - kc0) / kSubK) * kBBytes;
       const uint32_t col0 = DBL ? (g & 1) * 256 : 0;
-      for (int blk = 0; blk < nblk; ++blk) {
+      for (int blk = 0; blk < nbk[g & 1]; ++blk) {
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
           const uint32_t koff = (blk >> 1) * kABytes + ((blk & 1) * 2 + ks) * 256;  // 16 K = two core matrices
@@ -454,15 +463,12 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
       mma_commit(&bars[g & 1]);
     }
     if (DBL && g > 0) {
-      readout(g - 1, s_prev, nblk_prev);
+      readout(g - 1);
       if ((g - 1) % npass == npass - 1) epilogue(pass_tile(g - 1), true);
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s_prev[i] = s_cur[i];
-    nblk_prev = nblk;
   }
   if (total > 0) {
-    readout(total - 1, s_prev, nblk_prev);
+    readout(total - 1);
     epilogue(pass_tile(total - 1), false);
   }
   cp_async_wait<0>();
@@ -531,12 +537,19 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   if (t == 0) *a.count = 0u;
 }
 
-// CTAs per tile for K columns: the largest of 8, 4, 2, 1 whose share of K is
-// whole 32-wide blocks.
-__host__ __device__ inline int mm_cluster(int K) {
-  for (int c = kMaxCluster; c > 1; c >>= 1)
-    if (K % (32 * c) == 0) return c;
-  return 1;
+// CTAs per tile (the cluster) for a [rows x K] projection: the largest of 8,
+// 4, 2, 1 whose share of K is whole 32-wide blocks and fits the CTA's B
+// buffer, preferring sizes that keep every CTA of the launch in one wave at
+// two CTAs per SM; 0 if none fits.
+int mm_cluster(int K, int rows, int num_sms) {
+  const int tiles = (rows + kTcM - 1) / kTcM;
+  int fit = 0;
+  for (int c = kMaxCluster; c >= 1; c >>= 1) {
+    if (K % (32 * c) != 0 || K / c > kSplitMaxK) continue;
+    if (tiles * c <= 2 * num_sms) return c;
+    if (!fit) fit = c;
+  }
+  return fit;
 }
 
 // ---------------------------------------------------------------- embedding
@@ -885,7 +898,7 @@ int batch_ss_slots(int H) { return ((H + kTcM - 1) / kTcM) * kMaxCluster; }
 
 bool batch_supported(const DevModel& m) {
   const int G = m.nq / m.nkv;
-  auto split_ok = [](int K) { return K % 64 == 0 && K / mm_cluster(K) <= kSplitMaxK; };
+  auto split_ok = [](int K) { return K % 64 == 0 && mm_cluster(K, kTcM, 1) > 0; };
   return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && split_ok(m.H) && split_ok(m.qw) &&
          split_ok(m.I) && m.H <= kHeadMaxK && attn_batch_smem(m) <= 227 * 1024;
 }
@@ -933,21 +946,22 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
   };
   const int fmt = m.wtype;
   const int tiles_h = (m.H + kTcM - 1) / kTcM;
+  cudaError_t e0;
+  int dev = 0, num_sms = 0;
+  if ((e0 = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e0 = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e0;
   float* ss_x = SS;                                       // after the embedding / down projection
   float* ss_mid = SS + batch_ss_slots(m.H) * kTcN;        // after the O projection
-  const int nss_x = tiles_h * mm_cluster(m.I), nss_mid = tiles_h * mm_cluster(m.qw);
+  const int nss_x = tiles_h * mm_cluster(m.I, m.H, num_sms), nss_mid = tiles_h * mm_cluster(m.qw, m.H, num_sms);
   cudaLaunchConfig_t ce = config(n, 256, 0, 1);
   cudaError_t e = cudaLaunchKernelEx(&ce, k_embed_batch, m, seqs, n, X, ss_x, nss_x);
   if (e != cudaSuccess) return e;
-  int dev = 0, num_sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
   auto mm = [&](const uint8_t* W, size_t rb, int K, int rows, const float* Xin, int ldx, const float* gain,
                 const float* ss, int nss, int epi, float* Y, int ldy, float* ss_out, bool split) {
     MmArgs a{};
     a.W = W; a.rb = rb; a.K = K; a.rows = rows; a.fmt = fmt;
-    a.cs = split ? mm_cluster(K) : 1;
+    a.cs = split ? mm_cluster(K, rows, num_sms) : 1;
     a.X = Xin; a.ldx = ldx; a.n = n; a.gain = gain; a.ss = ss; a.nss = nss; a.eps = m.eps;
     a.epi = epi; a.Y = Y; a.ldy = ldy; a.ss_out = ss_out;
     a.seqs = seqs; a.count = count; a.err = err; a.max_seq = m.max_seq;
