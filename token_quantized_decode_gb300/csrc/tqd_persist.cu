@@ -341,19 +341,6 @@ struct Cons {
   __device__ Cons(const DevModel& m_, const DevSeq& s_) : m(m_), s(s_) {}
 };
 
-// Stage n floats of global memory (written by other blocks before the last
-// grid barrier) into shared memory with 16-byte cp.async copies.  Every stage
-// follows a consumer sync, so earlier readers of dst are done.
-__device__ __forceinline__ void stage(Cons& C, float* dst, const float* src, int n) {
-  (void)C;
-  for (int i = threadIdx.x; i < n / 4; i += kCT)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst + 4 * i)),
-                 "l"(src + 4 * i)
-                 : "memory");
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-  csync();
-}
-
 __device__ __forceinline__ int xpad(int fmt, int e) {
   return fmt == kFmtQ8 ? 20 * (e >> 4) + (e & 15) : 12 * (e >> 3) + (e & 7);
 }
@@ -385,6 +372,40 @@ __device__ __forceinline__ float to_xin_norm(Cons& C, const float* src, int K, c
       const float v = src[i];
       ss = fmaf(v, v, ss);
       C.xin[xpad(C.fmt, i)] = v * g.v[j];
+    }
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  csync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCW; ++w) t += red[w];
+  return rsqrtf(t / static_cast<float>(K) + C.m.eps);
+}
+
+// RMSNorm input read straight from global memory (written by other blocks
+// before the last grid barrier): each thread loads its elements into
+// registers and writes the plain copy (residual source) and the padded
+// product with the gain in one pass; returns the folded 1/rms factor as
+// to_xin_norm does.  The barrier wait that precedes it ended with a consumer
+// sync, so earlier readers of xraw and xin are done.
+__device__ __forceinline__ float load_norm(Cons& C, const float* src, int K, const Gain& g) {
+  float* red = C.red + 16 * C.rsel;
+  C.rsel ^= 1u;
+  float v[kMaxGain];
+#pragma unroll
+  for (int j = 0; j < kMaxGain; ++j) {
+    const int i = threadIdx.x + kCT * j;
+    v[j] = i < K ? __ldcg(src + i) : 0.f;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxGain; ++j) {
+    const int i = threadIdx.x + kCT * j;
+    if (i < K) {
+      ss = fmaf(v[j], v[j], ss);
+      C.xraw[i] = v[j];
+      C.xin[xpad(C.fmt, i)] = v[j] * g.v[j];
     }
   }
   ss = warp_sum(ss);
@@ -851,11 +872,11 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
           for (int i = threadIdx.x; i < m.H; i += kCT) C.xraw[i] = __uint_as_float(static_cast<uint32_t>(row[i]) << 16);
         }
         csync();
+        o.scale = to_xin_norm(C, C.xraw, m.H, gain);
       } else {
         if (!wait()) return;
-        stage(C, C.xraw, s.x, m.H);
+        o.scale = load_norm(C, s.x, m.H, gain);
       }
-      o.scale = to_xin_norm(C, C.xraw, m.H, gain);
       o.epi = kEpiStore;
       o.y = s.qkv;
       mv_phase<FMT>(C, m.row_bytes_h, m.H, q0, q1, o);
@@ -883,8 +904,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       arrive();
       // ---- RMSNorm + gate/up + SwiGLU ----
       if (!wait()) return;
-      stage(C, C.xraw, s.x_mid, m.H);
-      o.scale = to_xin_norm(C, C.xraw, m.H, gain);
+      o.scale = load_norm(C, s.x_mid, m.H, gain);
       o.epi = kEpiSwiGLU;
       o.y = s.h;
       mv_phase<FMT>(C, m.row_bytes_h, m.H, g0, g1, o);
@@ -904,9 +924,8 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       Gain gain;
       load_gain(gain, m.out_norm, m.H);
       if (!wait()) return;
-      stage(C, C.xraw, s.x, m.H);
       MvOut o{};
-      o.scale = to_xin_norm(C, C.xraw, m.H, gain);
+      o.scale = load_norm(C, s.x, m.H, gain);
       o.epi = kEpiArgmax;
       o.y = s.logits;
       o.bv = -INFINITY;
