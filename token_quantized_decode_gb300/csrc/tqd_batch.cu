@@ -47,7 +47,7 @@ constexpr uint32_t kBPartBytes = kTcN * kSubK * 2;   // one bf16 part of B
 constexpr uint32_t kBBytes = 3 * kBPartBytes;        // one sub-chunk of B: N = 48 rows
 constexpr uint32_t kRecvBytes = kTcM * kTcN * 4;     // cluster partials received: [rank][row][16]
 constexpr uint32_t kPassCols = 4 * kTcN3;            // tensor-memory columns of one pass (four blocks)
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;       // 16 is a non-portable cluster size (allowed per kernel)
 // Split projections (one tile per CTA, two CTAs per SM): B for up to 384
 // columns, one pass of A and of tensor memory at a time.  lm_head (one CTA
 // per SM looping over tiles): B for all of H <= 1024, deeper weight
@@ -537,8 +537,8 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   if (t == 0) *a.count = 0u;
 }
 
-// CTAs per tile (the cluster) for a [rows x K] projection: the largest of 8,
-// 4, 2, 1 whose share of K is whole 32-wide blocks and fits the CTA's B
+// CTAs per tile (the cluster) for a [rows x K] projection: the largest of 16,
+// 8, 4, 2, 1 whose share of K is whole 32-wide blocks and fits the CTA's B
 // buffer, preferring sizes that keep every CTA of the launch in one wave at
 // two CTAs per SM; 0 if none fits.
 int mm_cluster(int K, int rows, int num_sms) {
@@ -907,6 +907,9 @@ cudaError_t batch_setup(const DevModel& m) {
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<SplitCfg>),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SplitCfg::total));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<SplitCfg>),
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<HeadCfg>),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(HeadCfg::total));
