@@ -204,6 +204,7 @@ __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
 struct DevLayer {
   const uint8_t* wqkv;
   const uint8_t* wo;
+  const uint8_t* wo_g;    // persistent schedule: wo's columns split by kv group, [n_kv][H][G hd]
   const uint8_t* wgu;
   const uint8_t* wd;
   const float* attn_norm;
@@ -219,9 +220,10 @@ struct DevState {  // per sequence, in device memory
   uint32_t pad;
 };
 
-// Grid barrier of the persistent schedule: a monotonic arrival count and the
-// number of barriers completed so far.  Set to zero once at creation and never
-// reset, so every barrier's target is (completed + 1) * blocks.
+// Barrier of the persistent schedule (the whole grid, or the blocks of one kv
+// group): a monotonic arrival count and the number of barriers completed so
+// far.  Set to zero once at creation and never reset, so every barrier's
+// target is (completed + 1) * members.
 struct DevBarrier {
   unsigned long long count;
   unsigned long long epoch;
@@ -234,6 +236,7 @@ struct DevModel {
   size_t row_bytes_h;     // bytes per row of a matrix with H columns
   size_t row_bytes_qw;    // ... with qw columns
   size_t row_bytes_i;     // ... with I columns
+  size_t row_bytes_gh;    // ... with (n_heads / n_kv_heads) * head_dim columns
   const DevLayer* layers;
   const uint8_t* lm_head;
   const uint8_t* embed;
@@ -260,6 +263,8 @@ struct DevSeq {
   uint32_t* amax_count;   // [1]
   DevBarrier* bar;        // grid barrier of the persistent schedule
   float* x_mid;           // [H] residual after the attention block
+  DevBarrier* gbar;       // per kv group g: [16 g] QKV rows written, [16 g + 8] attention partials written
+  float* opart;           // [n_kv][H] per-group partial O products (persistent schedule)
 };
 
 }  // namespace tqd

@@ -411,11 +411,17 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     off = align_up(off + bytes, A);
     return o;
   };
-  struct LayerOff { size_t wqkv, wo, wgu, wd, an, qn, kn, fn; };
+  // the persistent schedule reads wo's columns split by kv group: nkv
+  // matrices [H x G hd], one per group
+  const bool persist = cfg->schedule == TQD_SCHED_PERSISTENT;
+  const int gh = (nq / nkv) * hd;
+  const size_t rbg = row_bytes(wt, gh);
+  struct LayerOff { size_t wqkv, wo, wog, wgu, wd, an, qn, kn, fn; };
   std::vector<LayerOff> lo(L);
   for (int l = 0; l < L; ++l) {
     lo[l].wqkv = take(rbh * (qw + 2 * kvw));
     lo[l].wo = take(rbq * H);
+    lo[l].wog = persist ? take(rbg * H * nkv) : 0;
     lo[l].wgu = take(rbh * 2 * I);
     lo[l].wd = take(rbi * H);
     lo[l].an = take(4 * H);
@@ -429,7 +435,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const size_t o_rope = take(sizeof(float2) * static_cast<size_t>(S) * (hd / 2));
   const size_t o_layers = take(sizeof(DevLayer) * L);
   const size_t weights_end = off;
-  struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar; };
+  struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar, gbar, opart; };
   std::vector<SeqOff> so(cfg->max_batch);
   const size_t kv_bytes = sizeof(float) * static_cast<size_t>(L) * S * kvw;
   for (int b = 0; b < cfg->max_batch; ++b) {
@@ -450,6 +456,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].ai = take(4 * kMaxArgmaxBlocks);
     so[b].acount = take(4);
     so[b].bar = take(sizeof(DevBarrier));
+    so[b].gbar = take(sizeof(DevBarrier) * 16 * nkv);  // two per group, 128 bytes apart
+    so[b].opart = take(4ull * nkv * H);
   }
   // batched-step buffers (only for models holding several sequences)
   const int bmax = batch_max();
@@ -545,6 +553,24 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
       if (tmp) cudaFree(tmp);
       return fail(e, "upload qk-norm gains");
     }
+    if (persist) {
+      // wo's columns of each kv group as its own [H x gh] matrix
+      const size_t hrb = host_row_bytes(wt, qw), hsb = host_row_bytes(wt, gh);
+      std::vector<uint8_t> slice(hsb * H);
+      for (int g = 0; g < nkv && e == cudaSuccess; ++g) {
+        const uint8_t* src = static_cast<const uint8_t*>(W.wo);
+        for (int r = 0; r < H; ++r)
+          memcpy(slice.data() + hsb * r, src + hrb * r + hsb * g, hsb);
+        e = put(slice.data(), H, gh, lo[l].wog + rbg * H * g, 0, 1);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // the host slice is reused
+        wbytes -= static_cast<int64_t>(rbg) * H;  // a second layout of wo, not more weights
+      }
+      if (e != cudaSuccess) {
+        if (tmp) cudaFree(tmp);
+        return fail(e, "upload the grouped O projection");
+      }
+      dl[l].wo_g = base + lo[l].wog;
+    }
     dl[l].wqkv = base + lo[l].wqkv;
     dl[l].wo = base + lo[l].wo;
     dl[l].wgu = base + lo[l].wgu;
@@ -576,7 +602,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   dm.qw = qw; dm.kvw = kvw; dm.n_chunks = nch;
   dm.eps = cfg->rms_eps;
   dm.attn_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
-  dm.row_bytes_h = rbh; dm.row_bytes_qw = rbq; dm.row_bytes_i = rbi;
+  dm.row_bytes_h = rbh; dm.row_bytes_qw = rbq; dm.row_bytes_i = rbi; dm.row_bytes_gh = rbg;
   dm.layers = reinterpret_cast<const DevLayer*>(base + o_layers);
   dm.lm_head = base + o_lm;
   dm.embed = base + o_embed;
@@ -603,6 +629,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.amax_i = reinterpret_cast<int32_t*>(base + so[b].ai);
     d.amax_count = reinterpret_cast<uint32_t*>(base + so[b].acount);
     d.bar = reinterpret_cast<DevBarrier*>(base + so[b].bar);
+    d.gbar = reinterpret_cast<DevBarrier*>(base + so[b].gbar);
+    d.opart = reinterpret_cast<float*>(base + so[b].opart);
   }
   if (cfg->max_batch > 1 && batch_supported(dm) && (V + 127) / 128 <= kMaxArgmaxBlocks) {
     m->bx = reinterpret_cast<float*>(base + o_bx);

@@ -242,6 +242,74 @@ __device__ __forceinline__ void chunk_range(int S, int n_chunks, int c, int& t0,
   t1 = min(S, t0 + cs);
 }
 
+// ---------------------------------------------------------------- work plan
+// What block b does in every layer; producer and consumers derive the same
+// plan.  The blocks are split into one group per kv head (blocks beyond
+// n_kv_heads * (blocks / n_kv_heads) belong to none).  A group computes the
+// Q, K and V rows of its head group, runs its attention chunks, combines them,
+// and applies its columns of the O projection (a split over heads: the O
+// product is a sum over the groups' column slices), all synchronised inside
+// the group only.  Gate/up, down and the lm_head are split over all blocks.
+struct Plan {
+  int grp, j, bpg;   // group (-1: none), index in the group, blocks per group
+  int qr0[3], qr1[3];  // QKV matrix rows: the group's q, k and v rows this block owns
+  int chunk;         // attention chunk of item (grp, chunk), or -1
+  int o0, o1;        // rows of the group's O column slice
+  int g0, g1, d0, d1, v0, v1;
+};
+
+__device__ __forceinline__ Plan make_plan(const DevModel& m, int b, int nb) {
+  Plan p;
+  p.bpg = nb / m.nkv;
+  p.grp = (p.bpg > 0 && b < p.bpg * m.nkv) ? b / p.bpg : -1;
+  p.j = p.grp >= 0 ? b - p.grp * p.bpg : 0;
+  const int G = m.nq / m.nkv, gh = G * m.hd;
+  p.o0 = p.o1 = 0;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) p.qr0[i] = p.qr1[i] = 0;
+  if (p.grp >= 0) {
+    block_rows(m.H, 1, p.j, p.bpg, p.o0, p.o1);
+    // the group's q (gh rows), k (hd) and v (hd) rows of the QKV matrix
+    const int segr[3] = {gh, m.hd, m.hd};
+    const int phys[3] = {p.grp * gh, m.qw + p.grp * m.hd, m.qw + m.kvw + p.grp * m.hd};
+    if (p.bpg >= 3) {
+      // every block takes rows of one segment: blocks go one at a time to the
+      // segment with the most rows per block (ties: the first)
+      int nbk[3] = {1, 1, 1};
+      for (int k = 3; k < p.bpg; ++k) {
+        int best = 0;
+        for (int i = 1; i < 3; ++i)
+          if ((segr[i] + nbk[i] - 1) / nbk[i] > (segr[best] + nbk[best] - 1) / nbk[best]) best = i;
+        ++nbk[best];
+      }
+      int i = 0, jj = p.j;
+      while (jj >= nbk[i]) jj -= nbk[i++];
+      int a, e;
+      block_rows(segr[i], 1, jj, nbk[i], a, e);
+      p.qr0[i] = phys[i] + a;
+      p.qr1[i] = phys[i] + e;
+    } else {
+      // fewer than three blocks: contiguous shares of the q, k, v sequence
+      int l0, l1;
+      block_rows(gh + 2 * m.hd, 1, p.j, p.bpg, l0, l1);
+      const int seg0[3] = {0, gh, gh + m.hd};
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        const int a = max(l0, seg0[i]), e = min(l1, seg0[i] + segr[i]);
+        if (a < e) {
+          p.qr0[i] = phys[i] + (a - seg0[i]);
+          p.qr1[i] = phys[i] + (e - seg0[i]);
+        }
+      }
+    }
+  }
+  p.chunk = (p.grp >= 0 && p.j < m.n_chunks) ? p.j : -1;
+  block_rows(2 * m.I, 2, b, nb, p.g0, p.g1);
+  block_rows(m.H, 1, b, nb, p.d0, p.d1);
+  block_rows(m.V, 1, b, nb, p.v0, p.v1);
+  return p;
+}
+
 // ---------------------------------------------------------------- producer
 struct Producer {
   Ring r;
@@ -293,34 +361,25 @@ struct Producer {
 __device__ void run_producer(const DevModel& m, const DevSeq& s, int n_steps, int full_from,
                              uint32_t pos0, Ring ring) {
   Producer P{ring, &s.state->err, true};
-  const int b = blockIdx.x, nb = gridDim.x;
-  const int n_items = m.nkv * m.n_chunks;
-  const int rows_qkv = m.qw + 2 * m.kvw;
-  int q0, q1, o0, o1, g0, g1, d0, d1, v0, v1;
-  block_rows(rows_qkv, 1, b, nb, q0, q1);
-  block_rows(m.H, 1, b, nb, o0, o1);
-  block_rows(2 * m.I, 2, b, nb, g0, g1);
-  block_rows(m.H, 1, b, nb, d0, d1);
-  block_rows(m.V, 1, b, nb, v0, v1);
+  const Plan pl = make_plan(m, blockIdx.x, gridDim.x);
   for (int step = 0; step < n_steps && P.ok; ++step) {
     const int pos = static_cast<int>(pos0) + step;
     if (pos >= m.max_seq) break;
     for (int l = 0; l < m.n_layers && P.ok; ++l) {
       const DevLayer& L = m.layers[l];
-      P.rows(L.wqkv, m.row_bytes_h, q0, q1);
-      const size_t lay = static_cast<size_t>(l) * m.nkv * m.max_seq * m.hd;
-      for (int item = b; item < n_items; item += nb) {
-        const int g = item / m.n_chunks, c = item - g * m.n_chunks;
+      for (int i = 0; i < 3; ++i) P.rows(L.wqkv, m.row_bytes_h, pl.qr0[i], pl.qr1[i]);
+      if (pl.chunk >= 0) {
         int t0, t1;
-        chunk_range(pos + 1, m.n_chunks, c, t0, t1);
-        const size_t head = lay + static_cast<size_t>(g) * m.max_seq * m.hd;
+        chunk_range(pos + 1, m.n_chunks, pl.chunk, t0, t1);
+        const size_t head = (static_cast<size_t>(l) * m.nkv + pl.grp) * m.max_seq * m.hd;
         P.kv(s.kcache + head, s.vcache + head, m.hd, t0, min(t1, pos));
       }
-      P.rows(L.wo, m.row_bytes_qw, o0, o1);
-      P.rows(L.wgu, m.row_bytes_h, g0, g1);
-      P.rows(L.wd, m.row_bytes_i, d0, d1);
+      if (pl.grp >= 0)
+        P.rows(L.wo_g + static_cast<size_t>(pl.grp) * m.H * m.row_bytes_gh, m.row_bytes_gh, pl.o0, pl.o1);
+      P.rows(L.wgu, m.row_bytes_h, pl.g0, pl.g1);
+      P.rows(L.wd, m.row_bytes_i, pl.d0, pl.d1);
     }
-    if (step >= full_from) P.rows(m.lm_head, m.row_bytes_h, v0, v1);
+    if (step >= full_from) P.rows(m.lm_head, m.row_bytes_h, pl.v0, pl.v1);
   }
   if (!P.ok) P.drain();
 }
@@ -397,6 +456,45 @@ __device__ __forceinline__ float load_norm(Cons& C, const float* src, int K, con
   for (int j = 0; j < kMaxGain; ++j) {
     const int i = threadIdx.x + kCT * j;
     v[j] = i < K ? __ldcg(src + i) : 0.f;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxGain; ++j) {
+    const int i = threadIdx.x + kCT * j;
+    if (i < K) {
+      ss = fmaf(v[j], v[j], ss);
+      C.xraw[i] = v[j];
+      C.xin[xpad(C.fmt, i)] = v[j] * g.v[j];
+    }
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  csync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCW; ++w) t += red[w];
+  return rsqrtf(t / static_cast<float>(K) + C.m.eps);
+}
+
+// As load_norm for x after the attention block: the layer's input x (still
+// in xraw, where this thread staged its own elements) plus the nparts partial
+// O products (one per kv group, [nparts][K] in global memory), added in group
+// order; xraw becomes x after the attention block.
+__device__ __forceinline__ float load_norm_sum(Cons& C, const float* parts, int nparts, int K, const Gain& g) {
+  float* red = C.red + 16 * C.rsel;
+  C.rsel ^= 1u;
+  float v[kMaxGain];
+#pragma unroll
+  for (int j = 0; j < kMaxGain; ++j) {
+    const int i = threadIdx.x + kCT * j;
+    v[j] = i < K ? C.xraw[i] : 0.f;
+  }
+  for (int q = 0; q < nparts; ++q) {
+#pragma unroll
+    for (int j = 0; j < kMaxGain; ++j) {
+      const int i = threadIdx.x + kCT * j;
+      if (i < K) v[j] += __ldcg(parts + static_cast<size_t>(q) * K + i);
+    }
   }
   float ss = 0.f;
 #pragma unroll
@@ -774,19 +872,17 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
       s.part_ml[(static_cast<size_t>(h) * m.n_chunks + c) * 2 + 1] = Lsum;
     }
   }
-  csync();
-  __shared__ uint32_t s_last;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t old = atomicAdd(s.attn_count + g, 1u);
-    s_last = old == static_cast<uint32_t>(m.n_chunks) - 1u;
-    if (s_last) __threadfence();
-  }
-  csync();
-  if (!s_last) return;
-  // combine: stage the group's partials, then one output per (head, dim)
+}
+
+// Combine group g's chunk partials by log-sum-exp ("Eight kernels",
+// attention_decode, as a split-K flash decode) into the matvec input (the
+// padded layout) of the group's O column slice: xin holds o of the group's
+// heads, G * head_dim values.
+__device__ void group_combine(Cons& C, int g, int HD, int G) {
+  const DevModel& m = C.m;
+  const DevSeq& s = C.s;
   const int NC = m.n_chunks;
-  float* po = wst;                        // [G][NC][HD]
+  float* po = C.scr;                      // [G][NC][HD]
   float* pml = po + G * NC * HD;          // [G][NC][2]
   const float4* src_o = reinterpret_cast<const float4*>(s.part_o + static_cast<size_t>(g) * G * NC * HD);
   for (int i = threadIdx.x; i < G * NC * HD / 4; i += kCT)
@@ -794,21 +890,32 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
   const float* src_ml = s.part_ml + static_cast<size_t>(g) * G * NC * 2;
   for (int i = threadIdx.x; i < G * NC * 2; i += kCT) pml[i] = __ldcg(src_ml + i);
   csync();
+  // chunk weights exp(m_c - M) / L of every head, once: one warp per head
+  float* wts = pml + G * NC * 2;          // [G][NC]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < G) {
+    float M = -INFINITY;
+    for (int cc = lane; cc < NC; cc += 32) M = fmaxf(M, pml[(warp * NC + cc) * 2]);
+    M = warp_max(M);
+    float den = 0.f;
+    for (int cc = lane; cc < NC; cc += 32) {
+      const float mc = pml[(warp * NC + cc) * 2];
+      const float f = mc == -INFINITY ? 0.f : expf(mc - M);
+      wts[warp * NC + cc] = f;
+      den = fmaf(f, pml[(warp * NC + cc) * 2 + 1], den);
+    }
+    den = warp_sum(den);
+    __syncwarp();
+    for (int cc = lane; cc < NC; cc += 32) wts[warp * NC + cc] /= den;
+  }
+  csync();
   for (int idx = threadIdx.x; idx < G * HD; idx += kCT) {
     const int hh = idx / HD, d = idx - hh * HD;
-    float M = -INFINITY;
-    for (int cc = 0; cc < NC; ++cc) M = fmaxf(M, pml[(hh * NC + cc) * 2]);
-    float num = 0.f, den = 0.f;
-    for (int cc = 0; cc < NC; ++cc) {
-      const float mc = pml[(hh * NC + cc) * 2];
-      if (mc == -INFINITY) continue;
-      const float f = expf(mc - M);
-      num = fmaf(f, po[(hh * NC + cc) * HD + d], num);
-      den = fmaf(f, pml[(hh * NC + cc) * 2 + 1], den);
-    }
-    s.attn[(g * G + hh) * HD + d] = num / den;
+    float num = 0.f;
+    for (int cc = 0; cc < NC; ++cc) num = fmaf(wts[hh * NC + cc], po[(hh * NC + cc) * HD + d], num);
+    C.xin[xpad(C.fmt, idx)] = num;
   }
-  if (threadIdx.x == 0) s.attn_count[g] = 0u;
+  csync();
 }
 
 template <int HD>
@@ -829,19 +936,18 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
   const int b = blockIdx.x, nb = gridDim.x;
   DevBarrier* bar = s.bar;
   unsigned long long epoch = s.bar->epoch;  // barriers completed before this launch
-  const int n_items = m.nkv * m.n_chunks;
   const int G = m.nq / m.nkv;
-  int q0, q1, o0, o1, g0, g1, d0, d1, v0, v1;
-  block_rows(m.qw + 2 * m.kvw, 1, b, nb, q0, q1);
-  block_rows(m.H, 1, b, nb, o0, o1);
-  block_rows(2 * m.I, 2, b, nb, g0, g1);
-  block_rows(m.H, 1, b, nb, d0, d1);
-  block_rows(m.V, 1, b, nb, v0, v1);
   auto arrive = [&]() {
     gb_arrive(bar);
     ++epoch;
   };
   auto wait = [&]() { return gb_wait(bar, epoch * static_cast<unsigned long long>(nb), C.err); };
+  const Plan pl = make_plan(m, b, nb);
+  const int v0 = pl.v0, v1 = pl.v1;
+  // each counter on its own 128-byte line: groups do not contend
+  DevBarrier* ga = pl.grp >= 0 ? s.gbar + 16 * pl.grp : nullptr;  // the group's QKV rows are written
+  DevBarrier* gb = pl.grp >= 0 ? ga + 8 : nullptr;                 // the group's attention partials are written
+  unsigned long long gepoch = pl.grp >= 0 ? ga->epoch : 0ull;      // group barriers completed before this launch
   for (int step = 0; step < n_steps; ++step) {
     const uint32_t pos = pos0 + step;
     if (pos >= static_cast<uint32_t>(m.max_seq)) {
@@ -859,7 +965,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       MvOut o{};
       Gain gain;
       load_gain(gain, L.attn_norm, m.H);
-      // ---- RMSNorm + QKV ----
+      // ---- RMSNorm + the group's Q, K, V rows ----
       if (l == 0) {
         csync();
         if (FMT == kFmtQ8) {
@@ -879,35 +985,37 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       }
       o.epi = kEpiStore;
       o.y = s.qkv;
-      mv_phase<FMT>(C, m.row_bytes_h, m.H, q0, q1, o);
-      arrive();
-      // ---- QK-norm + RoPE + append + attention ----
-      AttnPre pre;
-      load_attn_pre(pre, m, L, static_cast<int>(pos));
-      if (!wait()) return;
-      for (int item = b; item < n_items; item += nb) {
-        const int g = item / m.n_chunks, c = item - g * m.n_chunks;
-        if (m.hd == 128) attn_dispatch_g<128>(C, G, l, g, c, pos, pre);
-        else attn_dispatch_g<64>(C, G, l, g, c, pos, pre);
-        csync();
+      for (int i = 0; i < 3; ++i)
+        if (pl.qr0[i] < pl.qr1[i]) mv_phase<FMT>(C, m.row_bytes_h, m.H, pl.qr0[i], pl.qr1[i], o);
+      load_gain(gain, L.ffn_norm, m.H);  // for the gate/up phase
+      if (pl.grp >= 0) {
+        const unsigned long long tgt = (gepoch + 1) * static_cast<unsigned long long>(pl.bpg);
+        gb_arrive(ga);
+        // ---- QK-norm + RoPE + append + attention chunk ----
+        if (pl.chunk >= 0) {
+          AttnPre pre;
+          load_attn_pre(pre, m, L, static_cast<int>(pos));
+          if (!gb_wait(ga, tgt, C.err)) return;
+          if (m.hd == 128) attn_dispatch_g<128>(C, G, l, pl.grp, pl.chunk, pos, pre);
+          else attn_dispatch_g<64>(C, G, l, pl.grp, pl.chunk, pos, pre);
+        }
+        gb_arrive(gb);
+        ++gepoch;
+        // ---- combine the group's chunks + its O column slice ----
+        if (!gb_wait(gb, tgt, C.err)) return;
+        group_combine(C, pl.grp, m.hd, G);
+        o.scale = 1.f;
+        o.epi = kEpiStore;
+        o.y = s.opart + static_cast<size_t>(pl.grp) * m.H;
+        mv_phase<FMT>(C, m.row_bytes_gh, G * m.hd, pl.o0, pl.o1, o);
       }
       arrive();
-      // ---- O projection + residual ----
-      load_gain(gain, L.ffn_norm, m.H);  // for the next phase
+      // ---- residual + RMSNorm + gate/up + SwiGLU ----
       if (!wait()) return;
-      stage_xin(C, s.attn, m.qw);
-      o.scale = 1.f;
-      o.epi = kEpiResid;
-      o.y = s.x_mid;
-      o.res = C.xraw;
-      mv_phase<FMT>(C, m.row_bytes_qw, m.qw, o0, o1, o);
-      arrive();
-      // ---- RMSNorm + gate/up + SwiGLU ----
-      if (!wait()) return;
-      o.scale = load_norm(C, s.x_mid, m.H, gain);
+      o.scale = load_norm_sum(C, s.opart, m.nkv, m.H, gain);
       o.epi = kEpiSwiGLU;
       o.y = s.h;
-      mv_phase<FMT>(C, m.row_bytes_h, m.H, g0, g1, o);
+      mv_phase<FMT>(C, m.row_bytes_h, m.H, pl.g0, pl.g1, o);
       arrive();
       // ---- down projection + residual ----
       if (!wait()) return;
@@ -916,7 +1024,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       o.epi = kEpiResid;
       o.y = s.x;
       o.res = C.xraw;
-      mv_phase<FMT>(C, m.row_bytes_i, m.I, d0, d1, o);
+      mv_phase<FMT>(C, m.row_bytes_i, m.I, pl.d0, pl.d1, o);
       arrive();
     }
     if (step >= full_from) {
@@ -987,6 +1095,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
     }
   }
   if (b == 0 && threadIdx.x == 0) s.bar->epoch = epoch;
+  if (pl.grp >= 0 && pl.j == 0 && threadIdx.x == 0) ga->epoch = gepoch;
 }
 
 template <int FMT>
