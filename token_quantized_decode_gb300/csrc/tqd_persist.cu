@@ -638,6 +638,54 @@ __device__ void mv_phase(Cons& C, size_t rb, int K, int r0, int r1, MvOut& o) {
     // every warp waits for the piece before releasing it, so no warp can run
     // ahead and release a later use of the same slot early
     mwait(fb, (C.r.n / kSlots) & 1u, C.err);
+    if (nchunks <= 16) {
+      // short rows (one 16-byte chunk per lane or fewer): each half-warp takes
+      // its own row pair; both halves run every round so the shuffles stay
+      // warp-uniform, an idle half repeats the last pair and skips the epilogue
+      constexpr int XS = FMT == kFmtQ8 ? 20 : 12;
+      const int half = lane >> 4, l16 = lane & 15;
+      for (int t0 = 2 * warp; t0 < pairs; t0 += 2 * kCW) {
+        const int pr = min(t0 + half, pairs - 1);
+        const int ra = 2 * pr, rbw = 2 * pr + 1;
+        const bool has_b = rbw < n;
+        const uint8_t* wa = slot + static_cast<size_t>(ra) * rb;
+        const uint8_t* wb = slot + static_cast<size_t>(has_b ? rbw : ra) * rb;
+        float acc_a = 0.f, acc_b = 0.f;
+        if (l16 < nchunks) {
+          const float4* xp = reinterpret_cast<const float4*>(C.xin + XS * l16);
+          const uint4 w0 = *reinterpret_cast<const uint4*>(wa + 16 * l16);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(wb + 16 * l16);
+          if (FMT == kFmtQ8) {
+            const float s0 = __half2float(*reinterpret_cast<const __half*>(wa + K + 2 * (l16 >> 1)));
+            const float s1 = __half2float(*reinterpret_cast<const __half*>(wb + K + 2 * (l16 >> 1)));
+            acc_a = s0 * dot16_q8(w0, xp);
+            acc_b = s1 * dot16_q8(w1, xp);
+          } else {
+            acc_a = dot8_bf16(w0, xp);
+            acc_b = dot8_bf16(w1, xp);
+          }
+        }
+#pragma unroll
+        for (int sh = 8; sh > 0; sh >>= 1) {
+          acc_a += __shfl_xor_sync(0xFFFFFFFFu, acc_a, sh);
+          acc_b += __shfl_xor_sync(0xFFFFFFFFu, acc_b, sh);
+        }
+        if (t0 + half < pairs && l16 == 0) {
+          acc_a *= o.scale;
+          acc_b *= o.scale;
+          if (o.epi == kEpiSwiGLU) {
+            o.y[(a + ra) >> 1] = silu_mul(acc_a, acc_b);
+          } else {
+            epi_row(o, a + ra, acc_a);
+            if (has_b) epi_row(o, a + rbw, acc_b);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(C.r.empty + C.r.n % kSlots)) : "memory");
+      ++C.r.n;
+      continue;
+    }
     for (int t = warp; t < tasks; t += kCW) {
       const int p = t / nseg, sg = t - p * nseg;
       const int ra = 2 * p, rbw = 2 * p + 1;
