@@ -30,6 +30,7 @@ constexpr int kSlots = 4;
 constexpr int kPartFloats = 320;        // per-task partial sums of one ring piece
 constexpr int kRedFloats = 64 + 2 * kPartFloats;
 constexpr int kMaxGain = 4;             // norm gains held per thread (H <= 4 * kCT)
+constexpr int kMaxParts = 8;            // kv groups whose partial O products are summed (n_kv_heads <= 8)
 // Error bits that end every block's waits; the others (a bad token id, every
 // logit NaN, capacity) are reported to the host without stopping the launch.
 constexpr uint32_t kFatal = kErrGridBarrier | kErrMbarrier;
@@ -489,13 +490,19 @@ __device__ __forceinline__ float load_norm_sum(Cons& C, const float* parts, int 
     const int i = threadIdx.x + kCT * j;
     v[j] = i < K ? C.xraw[i] : 0.f;
   }
-  for (int q = 0; q < nparts; ++q) {
+  // every partial is requested before any is added (one L2 round trip)
+  float pv[kMaxParts][kMaxGain];
+#pragma unroll
+  for (int q = 0; q < kMaxParts; ++q)
 #pragma unroll
     for (int j = 0; j < kMaxGain; ++j) {
       const int i = threadIdx.x + kCT * j;
-      if (i < K) v[j] += __ldcg(parts + static_cast<size_t>(q) * K + i);
+      pv[q][j] = (q < nparts && i < K) ? __ldcg(parts + static_cast<size_t>(q) * K + i) : 0.f;
     }
-  }
+#pragma unroll
+  for (int q = 0; q < kMaxParts; ++q)
+#pragma unroll
+    for (int j = 0; j < kMaxGain; ++j) v[j] += pv[q][j];
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxGain; ++j) {
@@ -1191,7 +1198,7 @@ size_t persistent_smem_bytes(const DevModel& m) { return playout(m).total; }
 
 bool persistent_supported(const DevModel& m) {
   const int G = m.nq / m.nkv;
-  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && m.H <= kMaxGain * kCT;
+  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && m.H <= kMaxGain * kCT && m.nkv <= kMaxParts;
 }
 
 int persistent_blocks_per_sm(const DevModel& m) {
