@@ -53,16 +53,18 @@ constexpr int kMaxCluster = 16;       // 16 is a non-portable cluster size (allo
 // per SM looping over tiles): B for all of H <= 1024, deeper weight
 // staging, and double-buffered A and tensor memory so one pass's read-out
 // overlaps the next pass's MMAs.
-template <int STAGES, int MAXSUB, bool DBL>
+template <int STAGES, int MAXSUB, bool DBL, int NH>
 struct MmCfg {
+  static constexpr int nh = NH;                  // threads per weight row (each a share of every pass)
+  static constexpr int threads = kMmThreads * NH;
   static constexpr uint32_t a = STAGES * kRawBytes;
   static constexpr uint32_t b = a + (DBL ? 2 : 1) * kAPassBytes;
   static constexpr uint32_t recv = b + MAXSUB * kBBytes;
-  static constexpr uint32_t total = recv + kRecvBytes;
+  static constexpr uint32_t total = recv + NH * kRecvBytes;
   static constexpr uint32_t tmem = DBL ? 512 : 256;
 };
-using SplitCfg = MmCfg<2, 6, false>;
-using HeadCfg = MmCfg<3, 16, true>;
+using SplitCfg = MmCfg<2, 6, false, 1>;
+using HeadCfg = MmCfg<3, 16, true, 2>;
 constexpr int kSplitMaxK = 6 * kSubK, kHeadMaxK = 16 * kSubK;
 
 // Shared-memory matrix descriptor, K-major without swizzle: core matrices of
@@ -189,23 +191,26 @@ struct MmArgs {
   int max_seq;
 };
 
-// Thread t of the CTA dequantises weight row t of the current tile and owns
-// tensor-memory lane t.  Projections split over a cluster run one tile per
-// CTA; the lm_head (cs == 1) runs one CTA per SM over tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ..., reading out one pass while the next pass's
-// MMAs run.
+// Thread t of the CTA works on weight row t % 128 of the current tile (tensor
+// memory lane t % 128): with NH threads per row, thread t takes the share
+// t / 128 of every pass's dequantisation and read-out.  Projections split over
+// a cluster run one tile per CTA; the lm_head (cs == 1) runs one CTA per SM
+// over tiles blockIdx.x, blockIdx.x + gridDim.x, ..., reading out one pass
+// while the next pass's MMAs run.
 template <class CFG>
-__global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
+__global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   constexpr bool DBL = CFG::tmem == 512;
   constexpr int STAGES = CFG::a / kRawBytes;
+  constexpr int NH = CFG::nh, NT = CFG::threads, NW = NT / 32;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ __align__(8) uint64_t bars[2];  // a pass's MMAs are complete (by pass parity)
   __shared__ uint32_t tmem_base;
   __shared__ float inv_rms[kTcN];
-  __shared__ float wred_v[4][kTcN];
-  __shared__ int wred_i[4][kTcN];
+  __shared__ float wred_v[NW][kTcN];
+  __shared__ int wred_i[NW][kTcN];
   __shared__ uint32_t s_last;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int tr = t & (kTcM - 1), hf = t / kTcM;  // weight row of the tile, share of the row
   const int rank = static_cast<int>(cluster_rank());
   const bool q8 = a.fmt == kFmtQ8;
   const int KR = a.K / a.cs, kc0 = rank * KR;
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
     const int k0 = kc0 + (g % npass) * PK, pk = min(PK, kc0 + KR - k0);
     const int chunks = (q8 ? pk : 2 * pk) / 16;
     unsigned char* dst = sm + (g % STAGES) * kRawBytes;
-    for (int c = t; c < kTcM * 8; c += kMmThreads) {
+    for (int c = t; c < kTcM * 8; c += NT) {
       const int r = c >> 3, ch = c & 7;
       if (ch < chunks) {
         const bool ok = row0 + r < a.rows;
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   };
   // f16 scale bits of this thread's row for the blocks of pass g
   auto load_scales = [&](int g, uint16_t (&sb)[4]) {
-    const int row = pass_tile(g) * kTcM + t;
+    const int row = pass_tile(g) * kTcM + tr;
     const int k0 = kc0 + (g % npass) * PK, nblk = min(PK, kc0 + KR - k0) / 32;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -261,12 +266,16 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   }
   uint16_t sc_next[4];
   load_scales(0, sc_next);
-  float sc[2][4];   // scales of the passes in flight, by pass parity
-  int nbk[2] = {0, 0};
+  // per-pass state of the two passes in flight, kept in registers (even and
+  // odd passes as separate variables: an array indexed by the pass parity
+  // would live in local memory, which misses the small L1 left beside the
+  // shared-memory carve-out)
+  float sc0[4], sc1[4];  // block scales of the even / odd pass
+  int nb0 = 0, nb1 = 0;  // blocks of the even / odd pass
+  uint32_t ph0 = 0u, ph1 = 0u;
   float acc[kTcN];
 #pragma unroll
   for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
-  uint32_t ph[2] = {0u, 0u};
   bool ok = true;
   const int b_ep = t & (kTcN - 1);  // the sequence this thread's epilogue items belong to
   float ssum = 0.f, bv = -INFINITY;
@@ -275,15 +284,21 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   uint32_t lane_addr = 0;
   // read out pass q: scale each block's column sums and add them up
   auto readout = [&](int q) {
-    if (!mbar_wait_bounded(&bars[q & 1], ph[q & 1], a.err)) ok = false;
-    ph[q & 1] ^= 1u;
+    const bool odd = q & 1;
+    if (!mbar_wait_bounded(&bars[odd ? 1 : 0], odd ? ph1 : ph0, a.err)) ok = false;
+    if (odd) ph1 ^= 1u;
+    else ph0 ^= 1u;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t base = lane_addr + (DBL ? (q & 1) * 256 : 0);
-    for (int blk = 0; blk < nbk[q & 1]; ++blk) {
+    const uint32_t base = lane_addr + (DBL && odd ? 256 : 0);
+    const int nbq = odd ? nb1 : nb0;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      if (blk % NH != hf || blk >= nbq) continue;
       float v[16];
       tmem_block_sum(base + blk * kTcN3, v);
+      const float scale = odd ? sc1[blk] : sc0[blk];
 #pragma unroll
-      for (int b = 0; b < kTcN; ++b) acc[b] = fmaf(sc[q & 1][blk], v[b], acc[b]);
+      for (int b = 0; b < kTcN; ++b) acc[b] = fmaf(scale, v[b], acc[b]);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   };
@@ -294,8 +309,8 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   auto epilogue = [&](int tile, bool more) {
     const int rpc = kTcM / a.cs, row0 = tile * kTcM;
     {
-      const int q = t / rpc, lr = t - q * rpc;
-      const uint32_t dst = mapa_u32(recv + (rank * rpc + lr) * kTcN, static_cast<uint32_t>(q));
+      const int q = tr / rpc, lr = tr - q * rpc;
+      const uint32_t dst = mapa_u32(recv + ((rank * NH + hf) * rpc + lr) * kTcN, static_cast<uint32_t>(q));
 #pragma unroll
       for (int i = 0; i < kTcN / 4; ++i)
         st_dsmem4(dst + 16 * i, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
@@ -304,10 +319,10 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
     }
     cluster_sync();
     const float scl = inv_rms[b_ep];
-    for (int idx = t; idx < rpc * (kTcN / 2); idx += kMmThreads) {
+    for (int idx = t; idx < rpc * (kTcN / 2); idx += NT) {
       const int lr = 2 * (idx / kTcN);
       float v0 = 0.f, v1 = 0.f;
-      for (int q = 0; q < a.cs; ++q) {
+      for (int q = 0; q < a.cs * NH; ++q) {
         v0 += recv[(q * rpc + lr) * kTcN + b_ep];
         v1 += recv[(q * rpc + lr + 1) * kTcN + b_ep];
       }
@@ -345,9 +360,15 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   // read out first
   auto load_pass = [&](int g) {
     const int k0 = kc0 + (g % npass) * PK, pk = min(PK, kc0 + KR - k0);
-    nbk[g & 1] = pk / 32;
+    if (g & 1) {
+      nb1 = pk / 32;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) sc[g & 1][i] = q8 ? __half2float(__ushort_as_half(sc_next[i])) : 1.f;
+      for (int i = 0; i < 4; ++i) sc1[i] = q8 ? __half2float(__ushort_as_half(sc_next[i])) : 1.f;
+    } else {
+      nb0 = pk / 32;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc0[i] = q8 ? __half2float(__ushort_as_half(sc_next[i])) : 1.f;
+    }
     load_scales(g + 1, sc_next);
     // keep STAGES - 1 passes in flight ahead of this one
     if (g + STAGES - 1 < total) issue_raw(g + STAGES - 1);
@@ -358,11 +379,11 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
       readout(g - 1);
       if ((g - 1) % npass == npass - 1) epilogue(pass_tile(g - 1), true);
     }
-    const unsigned char* raw = sm + (g % STAGES) * kRawBytes + t * kPassBytes;
+    const unsigned char* raw = sm + (g % STAGES) * kRawBytes + tr * kPassBytes;
     unsigned char* A = sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
     if (q8) {
-      for (int ch = 0; ch < pk / 16; ++ch) {
-        const uint4 w = *reinterpret_cast<const uint4*>(raw + ((ch ^ (t & 7)) << 4));
+      for (int ch = hf; ch < pk / 16; ch += NH) {
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + ((ch ^ (tr & 7)) << 4));
         uint32_t o[8];
         i8x4_to_bf16x4(w.x, o[0], o[1]);
         i8x4_to_bf16x4(w.y, o[2], o[3]);
@@ -370,13 +391,13 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
         i8x4_to_bf16x4(w.w, o[6], o[7]);
         unsigned char* As = A + (ch >> 2) * kABytes;
         const int kk = (ch & 3) * 16;
-        *reinterpret_cast<uint4*>(As + core_off16(t, kk)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(As + core_off16(t, kk + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+        *reinterpret_cast<uint4*>(As + core_off16(tr, kk)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(As + core_off16(tr, kk + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     } else {
-      for (int ch = 0; ch < pk / 8; ++ch)
-        *reinterpret_cast<uint4*>(A + core_off16(t, ch * 8)) =
-            *reinterpret_cast<const uint4*>(raw + ((ch ^ (t & 7)) << 4));
+      for (int ch = hf; ch < pk / 8; ch += NH)
+        *reinterpret_cast<uint4*>(A + core_off16(tr, ch * 8)) =
+            *reinterpret_cast<const uint4*>(raw + ((ch ^ (tr & 7)) << 4));
     }
   };
   // the first pass's weights are dequantised before the wait as well
@@ -389,15 +410,16 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   {
     float ss = 0.f;
     if (a.gain)
-      for (int i = t; i < a.nss * kTcN; i += kMmThreads) ss += __ldcg(a.ss + i);  // sequence i % 16 = t % 16
+      for (int i = t; i < a.nss * kTcN; i += NT) ss += __ldcg(a.ss + i);  // sequence i % 16 = t % 16
     const int nsubs = (KR + kSubK - 1) / kSubK;
-    const int b = t >> 3, k8 = (t & 7) * 8;
-    for (int s0 = 0; s0 < nsubs; s0 += 4) {
+    const int b = (t >> 3) & (kTcN - 1), k8 = (t & 7) * 8;
+    // thread share hf builds sub-chunks hf, hf + NH, ...
+    for (int s0 = hf; s0 < nsubs; s0 += 4 * NH) {
       float4 xv[4][2];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         xv[i][0] = xv[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int sidx = s0 + i;
+        const int sidx = s0 + i * NH;
         if (sidx < nsubs && b < a.n && k8 < min(kSubK, KR - sidx * kSubK)) {
           const float* src = a.X + static_cast<size_t>(b) * a.ldx + kc0 + sidx * kSubK + k8;
           xv[i][0] = __ldcg(reinterpret_cast<const float4*>(src));
@@ -413,7 +435,7 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int sidx = s0 + i;
+        const int sidx = s0 + i * NH;
         if (sidx >= nsubs) break;
         const float x[8] = {xv[i][0].x, xv[i][0].y, xv[i][0].z, xv[i][0].w,
                             xv[i][1].x, xv[i][1].y, xv[i][1].z, xv[i][1].w};
@@ -435,12 +457,13 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  if (t < kTcN)
-    inv_rms[t] = a.gain ? rsqrtf((wred_v[0][t] + wred_v[1][t] + wred_v[2][t] + wred_v[3][t]) / static_cast<float>(a.K) +
-                                 a.eps)
-                        : 1.f;
+  if (t < kTcN) {
+    float ss = 0.f;
+    for (int w = 0; w < NW; ++w) ss += wred_v[w][t];
+    inv_rms[t] = a.gain ? rsqrtf(ss / static_cast<float>(a.K) + a.eps) : 1.f;
+  }
   const uint32_t dt = tmem_base;
-  lane_addr = dt + (static_cast<uint32_t>(warp * 32) << 16);
+  lane_addr = dt + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   for (int g = 0; g < total; ++g) {
     if (g > 0) load_pass(g);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -451,7 +474,7 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
       unsigned char* A = sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
       const unsigned char* Bp = sm + CFG::b + ((k0 - kc0) / kSubK) * kBBytes;
       const uint32_t col0 = DBL ? (g & 1) * 256 : 0;
-      for (int blk = 0; blk < nbk[g & 1]; ++blk) {
+      for (int blk = 0; blk < ((g & 1) ? nb1 : nb0); ++blk) {
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
           const uint32_t koff = (blk >> 1) * kABytes + ((blk & 1) * 2 + ks) * 256;  // 16 K = two core matrices
@@ -482,7 +505,11 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
     ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, 16);
     if (lane < kTcN) wred_v[warp][lane] = ssum;
     __syncthreads();
-    if (t < kTcN) a.ss_out[blockIdx.x * kTcN + t] = wred_v[0][t] + wred_v[1][t] + wred_v[2][t] + wred_v[3][t];
+    if (t < kTcN) {
+      float v = 0.f;
+      for (int w = 0; w < NW; ++w) v += wred_v[w][t];
+      a.ss_out[blockIdx.x * kTcN + t] = v;
+    }
     return;
   }
   if (a.epi != kEpiArgmax) return;
@@ -501,7 +528,7 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   if (t < a.n) {
     float cv = -INFINITY;
     int ci = INT_MAX;
-    for (int w = 0; w < 4; ++w) argmax_merge(cv, ci, wred_v[w][t], wred_i[w][t]);
+    for (int w = 0; w < NW; ++w) argmax_merge(cv, ci, wred_v[w][t], wred_i[w][t]);
     a.seqs[t].amax_v[blockIdx.x] = cv;
     a.seqs[t].amax_i[blockIdx.x] = ci;
   }
@@ -515,7 +542,7 @@ __global__ void __launch_bounds__(kMmThreads, 1) k_mm16(MmArgs a) {
   __syncthreads();
   if (!s_last) return;
   // one warp per sequence reduces the blocks' candidates
-  for (int q = warp; q < a.n; q += 4) {
+  for (int q = warp; q < a.n; q += NW) {
     const DevSeq& s = a.seqs[q];
     float cv = -INFINITY;
     int ci = INT_MAX;
@@ -970,10 +997,10 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
     a.seqs = seqs; a.count = count; a.err = err; a.max_seq = m.max_seq;
     const int tiles = (rows + kTcM - 1) / kTcM;
     if (split) {
-      cudaLaunchConfig_t c = config(tiles * a.cs, kMmThreads, SplitCfg::total, a.cs);
+      cudaLaunchConfig_t c = config(tiles * a.cs, SplitCfg::threads, SplitCfg::total, a.cs);
       return cudaLaunchKernelEx(&c, k_mm16<SplitCfg>, a);
     }
-    cudaLaunchConfig_t c = config(std::min(tiles, num_sms), kMmThreads, HeadCfg::total, 1);
+    cudaLaunchConfig_t c = config(std::min(tiles, num_sms), HeadCfg::threads, HeadCfg::total, 1);
     return cudaLaunchKernelEx(&c, k_mm16<HeadCfg>, a);
   };
   const int lqkv = m.qw + 2 * m.kvw;
