@@ -201,7 +201,8 @@ int32_t tqd_generate_batch(tqd_model* model, int32_t n_seq, const int32_t* first
 int32_t tqd_read_logits(tqd_model* model, int32_t seq, float* host_out);
 
 /* Number of device phases one decode step runs (kernel launches for
- * TQD_SCHED_GRAPH, grid-barrier-separated phases for TQD_SCHED_PERSISTENT) —
+ * TQD_SCHED_GRAPH, barrier-separated phases for TQD_SCHED_PERSISTENT, counting
+ * the grid and the KV-group barriers) —
  * the analogue of the per-token dispatch budget of "Metal LLM decode". */
 int32_t tqd_phase_count(tqd_model* model, int32_t* out);
 
