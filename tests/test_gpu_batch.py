@@ -58,7 +58,7 @@ def batched_vs_oracle(tqd, cfg, n_seq, prompt_len, steps, max_seq, seed=0, kv_hi
 
 def test_batch_tiny_q8(tqd):
     w = batched_vs_oracle(tqd, synth.TINY, 4, 12, 4, 24)
-    assert w < 1e-4  # f32-level: the tf32 split keeps the contraction exact
+    assert w < 1e-4  # f32-level: the three-part bf16 split keeps the contraction exact
 
 
 def test_batch_tiny_bf16(tqd):

@@ -45,26 +45,32 @@ constexpr uint32_t kABytes = kTcM * kSubK * 2;       // one bf16 A sub-chunk
 constexpr uint32_t kAPassBytes = 2 * kABytes;        // A of one pass (up to 128 K)
 constexpr uint32_t kBPartBytes = kTcN * kSubK * 2;   // one bf16 part of B
 constexpr uint32_t kBBytes = 3 * kBPartBytes;        // one sub-chunk of B: N = 48 rows
-constexpr uint32_t kRecvBytes = kTcM * kTcN * 4;     // cluster partials received: [rank][row][16]
-constexpr uint32_t kPassCols = 4 * kTcN3;            // tensor-memory columns of one pass (four blocks)
 constexpr int kMaxCluster = 16;       // 16 is a non-portable cluster size (allowed per kernel)
+// rows of a tile each cluster rank reduces: whole row pairs, split as evenly as
+// the cluster size allows (at most 2 * ceil(64 / cs) rows)
+__host__ __device__ constexpr int pair_row0(int q, int cs) { return 2 * ((q * (kTcM / 2)) / cs); }
+__host__ __device__ constexpr int recv_stride(int cs) { return 2 * ((kTcM / 2 + cs - 1) / cs); }
+constexpr int kRecvRows = 160;       // >= cs * recv_stride(cs) for every cs <= 16
+constexpr uint32_t kPassCols = 4 * kTcN3;            // tensor-memory columns of one pass (four blocks)
 // Split projections (one tile per CTA, two CTAs per SM): B for up to 384
 // columns, one pass of A and of tensor memory at a time.  lm_head (one CTA
 // per SM looping over tiles): B for all of H <= 1024, deeper weight
 // staging, and double-buffered A and tensor memory so one pass's read-out
 // overlaps the next pass's MMAs.
-template <int STAGES, int MAXSUB, bool DBL, int NH>
+template <int STAGES, int MAXSUB, bool DBL, int NH, int RROWS>
 struct MmCfg {
   static constexpr int nh = NH;                  // threads per weight row (each a share of every pass)
   static constexpr int threads = kMmThreads * NH;
   static constexpr uint32_t a = STAGES * kRawBytes;
   static constexpr uint32_t b = a + (DBL ? 2 : 1) * kAPassBytes;
   static constexpr uint32_t recv = b + MAXSUB * kBBytes;
-  static constexpr uint32_t total = recv + NH * kRecvBytes;
+  static constexpr uint32_t total = recv + NH * RROWS * kTcN * 4;  // [rank][row][16] partials received
   static constexpr uint32_t tmem = DBL ? 512 : 256;
 };
-using SplitCfg = MmCfg<2, 6, false, 1>;
-using HeadCfg = MmCfg<3, 16, true, 2>;
+using SplitCfg = MmCfg<2, 6, false, 1, kRecvRows>;  // clusters of up to 16
+using HeadCfg = MmCfg<3, 16, true, 2, kTcM>;        // no cluster
+static_assert(2 * (SplitCfg::total + 2048) <= 228 * 1024, "two split CTAs per SM");
+static_assert(HeadCfg::total + 1024 <= 227 * 1024, "lm_head CTA fits");
 constexpr int kSplitMaxK = 6 * kSubK, kHeadMaxK = 16 * kSubK;
 
 // Shared-memory matrix descriptor, K-major without swizzle: core matrices of
@@ -164,6 +170,17 @@ __device__ __forceinline__ void st_dsmem4(uint32_t addr, float a, float b, float
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+// 16 bytes into another CTA's shared memory, counted on that CTA's mbarrier
+// (both addresses from mapa)
+__device__ __forceinline__ void st_async4(uint32_t addr, uint32_t bar, float a, float b, float c, float d) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ uint32_t mapa_u32(const void* p, uint32_t cta) {
   uint32_t a;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(cta));
@@ -189,6 +206,12 @@ struct MmArgs {
   uint32_t* count;      // kEpiArgmax: arrivals of all blocks
   uint32_t* err;
   int max_seq;
+  // X given as split-K attention partials instead (nullptr: plain X): per
+  // sequence b, head h and chunk c, part_o[((b * K / hd + h) * nch + c) * hd + d]
+  // and part_ml[((b * K / hd + h) * nch + c) * 2 + {0, 1}] = (max, sum)
+  const float* part_o;
+  const float* part_ml;
+  int nch, hd;
 };
 
 // Thread t of the CTA works on weight row t % 128 of the current tile (tensor
@@ -204,6 +227,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   constexpr int NH = CFG::nh, NT = CFG::threads, NW = NT / 32;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ __align__(8) uint64_t bars[2];  // a pass's MMAs are complete (by pass parity)
+  __shared__ __align__(8) uint64_t rbar;     // every cluster rank's partials of this CTA's rows have landed
   __shared__ uint32_t tmem_base;
   __shared__ float inv_rms[kTcN];
   __shared__ float wred_v[NW][kTcN];
@@ -213,7 +237,9 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   const int tr = t & (kTcM - 1), hf = t / kTcM;  // weight row of the tile, share of the row
   const int rank = static_cast<int>(cluster_rank());
   const bool q8 = a.fmt == kFmtQ8;
-  const int KR = a.K / a.cs, kc0 = rank * KR;
+  // this rank's K range: whole 32-wide blocks, split as evenly as the cluster size allows
+  const int nbk = a.K / 32;
+  const int kc0 = 32 * ((rank * nbk) / a.cs), KR = 32 * (((rank + 1) * nbk) / a.cs) - kc0;
   const int PK = q8 ? kPassBytes : kPassBytes / 2;  // K per pass
   const int npass = (KR + PK - 1) / PK;
   const int tiles = (a.rows + kTcM - 1) / kTcM;
@@ -248,10 +274,21 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
                   ? ld_weights_u16(a.W + static_cast<size_t>(row) * a.rb + a.K + 2 * (k0 / 32 + i))
                   : static_cast<uint16_t>(0);
   };
+  // split-K over a cluster (one tile per CTA): every rank sends its partial
+  // sums of the rows rank q owns straight into q's shared memory with st.async,
+  // and q waits on rbar for all of them (no cluster-wide barrier after the
+  // MMAs); rows [own0, own0 + own) of the tile are this rank's
+  const bool push = a.cs > 1 && NH == 1;
+  const int own0 = pair_row0(rank, a.cs), own = pair_row0(rank + 1, a.cs) - own0;
   if (t == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
+    mbar_init(&rbar, 1);
+    if (push) mbar_arrive_expect_tx(&rbar, static_cast<uint32_t>(a.cs * own * kTcN * 4));
     fence_mbar_init();
+  }
+  if (a.gain) {  // the RMSNorm gain of this rank's K range, into L2 ahead of the dependency wait
+    for (int i = t; i < KR / 32; i += NT) prefetch_l2(a.gain + kc0 + 32 * i);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -281,6 +318,10 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   float ssum = 0.f, bv = -INFINITY;
   int bi = INT_MAX;
   float* recv = reinterpret_cast<float*>(sm + CFG::recv);
+  // kEpiResid: the residual of this thread's first epilogue item, loaded with
+  // the activations (one round trip) instead of after the reduction
+  float res0 = 0.f, res1 = 0.f;
+  bool res_pre = false;
   uint32_t lane_addr = 0;
   // read out pass q: scale each block's column sums and add them up
   auto readout = [&](int q) {
@@ -307,28 +348,40 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   // epilogue; thread t handles row pairs (2m, 2m+1) of the rows this CTA owns
   // for sequence t % 16, summing the partials in rank order
   auto epilogue = [&](int tile, bool more) {
-    const int rpc = kTcM / a.cs, row0 = tile * kTcM;
+    const int rs = recv_stride(a.cs), row0 = tile * kTcM;
     {
-      const int q = tr / rpc, lr = tr - q * rpc;
-      const uint32_t dst = mapa_u32(recv + ((rank * NH + hf) * rpc + lr) * kTcN, static_cast<uint32_t>(q));
+      const int q = ((tr / 2 + 1) * a.cs - 1) / (kTcM / 2);  // the rank that owns row tr
+      const int lr = tr - pair_row0(q, a.cs);
+      const uint32_t dst = mapa_u32(recv + ((rank * NH + hf) * rs + lr) * kTcN, static_cast<uint32_t>(q));
+      if (push) {
+        const uint32_t qbar = mapa_u32(&rbar, static_cast<uint32_t>(q));
 #pragma unroll
-      for (int i = 0; i < kTcN / 4; ++i)
-        st_dsmem4(dst + 16 * i, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        for (int i = 0; i < kTcN / 4; ++i)
+          st_async4(dst + 16 * i, qbar, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTcN / 4; ++i)
+          st_dsmem4(dst + 16 * i, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+      }
 #pragma unroll
       for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
     }
-    cluster_sync();
+    if (push) {
+      if (!mbar_wait_bounded(&rbar, 0u, a.err)) ok = false;
+    } else {
+      cluster_sync();
+    }
     const float scl = inv_rms[b_ep];
-    for (int idx = t; idx < rpc * (kTcN / 2); idx += NT) {
+    for (int idx = t; idx < own * (kTcN / 2); idx += NT) {
       const int lr = 2 * (idx / kTcN);
       float v0 = 0.f, v1 = 0.f;
       for (int q = 0; q < a.cs * NH; ++q) {
-        v0 += recv[(q * rpc + lr) * kTcN + b_ep];
-        v1 += recv[(q * rpc + lr + 1) * kTcN + b_ep];
+        v0 += recv[(q * rs + lr) * kTcN + b_ep];
+        v1 += recv[(q * rs + lr + 1) * kTcN + b_ep];
       }
       v0 *= scl;
       v1 *= scl;
-      const int r0 = row0 + rank * rpc + lr, r1 = r0 + 1;
+      const int r0 = row0 + own0 + lr, r1 = r0 + 1;
       if (b_ep >= a.n || r0 >= a.rows) continue;
       const bool ok1 = r1 < a.rows;
       if (a.epi == kEpiSwiGLU) {
@@ -344,8 +397,9 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
       } else {
         float* y = a.Y + static_cast<size_t>(b_ep) * a.ldy;
         if (a.epi == kEpiResid) {
-          v0 += y[r0];
-          if (ok1) v1 += y[r1];
+          const bool pre = res_pre && idx == t;
+          v0 += pre ? res0 : y[r0];
+          if (ok1) v1 += pre ? res1 : y[r1];
           ssum = fmaf(v0, v0, ssum);
           if (ok1) ssum = fmaf(v1, v1, ssum);
         }
@@ -400,38 +454,163 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
             *reinterpret_cast<const uint4*>(raw + ((ch ^ (tr & 7)) << 4));
     }
   };
+  // a CTA with two passes of one tile dequantises its second pass before the
+  // wait too: that pass's quants are read from raw stage 1 into registers, and
+  // after a barrier its bf16 A is written over both raw stages (A's size)
+  const bool pre2 = !DBL && STAGES == 2 && NH == 1 && ntile == 1 && npass == 2;
+  static_assert(DBL || CFG::a >= kAPassBytes || STAGES != 2, "pass-1 A fits the raw stages");
+  auto prep_pass1 = [&]() {
+    const int k0 = kc0 + PK, pk = min(PK, kc0 + KR - k0);
+    nb1 = pk / 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc1[i] = q8 ? __half2float(__ushort_as_half(sc_next[i])) : 1.f;
+    cp_async_wait<0>();
+    __syncthreads();
+    const unsigned char* raw = sm + kRawBytes + tr * kPassBytes;
+    const int nch = q8 ? pk / 16 : pk / 8;
+    uint4 w[8];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      w[ch] = ch < nch ? *reinterpret_cast<const uint4*>(raw + ((ch ^ (tr & 7)) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      if (ch >= nch) break;
+      if (q8) {
+        uint32_t o[8];
+        i8x4_to_bf16x4(w[ch].x, o[0], o[1]);
+        i8x4_to_bf16x4(w[ch].y, o[2], o[3]);
+        i8x4_to_bf16x4(w[ch].z, o[4], o[5]);
+        i8x4_to_bf16x4(w[ch].w, o[6], o[7]);
+        unsigned char* As = sm + (ch >> 2) * kABytes;
+        const int kk = (ch & 3) * 16;
+        *reinterpret_cast<uint4*>(As + core_off16(tr, kk)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(As + core_off16(tr, kk + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+      } else {
+        *reinterpret_cast<uint4*>(sm + core_off16(tr, ch * 8)) = w[ch];
+      }
+    }
+  };
   // the first pass's weights are dequantised before the wait as well
   if (total > 0) load_pass(0);
+  if (pre2) prep_pass1();
+  if (push) cluster_sync();  // every rank's rbar is initialised before any partial is sent
   pdl_wait();
   pdl_launch_dependents();
   // inputs of the previous kernel: the RMSNorm sums of squares and B for the
   // CTA's whole K range (16 batch rows x KR activations times the gain, three
   // bf16 parts per sub-chunk: rows 0-15, 16-31, 32-47 of the N = 48 operand)
   {
-    float ss = 0.f;
-    if (a.gain)
-      for (int i = t; i < a.nss * kTcN; i += NT) ss += __ldcg(a.ss + i);  // sequence i % 16 = t % 16
+    // partial sums of squares, [nss][16]: thread t adds the float4 columns of
+    // sequences 4 (t % 4) .. 4 (t % 4) + 3; the first four loads per thread
+    // are issued before the activations' and consumed after them
+    const float4* ss4 = reinterpret_cast<const float4*>(a.ss);
+    const int n4 = a.gain ? a.nss * (kTcN / 4) : 0;
+    float4 sv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      sv[u] = t + u * NT < n4 ? __ldcg(ss4 + t + u * NT) : make_float4(0.f, 0.f, 0.f, 0.f);
     const int nsubs = (KR + kSubK - 1) / kSubK;
+    const bool parts = !DBL && a.part_o != nullptr;  // the split projections only
+    if (a.epi == kEpiResid && ntile == 1 && t < own * (kTcN / 2)) {
+      const int r0 = tile0 * kTcM + own0 + 2 * (t / kTcN);
+      if (b_ep < a.n && r0 < a.rows) {
+        const float* y = a.Y + static_cast<size_t>(b_ep) * a.ldy;
+        res0 = __ldcg(y + r0);
+        if (r0 + 1 < a.rows) res1 = __ldcg(y + r0 + 1);
+        res_pre = true;
+      }
+    }
     const int b = (t >> 3) & (kTcN - 1), k8 = (t & 7) * 8;
     // thread share hf builds sub-chunks hf, hf + NH, ...
     for (int s0 = hf; s0 < nsubs; s0 += 4 * NH) {
-      float4 xv[4][2];
+      // every load of the round first (activations, gains), arithmetic after
+      float4 xv[4][2], gv[4][2];
+      bool vld[4];
+      const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f), one4 = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        xv[i][0] = xv[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
         const int sidx = s0 + i * NH;
-        if (sidx < nsubs && b < a.n && k8 < min(kSubK, KR - sidx * kSubK)) {
-          const float* src = a.X + static_cast<size_t>(b) * a.ldx + kc0 + sidx * kSubK + k8;
-          xv[i][0] = __ldcg(reinterpret_cast<const float4*>(src));
-          xv[i][1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-          if (a.gain) {
-            const float* gp = a.gain + kc0 + sidx * kSubK + k8;
-            const float4 g0 = __ldg(reinterpret_cast<const float4*>(gp));
-            const float4 g1 = __ldg(reinterpret_cast<const float4*>(gp + 4));
-            xv[i][0].x *= g0.x; xv[i][0].y *= g0.y; xv[i][0].z *= g0.z; xv[i][0].w *= g0.w;
-            xv[i][1].x *= g1.x; xv[i][1].y *= g1.y; xv[i][1].z *= g1.z; xv[i][1].w *= g1.w;
+        vld[i] = sidx < nsubs && b < a.n && k8 < min(kSubK, KR - sidx * kSubK);
+        if (parts) continue;
+        const float4* src = reinterpret_cast<const float4*>(
+            a.X + (vld[i] ? static_cast<size_t>(b) * a.ldx + kc0 + sidx * kSubK + k8 : 0));
+        xv[i][0] = vld[i] ? __ldcg(src) : zero4;
+        xv[i][1] = vld[i] ? __ldcg(src + 1) : zero4;
+      }
+      if (parts) {
+        // merge the attention chunks of each element's head by log-sum-exp,
+        // two chunks per round for all four sub-chunks (branch-free, so every
+        // load of a round is issued before its arithmetic)
+        float M[4], L[4];
+        float4 o0[4], o1[4];
+        size_t base[4];
+        int dd[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int k = kc0 + (s0 + i * NH) * kSubK + k8, h = k / a.hd;
+          dd[i] = k - h * a.hd;
+          base[i] = (static_cast<size_t>(b) * (a.K / a.hd) + h) * a.nch;
+          M[i] = -INFINITY;
+          L[i] = 0.f;
+          o0[i] = o1[i] = zero4;
+        }
+        for (int c = 0; c < a.nch; c += 2) {
+          const bool two = c + 1 < a.nch;
+          float2 ml[4][2];
+          float4 q[4][2][2];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const bool on = vld[i] && (j == 0 || two);
+              const size_t e = on ? base[i] + c + j : 0;
+              ml[i][j] = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + e);
+              const float4* po = reinterpret_cast<const float4*>(a.part_o + (on ? e * a.hd + dd[i] : 0));
+              q[i][j][0] = __ldcg(po);
+              q[i][j][1] = __ldcg(po + 1);
+              if (!on) {  // a placeholder load: weight zero, and no NaN from unwritten memory
+                ml[i][j] = make_float2(-INFINITY, 0.f);
+                q[i][j][0] = q[i][j][1] = zero4;
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float Mn = fmaxf(M[i], fmaxf(ml[i][0].x, ml[i][1].x));
+            const float f = M[i] == -INFINITY ? 0.f : expf(M[i] - Mn);
+            const float w0 = ml[i][0].x == -INFINITY ? 0.f : expf(ml[i][0].x - Mn);
+            const float w1 = ml[i][1].x == -INFINITY ? 0.f : expf(ml[i][1].x - Mn);
+            L[i] = fmaf(w1, ml[i][1].y, fmaf(w0, ml[i][0].y, L[i] * f));
+            o0[i].x = fmaf(w1, q[i][1][0].x, fmaf(w0, q[i][0][0].x, o0[i].x * f));
+            o0[i].y = fmaf(w1, q[i][1][0].y, fmaf(w0, q[i][0][0].y, o0[i].y * f));
+            o0[i].z = fmaf(w1, q[i][1][0].z, fmaf(w0, q[i][0][0].z, o0[i].z * f));
+            o0[i].w = fmaf(w1, q[i][1][0].w, fmaf(w0, q[i][0][0].w, o0[i].w * f));
+            o1[i].x = fmaf(w1, q[i][1][1].x, fmaf(w0, q[i][0][1].x, o1[i].x * f));
+            o1[i].y = fmaf(w1, q[i][1][1].y, fmaf(w0, q[i][0][1].y, o1[i].y * f));
+            o1[i].z = fmaf(w1, q[i][1][1].z, fmaf(w0, q[i][0][1].z, o1[i].z * f));
+            o1[i].w = fmaf(w1, q[i][1][1].w, fmaf(w0, q[i][0][1].w, o1[i].w * f));
+            M[i] = Mn == -INFINITY ? M[i] : Mn;
           }
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const bool nz = L[i] > 0.f;
+          xv[i][0] = nz ? make_float4(o0[i].x / L[i], o0[i].y / L[i], o0[i].z / L[i], o0[i].w / L[i]) : zero4;
+          xv[i][1] = nz ? make_float4(o1[i].x / L[i], o1[i].y / L[i], o1[i].z / L[i], o1[i].w / L[i]) : zero4;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool gl = a.gain && vld[i];
+        const float4* gp = reinterpret_cast<const float4*>(gl ? a.gain + kc0 + (s0 + i * NH) * kSubK + k8 : a.gain);
+        gv[i][0] = gl ? __ldg(gp) : one4;
+        gv[i][1] = gl ? __ldg(gp + 1) : one4;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xv[i][0].x *= gv[i][0].x; xv[i][0].y *= gv[i][0].y; xv[i][0].z *= gv[i][0].z; xv[i][0].w *= gv[i][0].w;
+        xv[i][1].x *= gv[i][1].x; xv[i][1].y *= gv[i][1].y; xv[i][1].z *= gv[i][1].z; xv[i][1].w *= gv[i][1].w;
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -451,8 +630,26 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
             make_uint4(p3[0] | (p3[1] << 16), p3[2] | (p3[3] << 16), p3[4] | (p3[5] << 16), p3[6] | (p3[7] << 16));
       }
     }
-    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 16);
-    if (lane < kTcN) wred_v[warp][lane] = ss;
+    for (int i = t + 4 * NT; i < n4; i += 4 * NT) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (i + u * NT >= n4) break;
+        const float4 v = __ldcg(ss4 + i + u * NT);
+        sv[u].x += v.x; sv[u].y += v.y; sv[u].z += v.z; sv[u].w += v.w;
+      }
+    }
+    float s4[4] = {(sv[0].x + sv[1].x) + (sv[2].x + sv[3].x), (sv[0].y + sv[1].y) + (sv[2].y + sv[3].y),
+                   (sv[0].z + sv[1].z) + (sv[2].z + sv[3].z), (sv[0].w + sv[1].w) + (sv[2].w + sv[3].w)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s4[e] += __shfl_xor_sync(0xFFFFFFFFu, s4[e], 4);
+      s4[e] += __shfl_xor_sync(0xFFFFFFFFu, s4[e], 8);
+      s4[e] += __shfl_xor_sync(0xFFFFFFFFu, s4[e], 16);
+    }
+    if (lane < 4) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) wred_v[warp][4 * lane + e] = s4[e];
+    }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -465,13 +662,16 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   const uint32_t dt = tmem_base;
   lane_addr = dt + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   for (int g = 0; g < total; ++g) {
-    if (g > 0) load_pass(g);
+    if (g > 0) {
+      if (pre2) readout(0);  // the tensor memory is free for pass 1
+      else load_pass(g);
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     if (t == 0) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int k0 = kc0 + (g % npass) * PK;
-      unsigned char* A = sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
+      unsigned char* A = pre2 && g == 1 ? sm : sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
       const unsigned char* Bp = sm + CFG::b + ((k0 - kc0) / kSubK) * kBBytes;
       const uint32_t col0 = DBL ? (g & 1) * 256 : 0;
       for (int blk = 0; blk < ((g & 1) ? nb1 : nb0); ++blk) {
@@ -564,19 +764,29 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   if (t == 0) *a.count = 0u;
 }
 
-// CTAs per tile (the cluster) for a [rows x K] projection: the largest of 16,
-// 8, 4, 2, 1 whose share of K is whole 32-wide blocks and fits the CTA's B
-// buffer, preferring sizes that keep every CTA of the launch in one wave at
-// two CTAs per SM; 0 if none fits.
+// CTAs per tile (the cluster) for a [rows x K] projection.  A rank's share of
+// K is whole 32-wide blocks (ceil(blocks / cs) at most), which must fit the
+// CTA's B buffer.  Each 128-K pass of a CTA's share adds a dependent
+// dequantise / MMA / read-out round after the activations arrive, so the
+// fewest passes win; among those, the smallest cluster (the fewest CTAs, so
+// the next kernel's CTAs find room to start early) whose CTAs all fit one
+// wave at two CTAs per SM.  0 if no size fits.
 int mm_cluster(int K, int rows, int num_sms) {
-  const int tiles = (rows + kTcM - 1) / kTcM;
-  int fit = 0;
-  for (int c = kMaxCluster; c >= 1; c >>= 1) {
-    if (K % (32 * c) != 0 || K / c > kSplitMaxK) continue;
-    if (tiles * c <= 2 * num_sms) return c;
-    if (!fit) fit = c;
+  const int tiles = (rows + kTcM - 1) / kTcM, nbk = K / 32;
+  if (K % 32 != 0) return 0;
+  int best = 0, best_passes = 0, fallback = 0;
+  for (int c = 1; c <= kMaxCluster && c <= nbk; ++c) {
+    const int kr = 32 * ((nbk + c - 1) / c);
+    if (kr > kSplitMaxK) continue;
+    if (!fallback) fallback = c;
+    const int passes = (kr + kPassBytes - 1) / kPassBytes;
+    if (tiles * c > 2 * num_sms) continue;
+    if (!best || passes < best_passes) {
+      best = c;
+      best_passes = passes;
+    }
   }
-  return fit;
+  return best ? best : fallback;
 }
 
 // ---------------------------------------------------------------- embedding
@@ -625,9 +835,10 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------- attention
 // One block per (sequence, kv head, chunk): a producer thread streams the
 // chunk's cached K/V rows into a small shared-memory ring with bulk copies;
-// eight consumer warps run the online softmax; the last chunk of a (sequence,
-// kv head) combines the chunks ("Eight kernels", attention_decode, as a
-// split-K flash decode).
+// eight consumer warps run the online softmax and the block writes its
+// chunk's partial (max, sum, weighted V) per head; the O projection merges the
+// chunks by log-sum-exp while it stages its input ("Eight kernels",
+// attention_decode, as a split-K flash decode).
 constexpr int kAW = 8;                  // consumer warps
 constexpr int kAT = kAW * 32;           // consumer threads
 constexpr int kASlots = 3;
@@ -637,7 +848,7 @@ __device__ __forceinline__ void async() { asm volatile("bar.sync 1, %0;" ::"n"(k
 
 template <int HD, int G>
 __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, int g, int c, int nch,
-                                const float* qkv, float* attn, unsigned char* sm) {
+                                const float* qkv, float* po, float* pml, unsigned char* sm) {
   constexpr int NJ = HD / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kASlots * kASlotBytes);
@@ -832,46 +1043,17 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
         Ls = fmaf(f, ws[HD + 1], Ls);
       }
     const int h = g * G + hh;
-    s.part_o[(static_cast<size_t>(h) * nch + c) * HD + d] = O;
+    po[(static_cast<size_t>(h) * nch + c) * HD + d] = O;
     if (d == 0) {
-      s.part_ml[(static_cast<size_t>(h) * nch + c) * 2] = M;
-      s.part_ml[(static_cast<size_t>(h) * nch + c) * 2 + 1] = Ls;
+      pml[(static_cast<size_t>(h) * nch + c) * 2] = M;
+      pml[(static_cast<size_t>(h) * nch + c) * 2 + 1] = Ls;
     }
   }
-  async();
-  __shared__ uint32_t s_last;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t old = atomicAdd(s.attn_count + g, 1u);
-    s_last = old == static_cast<uint32_t>(nch) - 1u;
-    if (s_last) __threadfence();
-  }
-  async();
-  if (!s_last) return;
-  for (int idx = threadIdx.x; idx < G * HD; idx += kAT) {
-    const int hh = idx / HD, d = idx - hh * HD;
-    const int h = g * G + hh;
-    const float* ml = s.part_ml + static_cast<size_t>(h) * nch * 2;
-    const float* po = s.part_o + static_cast<size_t>(h) * nch * HD;
-    float M = -INFINITY;
-    for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(ml + 2 * cc));
-    float num = 0.f, den = 0.f;
-    for (int cc = 0; cc < nch; ++cc) {
-      const float mc = __ldcg(ml + 2 * cc);
-      if (mc == -INFINITY) continue;
-      const float f = expf(mc - M);
-      num = fmaf(f, __ldcg(po + static_cast<size_t>(cc) * HD + d), num);
-      den = fmaf(f, __ldcg(ml + 2 * cc + 1), den);
-    }
-    attn[h * HD + d] = num / den;
-  }
-  async();
-  if (threadIdx.x == 0) s.attn_count[g] = 0u;
 }
 
 template <int HD, int G>
 __global__ void __launch_bounds__(kAT + 32, 2)
-    k_attn_batch(DevModel m, const DevSeq* seqs, int layer, int nch, const float* QKV, float* ATTN) {
+    k_attn_batch(DevModel m, const DevSeq* seqs, int layer, int nch, const float* QKV, float* PO, float* PML) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int per_seq = m.nkv * nch;
   const int b = blockIdx.x / per_seq, item = blockIdx.x - b * per_seq;
@@ -888,8 +1070,9 @@ __global__ void __launch_bounds__(kAT + 32, 2)
   __syncthreads();
   if (s.state->pos >= static_cast<uint32_t>(m.max_seq)) return;
   const float* qkv = QKV + static_cast<size_t>(b) * (m.qw + 2 * m.kvw);
-  float* attn = ATTN + static_cast<size_t>(b) * m.qw;
-  attn_batch_item<HD, G>(m, s, layer, g, c, nch, qkv, attn, sm);
+  float* po = PO + static_cast<size_t>(b) * m.nq * nch * HD;
+  float* pml = PML + static_cast<size_t>(b) * m.nq * nch * 2;
+  attn_batch_item<HD, G>(m, s, layer, g, c, nch, qkv, po, pml, sm);
 }
 
 // The attention kernel instantiated for the model's head_dim and group size.
@@ -952,7 +1135,7 @@ cudaError_t batch_setup(const DevModel& m) {
 // it starts streaming its weights (or cached K/V rows) while its predecessor
 // finishes, and waits for it before touching activations.
 cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const DevSeq* seqs,
-                               int n, int nch, float* X, float* QKV, float* ATTN, float* H, float* SS,
+                               int n, int nch, float* X, float* QKV, float* PO, float* PML, float* H, float* SS,
                                uint32_t* count, uint32_t* err, cudaStream_t st) {
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -988,13 +1171,17 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
   cudaError_t e = cudaLaunchKernelEx(&ce, k_embed_batch, m, seqs, n, X, ss_x, nss_x);
   if (e != cudaSuccess) return e;
   auto mm = [&](const uint8_t* W, size_t rb, int K, int rows, const float* Xin, int ldx, const float* gain,
-                const float* ss, int nss, int epi, float* Y, int ldy, float* ss_out, bool split) {
+                const float* ss, int nss, int epi, float* Y, int ldy, float* ss_out, bool split,
+                bool from_parts = false) {
     MmArgs a{};
     a.W = W; a.rb = rb; a.K = K; a.rows = rows; a.fmt = fmt;
     a.cs = split ? mm_cluster(K, rows, num_sms) : 1;
     a.X = Xin; a.ldx = ldx; a.n = n; a.gain = gain; a.ss = ss; a.nss = nss; a.eps = m.eps;
     a.epi = epi; a.Y = Y; a.ldy = ldy; a.ss_out = ss_out;
     a.seqs = seqs; a.count = count; a.err = err; a.max_seq = m.max_seq;
+    if (from_parts) {  // X is the attention's chunk partials, merged while B is built
+      a.part_o = PO; a.part_ml = PML; a.nch = nch; a.hd = m.hd;
+    }
     const int tiles = (rows + kTcM - 1) / kTcM;
     if (split) {
       cudaLaunchConfig_t c = config(tiles * a.cs, SplitCfg::threads, SplitCfg::total, a.cs);
@@ -1016,12 +1203,13 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
       const DevSeq* sq = seqs;
       int layer = l, nc = nch;
       const float* q = QKV;
-      float* o = ATTN;
-      void* args[] = {&mm_, &sq, &layer, &nc, &q, &o};
+      float* po = PO;
+      float* pml = PML;
+      void* args[] = {&mm_, &sq, &layer, &nc, &q, &po, &pml};
       if ((e = cudaLaunchKernelExC(&ca, attn_fn, args)) != cudaSuccess) return e;
     }
-    if ((e = mm(L.wo, m.row_bytes_qw, m.qw, m.H, ATTN, m.qw, nullptr, nullptr, 0, kEpiResid, X, m.H, ss_mid,
-                true)) != cudaSuccess)
+    if ((e = mm(L.wo, m.row_bytes_qw, m.qw, m.H, nullptr, m.qw, nullptr, nullptr, 0, kEpiResid, X, m.H, ss_mid,
+                true, true)) != cudaSuccess)
       return e;
     if ((e = mm(L.wgu, m.row_bytes_h, m.H, 2 * m.I, X, m.H, L.ffn_norm, ss_mid, nss_mid, kEpiSwiGLU, H, m.I,
                 nullptr, true)) != cudaSuccess)

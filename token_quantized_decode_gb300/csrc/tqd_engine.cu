@@ -70,7 +70,7 @@ struct tqd_model {
   // batched step: activations of up to batch_max() sequences, the device copy
   // of the sequences' descriptors, one graph per batch size
   bool batch_ok = false;
-  float *bx = nullptr, *bqkv = nullptr, *battn = nullptr, *bh = nullptr;
+  float *bx = nullptr, *bqkv = nullptr, *bpo = nullptr, *bpml = nullptr, *bh = nullptr;
   DevSeq* dseqs = nullptr;
   uint32_t* bcount = nullptr;
   float* bss = nullptr;
@@ -461,11 +461,12 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   }
   // batched-step buffers (only for models holding several sequences)
   const int bmax = batch_max();
-  size_t o_bx = 0, o_bqkv = 0, o_battn = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0;
+  size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0;
   if (cfg->max_batch > 1) {
     o_bx = take(4ull * bmax * H);
     o_bqkv = take(4ull * bmax * (qw + 2 * kvw));
-    o_battn = take(4ull * bmax * qw);
+    o_bpo = take(4ull * bmax * nq * nch * hd);  // attention chunk partials (at most n_chunks chunks)
+    o_bpml = take(4ull * bmax * nq * nch * 2);
     o_bh = take(4ull * bmax * I);
     o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);
     o_bcount = take(4);
@@ -635,7 +636,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   if (cfg->max_batch > 1 && batch_supported(dm) && (V + 127) / 128 <= kMaxArgmaxBlocks) {
     m->bx = reinterpret_cast<float*>(base + o_bx);
     m->bqkv = reinterpret_cast<float*>(base + o_bqkv);
-    m->battn = reinterpret_cast<float*>(base + o_battn);
+    m->bpo = reinterpret_cast<float*>(base + o_bpo);
+    m->bpml = reinterpret_cast<float*>(base + o_bpml);
     m->bh = reinterpret_cast<float*>(base + o_bh);
     m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
     m->bcount = reinterpret_cast<uint32_t*>(base + o_bcount);
@@ -859,7 +861,7 @@ int32_t run_batch(tqd_model* m, int n, int steps) {
     cudaGraph_t graph = nullptr;
     CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
     cudaError_t e = enqueue_batch_step(m->dm, m->host_layers.data(), m->dseqs, n, nch, m->bx, m->bqkv,
-                                       m->battn, m->bh, m->bss, m->bcount, &m->seqs[0].d.state->err,
+                                       m->bpo, m->bpml, m->bh, m->bss, m->bcount, &m->seqs[0].d.state->err,
                                        m->stream);
     cudaError_t e2 = cudaStreamEndCapture(m->stream, &graph);
     if (e != cudaSuccess) {

@@ -100,8 +100,9 @@ int batch_max();
 int batch_ss_slots(int H);  // partial sums of squares per activation ([slots][batch_max()])
 bool batch_supported(const DevModel& m);
 cudaError_t batch_setup(const DevModel& m);
+// PO / PML: the attention's chunk partials, [n][nq][nch][hd] and [n][nq][nch][2].
 cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const DevSeq* seqs,
-                               int n, int nch, float* X, float* QKV, float* ATTN, float* H, float* SS,
+                               int n, int nch, float* X, float* QKV, float* PO, float* PML, float* H, float* SS,
                                uint32_t* count, uint32_t* err, cudaStream_t st);
 
 // Record the text tqd_last_error() returns on this thread.
