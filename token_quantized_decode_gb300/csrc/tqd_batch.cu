@@ -91,12 +91,54 @@ constexpr uint32_t idesc_bf16(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// kind::f16 with f16 A and B, f32 accumulator, both K-major, shape M x N.
+constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+constexpr int kHdN = 2 * kTcN;  // the lm_head's MMA N: two f16 parts of every batch row
+__device__ __forceinline__ void mma_f16_hd(uint32_t dt, uint64_t ad, uint64_t bd, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dt),
+      "l"(ad), "l"(bd), "r"(idesc_f16(kTcM, kHdN)), "r"(acc)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t dt, uint64_t ad, uint64_t bd, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dt),
       "l"(ad), "l"(bd), "r"(idesc_bf16(kTcM, kTcN3)), "r"(acc)
       : "memory");
+}
+
+// The MMAs of one pass: nb 32-wide blocks, two K = 16 steps each, block blk
+// into accumulator columns d + blk * n.  da / db are the descriptors of the
+// pass's A and of its first B sub-chunk; a descriptor's address field is the
+// byte address / 16 (shared memory stays below 256 KB, so adding an offset
+// / 16 never carries out of the field).  With nb == 4 (a full pass) the loop
+// is unrolled to constant offsets: one thread issues these, so its
+// instruction count per MMA is on the critical path.
+template <bool F16>
+__device__ __forceinline__ void mma_pass(uint32_t d, int n, uint64_t da, uint64_t db, uint32_t bsub, int nb) {
+  auto one = [&](int blk, int ks) {
+    const uint32_t koff = (blk >> 1) * kABytes + ((blk & 1) * 2 + ks) * 256;  // 16 K = two core matrices
+    const uint32_t boff = (blk >> 1) * bsub + ((blk & 1) * 2 + ks) * 256;
+    if (F16) mma_f16_hd(d + blk * n, da + (koff >> 4), db + (boff >> 4), ks ? 1u : 0u);
+    else mma_bf16(d + blk * n, da + (koff >> 4), db + (boff >> 4), ks ? 1u : 0u);
+  };
+  if (nb == 4) {
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      one(blk, 0);
+      one(blk, 1);
+    }
+  } else {
+    for (int blk = 0; blk < nb; ++blk) {
+      one(blk, 0);
+      one(blk, 1);
+    }
+  }
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -129,6 +171,26 @@ __device__ __forceinline__ void split3_bf16(float x, uint32_t& p1, uint32_t& p2,
   p1 = __bfloat16_as_ushort(h1);
   p2 = __bfloat16_as_ushort(h2);
   p3 = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+}
+
+// Four int8 (one word) -> four f16 (two words), exact: the byte plus 128 is
+// placed in the mantissa of 1024 (f16 0x64xx), and 1152 is subtracted.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t t = w ^ 0x80808080u;
+  const __half2 bias = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6480u)));
+  uint32_t l = __byte_perm(t, 0x64646464u, 0x4140), h = __byte_perm(t, 0x64646464u, 0x4342);
+  const __half2 hl = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
+  const __half2 hh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&hl);
+  hi = *reinterpret_cast<const uint32_t*>(&hh);
+}
+
+// x = x1 + x2 + r, each part f16, |r| <= 2^-22 |x| while 2^-3 <= |x| < 65504
+// (below, |r| <= 2^-25: the second part reaches the f16 subnormals).
+__device__ __forceinline__ void split2_f16(float x, uint32_t& p1, uint32_t& p2) {
+  const __half h1 = __float2half_rn(x);
+  p1 = __half_as_ushort(h1);
+  p2 = __half_as_ushort(__float2half_rn(x - __half2float(h1)));
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -301,8 +363,10 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
     if (g < total) issue_raw(g);
     else cp_async_commit();  // empty groups keep the group count uniform
   }
-  uint16_t sc_next[4];
+  // block scales of the next two passes, loaded as far ahead as their quants
+  uint16_t sc_next[4], sc_next2[4];
   load_scales(0, sc_next);
+  load_scales(1, sc_next2);
   // per-pass state of the two passes in flight, kept in registers (even and
   // odd passes as separate variables: an array indexed by the pass parity
   // would live in local memory, which misses the small L1 left beside the
@@ -423,7 +487,9 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) sc0[i] = q8 ? __half2float(__ushort_as_half(sc_next[i])) : 1.f;
     }
-    load_scales(g + 1, sc_next);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc_next[i] = sc_next2[i];
+    load_scales(g + 2, sc_next2);
     // keep STAGES - 1 passes in flight ahead of this one
     if (g + STAGES - 1 < total) issue_raw(g + STAGES - 1);
     else cp_async_commit();
@@ -674,15 +740,8 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
       unsigned char* A = pre2 && g == 1 ? sm : sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
       const unsigned char* Bp = sm + CFG::b + ((k0 - kc0) / kSubK) * kBBytes;
       const uint32_t col0 = DBL ? (g & 1) * 256 : 0;
-      for (int blk = 0; blk < ((g & 1) ? nb1 : nb0); ++blk) {
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint32_t koff = (blk >> 1) * kABytes + ((blk & 1) * 2 + ks) * 256;  // 16 K = two core matrices
-          const uint32_t boff = (blk >> 1) * kBBytes + ((blk & 1) * 2 + ks) * 256;
-          mma_bf16(dt + col0 + blk * kTcN3, smem_desc(A + koff, 128, (kSubK / 8) * 128),
-                   smem_desc(Bp + boff, 128, (kSubK / 8) * 128), ks ? 1u : 0u);
-        }
-      }
+      mma_pass<false>(dt + col0, kTcN3, smem_desc(A, 128, (kSubK / 8) * 128), smem_desc(Bp, 128, (kSubK / 8) * 128),
+                      kBBytes, (g & 1) ? nb1 : nb0);
       mma_commit(&bars[g & 1]);
     }
     if (DBL && g > 0) {
@@ -742,6 +801,405 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   __syncthreads();
   if (!s_last) return;
   // one warp per sequence reduces the blocks' candidates
+  for (int q = warp; q < a.n; q += NW) {
+    const DevSeq& s = a.seqs[q];
+    float cv = -INFINITY;
+    int ci = INT_MAX;
+    for (int k = lane; k < static_cast<int>(gridDim.x); k += 32)
+      argmax_merge(cv, ci, __ldcg(s.amax_v + k), __ldcg(s.amax_i + k));
+    warp_argmax(cv, ci);
+    if (lane == 0) {
+      const uint32_t pos = s.state->pos;
+      int next = ci;
+      if (ci == INT_MAX) {
+        atomicOr(&s.state->err, kErrAllNaN);
+        next = -1;
+      }
+      if (pos + 1 <= static_cast<uint32_t>(a.max_seq)) s.tokens[pos + 1] = next;
+      s.state->pos = pos + 1;
+      s.state->steps += 1;
+    }
+  }
+  if (t == 0) *a.count = 0u;
+}
+
+// ---------------------------------------------------------------- lm_head
+// One CTA per SM loops over 128-row tiles of the lm_head, 128 K (Q8_0) or
+// 64 K (bf16) per pass ("Eight kernels", lm_head_argmax, as a batched
+// tensor-core contraction).  The operands are f16 here: A = the int8 quants
+// (exact in f16; bf16 weights are stored rounded to f16), B = x (the final
+// RMSNorm output times its gain, bounded) as two f16 parts x1 + x2, which
+// carry x to 2^-22 relative; N = 32.  That halves B against the three bf16
+// parts of the projections and leaves room for deeper pipelines.
+// Warp-specialised:
+//  * warp 12 (one thread) streams whole passes of the tile-pass copy of the
+//    weights (k_tile_head) into kHdStages stages with bulk copies and issues
+//    each pass's MMAs into one of kHdRegions tensor-memory regions;
+//  * warps 4-11, two threads per weight row: convert the row's quants of a
+//    pass into one of kHdABufs A buffers;
+//  * warps 0-3, one thread per row (= tensor-memory lane): read a region out
+//    while the next passes are converted and multiplied, scale the block sums
+//    by the row's f16 block scales, and at a tile's end write the logits and
+//    fold them into running per-sequence argmax candidates.
+// mbarriers hand the passes over: full[stage] (a pass's quants have landed),
+// aready[buf] (an A buffer holds a pass), afree[buf] (its MMAs are done with
+// it), afull[region] (the MMAs into a region are done), tfree[region] (it has
+// been read out).
+constexpr int kHdStages = 4;   // raw stages
+constexpr int kHdABufs = 3;    // A buffers
+constexpr int kHdRegions = 4;  // tensor-memory regions of kTcN * 8 = 128 columns (four blocks of N = 32)
+constexpr uint32_t kHdBBytes = 2 * kBPartBytes;  // one sub-chunk of B: two f16 parts
+constexpr int kHdThreads = 416;  // read-out warps 0-3, dequantising warps 4-11, issuing warp 12
+struct HeadSm {
+  static constexpr uint32_t b = 0;                          // B: 16 sub-chunks of 64 K
+  static constexpr uint32_t a = b + 16 * kHdBBytes;         // A: kHdABufs passes
+  static constexpr uint32_t raw = a + kHdABufs * kAPassBytes;  // raw quants: kHdStages passes
+  static constexpr uint32_t total = raw + kHdStages * kRawBytes;
+};
+static_assert(HeadSm::total + 2048 <= 227 * 1024, "lm_head CTA fits");
+
+__device__ __forceinline__ uint2 ld_weights8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// The lm_head in tile-pass order for the batched step: for every 128-row
+// tile and every pass (128 K of Q8_0, 64 K of bf16) one contiguous
+// kHdPassBytes block: the 128 rows' quants of the pass (128 bytes a row, its
+// 16-byte chunks already in the XOR-swizzled order the dequantisation reads),
+// then the 128 rows' four f16 block scales (1.0 for bf16 weights, whose
+// values are stored as f16, rounded to nearest; zero rows past the end).  One
+// 1-D bulk copy then brings a whole pass.
+constexpr uint32_t kHdScaleOff = kRawBytes;
+constexpr uint32_t kHdPassBytes = kRawBytes + kTcM * 8;
+__global__ void __launch_bounds__(kTcM) k_tile_head(const uint8_t* src, size_t rb, int rows, int K, int fmt,
+                                                   uint8_t* dst) {
+  const bool q8 = fmt == kFmtQ8;
+  const int PK = q8 ? kPassBytes : kPassBytes / 2, npass = (K + PK - 1) / PK;
+  const int tile = static_cast<int>(blockIdx.x) / npass, p = static_cast<int>(blockIdx.x) - tile * npass;
+  const int r = static_cast<int>(threadIdx.x), row = tile * kTcM + r;
+  const int k0 = p * PK, pk = min(PK, K - k0), chunks = (q8 ? pk : 2 * pk) / 16;
+  uint8_t* d = dst + static_cast<size_t>(blockIdx.x) * kHdPassBytes;
+  const uint8_t* s = src + static_cast<size_t>(row < rows ? row : 0) * rb;
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < rows && ch < chunks) v = *reinterpret_cast<const uint4*>(s + (q8 ? k0 : 2 * k0) + 16 * ch);
+    if (!q8) {  // bf16 pairs -> f16 pairs
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+        w[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+    *reinterpret_cast<uint4*>(d + r * kPassBytes + ((ch ^ (r & 7)) << 4)) = v;
+  }
+  uint16_t sc[4];
+  for (int i = 0; i < 4; ++i) {
+    const int blk = k0 / 32 + i;
+    sc[i] = 0;
+    if (row < rows && i < pk / 32) sc[i] = q8 ? *reinterpret_cast<const uint16_t*>(s + K + 2 * blk) : 0x3C00u;
+  }
+  *reinterpret_cast<uint2*>(d + kHdScaleOff + r * 8) =
+      make_uint2(sc[0] | (static_cast<uint32_t>(sc[1]) << 16), sc[2] | (static_cast<uint32_t>(sc[3]) << 16));
+}
+
+__global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
+  constexpr int NT = kHdThreads, NW = NT / 32;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  __shared__ __align__(8) uint64_t aready[kHdABufs], afree[kHdABufs], afull[kHdRegions], tfree[kHdRegions];
+  __shared__ __align__(8) uint64_t full[kHdStages];
+  __shared__ uint32_t tmem_base;
+  __shared__ float inv_rms[kTcN];
+  __shared__ float wred_v[NW][kTcN];
+  __shared__ int wred_i[NW][kTcN];
+  __shared__ float* s_logits[kTcN];
+  __shared__ uint32_t s_last;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, tr = t & (kTcM - 1);
+  const bool loader = t >= kTcM && t < 3 * kTcM, issuer = t == 3 * kTcM;
+  const int hf = (t >> 7) - 1;  // a dequantising thread's half of its row's chunks
+  const bool q8 = a.fmt == kFmtQ8;
+  const int PK = q8 ? kPassBytes : kPassBytes / 2;  // K per pass
+  const int npass = (a.K + PK - 1) / PK;
+  const int tiles = (a.rows + kTcM - 1) / kTcM;
+  const int bx = static_cast<int>(blockIdx.x), gx = static_cast<int>(gridDim.x);
+  const int ntile = bx < tiles ? (tiles - 1 - bx) / gx + 1 : 0;
+  const int total = ntile * npass;  // passes of this CTA
+  auto pass_row0 = [&](int g) { return (bx + (g / npass) * gx) * kTcM; };
+  auto pass_k0 = [&](int g) { return (g % npass) * PK; };
+  // pass g's block of the tile-pass copy (a.W)
+  auto pass_src = [&](int g) {
+    return a.W + (static_cast<size_t>(pass_row0(g) / kTcM) * npass + g % npass) * kHdPassBytes;
+  };
+  // pass g's quants -> stage g % kHdStages, one bulk copy (issued by one thread)
+  auto issue_pass = [&](int g) {
+    if (g >= total) return;
+    uint64_t* bar = &full[g % kHdStages];
+    mbar_arrive_expect_tx(bar, kRawBytes);
+    bulk_g2s(sm + HeadSm::raw + (g % kHdStages) * kRawBytes, pass_src(g), kRawBytes, bar);
+  };
+  // this thread's half of its row of pass g, converted to f16 in A buffer g % kHdABufs
+  auto dequant = [&](int g) {
+    const int pk = min(PK, a.K - pass_k0(g));
+    const unsigned char* raw = sm + HeadSm::raw + (g % kHdStages) * kRawBytes + tr * kPassBytes;
+    unsigned char* A = sm + HeadSm::a + (g % kHdABufs) * kAPassBytes;
+    if (q8) {
+      for (int ch = hf; ch < pk / 16; ch += 2) {
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + ((ch ^ (tr & 7)) << 4));
+        uint32_t o[8];
+        i8x4_to_f16x4(w.x, o[0], o[1]);
+        i8x4_to_f16x4(w.y, o[2], o[3]);
+        i8x4_to_f16x4(w.z, o[4], o[5]);
+        i8x4_to_f16x4(w.w, o[6], o[7]);
+        unsigned char* As = A + (ch >> 2) * kABytes;
+        const int kk = (ch & 3) * 16;
+        *reinterpret_cast<uint4*>(As + core_off16(tr, kk)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(As + core_off16(tr, kk + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    } else {
+      for (int ch = hf; ch < pk / 8; ch += 2)
+        *reinterpret_cast<uint4*>(A + core_off16(tr, ch * 8)) =
+            *reinterpret_cast<const uint4*>(raw + ((ch ^ (tr & 7)) << 4));
+    }
+  };
+  // the four f16 block scales of this thread's row in pass g
+  auto load_sc = [&](int g) {
+    if (g >= total) return make_uint2(0u, 0u);
+    return ld_weights8(pass_src(g) + kHdScaleOff + tr * 8);
+  };
+  if (t == 0) {
+    for (int i = 0; i < kHdABufs; ++i) {
+      mbar_init(&aready[i], 2 * kTcM);
+      mbar_init(&afree[i], 1);
+    }
+    for (int i = 0; i < kHdRegions; ++i) {
+      mbar_init(&afull[i], 1);
+      mbar_init(&tfree[i], kTcM);
+    }
+    for (int i = 0; i < kHdStages; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+  }
+  if (t < kTcN) s_logits[t] = t < a.n ? a.seqs[t].logits : nullptr;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_addr(&tmem_base))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // weights never depend on earlier kernels: the first stages, pass 0's
+  // dequantisation and the first scales happen before the wait
+  __syncthreads();  // the barriers are initialised
+  uint2 sc0 = make_uint2(0u, 0u), sc1 = sc0, sc2 = sc0, sc3 = sc0;
+  bool ok = true;
+  if (issuer) {
+    for (int g = 0; g < kHdStages; ++g) issue_pass(g);
+  } else if (loader) {
+    if (total > 0) {
+      if (!mbar_wait_bounded(&full[0], 0u, a.err)) ok = false;
+      dequant(0);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&aready[0]);
+    }
+  } else if (t < kTcM) {
+    sc0 = load_sc(0);
+    sc1 = load_sc(1);
+    sc2 = load_sc(2);
+    sc3 = load_sc(3);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  // B for all of K: 16 batch rows x K activations times the gain, three bf16
+  // parts per sub-chunk; and the RMSNorm scale of every sequence (warps 0-7)
+  constexpr int RT = 2 * kTcM, RW = RT / 32;
+  if (t < RT) {
+    const float4* ss4 = reinterpret_cast<const float4*>(a.ss);
+    const int n4 = a.gain ? a.nss * (kTcN / 4) : 0;
+    float4 sv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      sv[u] = t + u * RT < n4 ? __ldcg(ss4 + t + u * RT) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int nsubs = (a.K + kSubK - 1) / kSubK;
+    const int b = (t >> 3) & (kTcN - 1), k8 = (t & 7) * 8, hf = t / kTcM;
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f), one4 = make_float4(1.f, 1.f, 1.f, 1.f);
+    for (int s0 = hf; s0 < nsubs; s0 += 8) {  // sub-chunks s0, s0 + 2, s0 + 4, s0 + 6
+      float4 xv[4][2], gv[4][2];
+      bool vld[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int sidx = s0 + 2 * i;
+        vld[i] = sidx < nsubs && b < a.n && k8 < min(kSubK, a.K - sidx * kSubK);
+        const float4* src =
+            reinterpret_cast<const float4*>(a.X + (vld[i] ? static_cast<size_t>(b) * a.ldx + sidx * kSubK + k8 : 0));
+        xv[i][0] = vld[i] ? __ldcg(src) : zero4;
+        xv[i][1] = vld[i] ? __ldcg(src + 1) : zero4;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool gl = a.gain && vld[i];
+        const float4* gp = reinterpret_cast<const float4*>(gl ? a.gain + (s0 + 2 * i) * kSubK + k8 : a.gain);
+        gv[i][0] = gl ? __ldg(gp) : one4;
+        gv[i][1] = gl ? __ldg(gp + 1) : one4;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int sidx = s0 + 2 * i;
+        if (sidx >= nsubs) break;
+        const float x[8] = {xv[i][0].x * gv[i][0].x, xv[i][0].y * gv[i][0].y, xv[i][0].z * gv[i][0].z,
+                            xv[i][0].w * gv[i][0].w, xv[i][1].x * gv[i][1].x, xv[i][1].y * gv[i][1].y,
+                            xv[i][1].z * gv[i][1].z, xv[i][1].w * gv[i][1].w};
+        uint32_t p1[8], p2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split2_f16(x[e], p1[e], p2[e]);
+        unsigned char* B = sm + HeadSm::b + sidx * kHdBBytes + core_off16(b, k8);
+        *reinterpret_cast<uint4*>(B) =
+            make_uint4(p1[0] | (p1[1] << 16), p1[2] | (p1[3] << 16), p1[4] | (p1[5] << 16), p1[6] | (p1[7] << 16));
+        *reinterpret_cast<uint4*>(B + kBPartBytes) =
+            make_uint4(p2[0] | (p2[1] << 16), p2[2] | (p2[3] << 16), p2[4] | (p2[5] << 16), p2[6] | (p2[7] << 16));
+      }
+    }
+    for (int i = t + 4 * RT; i < n4; i += RT) {
+      const float4 v = __ldcg(ss4 + i);
+      sv[0].x += v.x; sv[0].y += v.y; sv[0].z += v.z; sv[0].w += v.w;
+    }
+    float s4[4] = {(sv[0].x + sv[1].x) + (sv[2].x + sv[3].x), (sv[0].y + sv[1].y) + (sv[2].y + sv[3].y),
+                   (sv[0].z + sv[1].z) + (sv[2].z + sv[3].z), (sv[0].w + sv[1].w) + (sv[2].w + sv[3].w)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s4[e] += __shfl_xor_sync(0xFFFFFFFFu, s4[e], 4);
+      s4[e] += __shfl_xor_sync(0xFFFFFFFFu, s4[e], 8);
+      s4[e] += __shfl_xor_sync(0xFFFFFFFFu, s4[e], 16);
+    }
+    if (lane < 4) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) wred_v[warp][4 * lane + e] = s4[e];
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // B and A buffer 0, for the MMAs
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (t < kTcN) {
+    float ss = 0.f;
+    for (int w = 0; w < RW; ++w) ss += wred_v[w][t];
+    inv_rms[t] = a.gain ? rsqrtf(ss / static_cast<float>(a.K) + a.eps) : 1.f;
+  }
+  __syncthreads();
+  const uint32_t dt = tmem_base;
+  if (loader) {
+    for (int g = 1; g < total; ++g) {
+      if (!mbar_wait_bounded(&full[g % kHdStages], (g / kHdStages) & 1u, a.err)) ok = false;
+      // the MMAs of pass g - kHdABufs have read this pass's A buffer
+      if (g >= kHdABufs && !mbar_wait_bounded(&afree[g % kHdABufs], ((g - kHdABufs) / kHdABufs) & 1u, a.err))
+        ok = false;
+      dequant(g);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&aready[g % kHdABufs]);
+    }
+  } else if (issuer) {
+    const uint64_t dA0 = smem_desc(sm + HeadSm::a, 128, (kSubK / 8) * 128);
+    const uint64_t dB0 = smem_desc(sm + HeadSm::b, 128, (kSubK / 8) * 128);
+    for (int g = 0; g < total; ++g) {
+      // every row of pass g is in its A buffer, so its stage is free
+      if (!mbar_wait_bounded(&aready[g % kHdABufs], (g / kHdABufs) & 1u, a.err)) ok = false;
+      issue_pass(g + kHdStages);
+      // the pass's tensor-memory region has been read out (pass g - kHdRegions)
+      if (g >= kHdRegions && !mbar_wait_bounded(&tfree[g % kHdRegions], ((g - kHdRegions) / kHdRegions) & 1u, a.err))
+        ok = false;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int k0 = pass_k0(g), nb = min(PK, a.K - k0) / 32;
+      mma_pass<true>(dt + (g % kHdRegions) * (4 * kHdN), kHdN,
+                     dA0 + (((g % kHdABufs) * kAPassBytes) >> 4), dB0 + (((k0 / kSubK) * kHdBBytes) >> 4), kHdBBytes,
+                     nb);
+      mma_commit(&afull[g % kHdRegions]);
+      mma_commit(&afree[g % kHdABufs]);
+    }
+  } else if (t < kTcM) {
+    float acc[kTcN], bv[kTcN];
+    int bi[kTcN];
+#pragma unroll
+    for (int b = 0; b < kTcN; ++b) {
+      acc[b] = 0.f;
+      bv[b] = -INFINITY;
+      bi[b] = INT_MAX;
+    }
+    const uint32_t lane_addr = dt + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    for (int g = 0; g < total; ++g) {
+      const int h = g % kHdRegions, nb = min(PK, a.K - pass_k0(g)) / 32;
+      if (!mbar_wait_bounded(&afull[h], (g / kHdRegions) & 1u, a.err)) ok = false;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const float s[4] = {__half2float(__ushort_as_half(static_cast<uint16_t>(sc0.x & 0xFFFFu))),
+                          __half2float(__ushort_as_half(static_cast<uint16_t>(sc0.x >> 16))),
+                          __half2float(__ushort_as_half(static_cast<uint16_t>(sc0.y & 0xFFFFu))),
+                          __half2float(__ushort_as_half(static_cast<uint16_t>(sc0.y >> 16)))};
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        if (blk >= nb) break;
+        uint32_t r0[16], r1[16];  // the block's two parts
+        tmem_ld16(lane_addr + h * (4 * kHdN) + blk * kHdN, r0);
+        tmem_ld16(lane_addr + h * (4 * kHdN) + blk * kHdN + kTcN, r1);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int b = 0; b < kTcN; ++b)
+          acc[b] = fmaf(s[blk], __uint_as_float(r0[b]) + __uint_as_float(r1[b]), acc[b]);
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(&tfree[h]);
+      sc0 = sc1;
+      sc1 = sc2;
+      sc2 = sc3;
+      sc3 = load_sc(g + 4);
+      if (g % npass == npass - 1) {  // the tile's logits, into the running candidates
+        const int row = pass_row0(g) + tr;
+#pragma unroll
+        for (int b = 0; b < kTcN; ++b) {
+          const float val = acc[b] * inv_rms[b];
+          acc[b] = 0.f;
+          if (b < a.n && row < a.rows) {
+            s_logits[b][row] = val;
+            argmax_merge(bv[b], bi[b], val, row);
+          }
+        }
+      }
+    }
+    // this CTA's candidate per sequence
+#pragma unroll
+    for (int b = 0; b < kTcN; ++b) {
+      warp_argmax(bv[b], bi[b]);
+      if (lane == 0) {
+        wred_v[warp][b] = bv[b];
+        wred_i[warp][b] = bi[b];
+      }
+    }
+    named_sync(2, kTcM);
+    if (t < a.n) {
+      float cv = -INFINITY;
+      int ci = INT_MAX;
+      for (int w = 0; w < kTcM / 32; ++w) argmax_merge(cv, ci, wred_v[w][t], wred_i[w][t]);
+      a.seqs[t].amax_v[bx] = cv;
+      a.seqs[t].amax_i[bx] = ci;
+    }
+  }
+  (void)ok;  // a timed-out wait has set the error word; the host reports it
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {  // every MMA has completed (its half was read out) and every read-out is done
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(dt) : "memory");
+  }
+  // the last CTA to arrive picks every sequence's winner
+  if (t == 0) {
+    __threadfence();
+    const uint32_t old = atomicAdd(a.count, 1u);
+    s_last = old == gridDim.x - 1u;
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
   for (int q = warp; q < a.n; q += NW) {
     const DevSeq& s = a.seqs[q];
     float cv = -INFINITY;
@@ -1104,6 +1562,19 @@ size_t attn_batch_smem(const DevModel& m) {
 
 int batch_max() { return kTcN; }
 
+size_t batch_head_bytes(int rows, int K, int fmt) {
+  const int PK = fmt == kFmtQ8 ? kPassBytes : kPassBytes / 2;
+  return static_cast<size_t>((rows + kTcM - 1) / kTcM) * ((K + PK - 1) / PK) * kHdPassBytes;
+}
+
+cudaError_t launch_head_tile(const uint8_t* rows_src, size_t rb, int rows, int K, int fmt, uint8_t* dst,
+                             cudaStream_t st) {
+  const int PK = fmt == kFmtQ8 ? kPassBytes : kPassBytes / 2;
+  const int blocks = ((rows + kTcM - 1) / kTcM) * ((K + PK - 1) / PK);
+  k_tile_head<<<blocks, kTcM, 0, st>>>(rows_src, rb, rows, K, fmt, dst);
+  return cudaGetLastError();
+}
+
 int batch_ss_slots(int H) { return ((H + kTcM - 1) / kTcM) * kMaxCluster; }
 
 bool batch_supported(const DevModel& m) {
@@ -1121,8 +1592,8 @@ cudaError_t batch_setup(const DevModel& m) {
   e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<SplitCfg>),
                            cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<HeadCfg>),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(HeadCfg::total));
+  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_head16), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(HeadSm::total));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(attn_batch_fn(m), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(attn_batch_smem(m)));
@@ -1134,9 +1605,9 @@ cudaError_t batch_setup(const DevModel& m) {
 // [slots][16]).  Every kernel is launched with programmatic dependent launch:
 // it starts streaming its weights (or cached K/V rows) while its predecessor
 // finishes, and waits for it before touching activations.
-cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const DevSeq* seqs,
-                               int n, int nch, float* X, float* QKV, float* PO, float* PML, float* H, float* SS,
-                               uint32_t* count, uint32_t* err, cudaStream_t st) {
+cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const uint8_t* lm_tiled,
+                               const DevSeq* seqs, int n, int nch, float* X, float* QKV, float* PO, float* PML,
+                               float* H, float* SS, uint32_t* count, uint32_t* err, cudaStream_t st) {
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1187,8 +1658,8 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
       cudaLaunchConfig_t c = config(tiles * a.cs, SplitCfg::threads, SplitCfg::total, a.cs);
       return cudaLaunchKernelEx(&c, k_mm16<SplitCfg>, a);
     }
-    cudaLaunchConfig_t c = config(std::min(tiles, num_sms), HeadCfg::threads, HeadCfg::total, 1);
-    return cudaLaunchKernelEx(&c, k_mm16<HeadCfg>, a);
+    cudaLaunchConfig_t c = config(std::min(tiles, num_sms), kHdThreads, HeadSm::total, 1);
+    return cudaLaunchKernelEx(&c, k_head16, a);
   };
   const int lqkv = m.qw + 2 * m.kvw;
   const void* attn_fn = attn_batch_fn(m);
@@ -1218,7 +1689,7 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
         cudaSuccess)
       return e;
   }
-  return mm(m.lm_head, m.row_bytes_h, m.H, m.V, X, m.H, m.out_norm, ss_x, nss_x, kEpiArgmax, nullptr, 0,
+  return mm(lm_tiled, m.row_bytes_h, m.H, m.V, X, m.H, m.out_norm, ss_x, nss_x, kEpiArgmax, nullptr, 0,
             nullptr, false);
 }
 

@@ -74,6 +74,7 @@ struct tqd_model {
   DevSeq* dseqs = nullptr;
   uint32_t* bcount = nullptr;
   float* bss = nullptr;
+  uint8_t* blm = nullptr;  // the lm_head in the batched step's tile-pass order
   int batch_nch = 1;
   cudaGraphExec_t bgraph[17] = {};
 };
@@ -461,7 +462,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   }
   // batched-step buffers (only for models holding several sequences)
   const int bmax = batch_max();
-  size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0;
+  size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0, o_blm = 0;
   if (cfg->max_batch > 1) {
     o_bx = take(4ull * bmax * H);
     o_bqkv = take(4ull * bmax * (qw + 2 * kvw));
@@ -471,6 +472,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);
     o_bcount = take(4);
     o_bss = take(4ull * 2 * batch_ss_slots(H) * bmax);
+    o_blm = take(batch_head_bytes(V, H, fmt));
   }
   m->arena_bytes = off;
   cudaError_t ce = cudaMalloc(&m->arena, m->arena_bytes);
@@ -592,6 +594,12 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     if (tmp) cudaFree(tmp);
     return fail(e, "upload head weights");
   }
+  if (cfg->max_batch > 1 &&
+      ((e = launch_head_tile(base + o_lm, rbh, V, H, fmt, base + o_blm, st)) != cudaSuccess ||
+       (e = cudaStreamSynchronize(st)) != cudaSuccess)) {
+    if (tmp) cudaFree(tmp);
+    return fail(e, "tile the lm_head");
+  }
   if (tmp) cudaFree(tmp);
   m->host_layers = dl;
   if (w->embed) wbytes -= static_cast<int64_t>(row_bytes(wt, H)) * V;  // one row per step
@@ -642,6 +650,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
     m->bcount = reinterpret_cast<uint32_t*>(base + o_bcount);
     m->bss = reinterpret_cast<float*>(base + o_bss);
+    m->blm = base + o_blm;
     std::vector<DevSeq> hs(cfg->max_batch);
     for (int b = 0; b < cfg->max_batch; ++b) hs[b] = m->seqs[b].d;
     if ((e = cudaMemcpy(m->dseqs, hs.data(), sizeof(DevSeq) * cfg->max_batch,
@@ -860,7 +869,7 @@ int32_t run_batch(tqd_model* m, int n, int steps) {
     m->batch_nch = nch;
     cudaGraph_t graph = nullptr;
     CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
-    cudaError_t e = enqueue_batch_step(m->dm, m->host_layers.data(), m->dseqs, n, nch, m->bx, m->bqkv,
+    cudaError_t e = enqueue_batch_step(m->dm, m->host_layers.data(), m->blm, m->dseqs, n, nch, m->bx, m->bqkv,
                                        m->bpo, m->bpml, m->bh, m->bss, m->bcount, &m->seqs[0].d.state->err,
                                        m->stream);
     cudaError_t e2 = cudaStreamEndCapture(m->stream, &graph);

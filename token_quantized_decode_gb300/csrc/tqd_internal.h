@@ -100,10 +100,15 @@ int batch_max();
 int batch_ss_slots(int H);  // partial sums of squares per activation ([slots][batch_max()])
 bool batch_supported(const DevModel& m);
 cudaError_t batch_setup(const DevModel& m);
+// The lm_head in the tile-pass order the batched step streams: its size, and
+// the kernel that writes it from the row layout.
+size_t batch_head_bytes(int rows, int K, int fmt);
+cudaError_t launch_head_tile(const uint8_t* rows_src, size_t rb, int rows, int K, int fmt, uint8_t* dst,
+                             cudaStream_t st);
 // PO / PML: the attention's chunk partials, [n][nq][nch][hd] and [n][nq][nch][2].
-cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const DevSeq* seqs,
-                               int n, int nch, float* X, float* QKV, float* PO, float* PML, float* H, float* SS,
-                               uint32_t* count, uint32_t* err, cudaStream_t st);
+cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const uint8_t* lm_tiled,
+                               const DevSeq* seqs, int n, int nch, float* X, float* QKV, float* PO, float* PML,
+                               float* H, float* SS, uint32_t* count, uint32_t* err, cudaStream_t st);
 
 // Record the text tqd_last_error() returns on this thread.
 void set_last_error(const char* msg);
