@@ -1226,25 +1226,30 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
 // K is whole 32-wide blocks (ceil(blocks / cs) at most), which must fit the
 // CTA's B buffer.  Each 128-K pass of a CTA's share adds a dependent
 // dequantise / MMA / read-out round after the activations arrive, so the
-// fewest passes win; among those, the smallest cluster (the fewest CTAs, so
-// the next kernel's CTAs find room to start early) whose CTAs all fit one
-// wave at two CTAs per SM.  0 if no size fits.
+// fewest passes win.  Among those: if some sizes keep the launch at one CTA
+// per SM (the next kernel's CTAs then find room to start early), the largest
+// of them (the shortest last pass); otherwise the smallest size (the fewest
+// CTAs) that still fits one wave at two CTAs per SM.  0 if no size fits.
 int mm_cluster(int K, int rows, int num_sms) {
   const int tiles = (rows + kTcM - 1) / kTcM, nbk = K / 32;
   if (K % 32 != 0) return 0;
-  int best = 0, best_passes = 0, fallback = 0;
-  for (int c = 1; c <= kMaxCluster && c <= nbk; ++c) {
+  int fallback = 0, best_passes = 0;
+  for (int c = 1; c <= kMaxCluster && c <= nbk; ++c) {  // the fewest passes within one wave
     const int kr = 32 * ((nbk + c - 1) / c);
     if (kr > kSplitMaxK) continue;
     if (!fallback) fallback = c;
     const int passes = (kr + kPassBytes - 1) / kPassBytes;
-    if (tiles * c > 2 * num_sms) continue;
-    if (!best || passes < best_passes) {
-      best = c;
-      best_passes = passes;
-    }
+    if (tiles * c <= 2 * num_sms && (!best_passes || passes < best_passes)) best_passes = passes;
   }
-  return best ? best : fallback;
+  if (!best_passes) return fallback;
+  int one_per_sm = 0, smallest = 0;
+  for (int c = 1; c <= kMaxCluster && c <= nbk; ++c) {
+    const int kr = 32 * ((nbk + c - 1) / c);
+    if (kr > kSplitMaxK || (kr + kPassBytes - 1) / kPassBytes != best_passes || tiles * c > 2 * num_sms) continue;
+    if (!smallest) smallest = c;
+    if (tiles * c <= num_sms) one_per_sm = c;
+  }
+  return one_per_sm ? one_per_sm : smallest;
 }
 
 // ---------------------------------------------------------------- embedding
