@@ -51,27 +51,21 @@ constexpr int kMaxCluster = 16;       // 16 is a non-portable cluster size (allo
 __host__ __device__ constexpr int pair_row0(int q, int cs) { return 2 * ((q * (kTcM / 2)) / cs); }
 __host__ __device__ constexpr int recv_stride(int cs) { return 2 * ((kTcM / 2 + cs - 1) / cs); }
 constexpr int kRecvRows = 160;       // >= cs * recv_stride(cs) for every cs <= 16
-constexpr uint32_t kPassCols = 4 * kTcN3;            // tensor-memory columns of one pass (four blocks)
-// Split projections (one tile per CTA, two CTAs per SM): B for up to 384
-// columns, one pass of A and of tensor memory at a time.  lm_head (one CTA
-// per SM looping over tiles): B for all of H <= 1024, deeper weight
-// staging, and double-buffered A and tensor memory so one pass's read-out
-// overlaps the next pass's MMAs.
-template <int STAGES, int MAXSUB, bool DBL, int NH, int RROWS>
+// Shared memory of a split projection CTA (one tile, two CTAs per SM): raw
+// weight stages, one pass of A, B for up to MAXSUB sub-chunks (384 K), and
+// the partial sums received from the cluster ranks.
+template <int STAGES, int MAXSUB>
 struct MmCfg {
-  static constexpr int nh = NH;                  // threads per weight row (each a share of every pass)
-  static constexpr int threads = kMmThreads * NH;
+  static constexpr int threads = kMmThreads;
   static constexpr uint32_t a = STAGES * kRawBytes;
-  static constexpr uint32_t b = a + (DBL ? 2 : 1) * kAPassBytes;
+  static constexpr uint32_t b = a + kAPassBytes;
   static constexpr uint32_t recv = b + MAXSUB * kBBytes;
-  static constexpr uint32_t total = recv + NH * RROWS * kTcN * 4;  // [rank][row][16] partials received
-  static constexpr uint32_t tmem = DBL ? 512 : 256;
+  static constexpr uint32_t total = recv + kRecvRows * kTcN * 4;  // [rank][row][16] partials received
+  static constexpr uint32_t tmem = 256;                          // one pass: four blocks of 48 columns
 };
-using SplitCfg = MmCfg<2, 6, false, 1, kRecvRows>;  // clusters of up to 16
-using HeadCfg = MmCfg<3, 16, true, 2, kTcM>;        // no cluster
+using SplitCfg = MmCfg<2, 6>;
 static_assert(2 * (SplitCfg::total + 2048) <= 228 * 1024, "two split CTAs per SM");
-static_assert(HeadCfg::total + 1024 <= 227 * 1024, "lm_head CTA fits");
-constexpr int kSplitMaxK = 6 * kSubK, kHeadMaxK = 16 * kSubK;
+constexpr int kSplitMaxK = 6 * kSubK, kHeadMaxK = 16 * kSubK;  // K of a split rank, of the lm_head
 
 // Shared-memory matrix descriptor, K-major without swizzle: core matrices of
 // 8 rows x 16 bytes; lbo = byte step between core matrices along K, sbo =
@@ -276,27 +270,21 @@ struct MmArgs {
   int nch, hd;
 };
 
-// Thread t of the CTA works on weight row t % 128 of the current tile (tensor
-// memory lane t % 128): with NH threads per row, thread t takes the share
-// t / 128 of every pass's dequantisation and read-out.  Projections split over
-// a cluster run one tile per CTA; the lm_head (cs == 1) runs one CTA per SM
-// over tiles blockIdx.x, blockIdx.x + gridDim.x, ..., reading out one pass
-// while the next pass's MMAs run.
+// Thread t of the CTA works on weight row t of its tile (tensor-memory lane
+// t); the cluster's ranks split the tile's K, and each rank owns a range of
+// the tile's row pairs for the reduction and the epilogue.
 template <class CFG>
 __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
-  constexpr bool DBL = CFG::tmem == 512;
   constexpr int STAGES = CFG::a / kRawBytes;
-  constexpr int NH = CFG::nh, NT = CFG::threads, NW = NT / 32;
+  constexpr int NT = CFG::threads, NW = NT / 32;
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ __align__(8) uint64_t bars[2];  // a pass's MMAs are complete (by pass parity)
   __shared__ __align__(8) uint64_t rbar;     // every cluster rank's partials of this CTA's rows have landed
   __shared__ uint32_t tmem_base;
   __shared__ float inv_rms[kTcN];
   __shared__ float wred_v[NW][kTcN];
-  __shared__ int wred_i[NW][kTcN];
-  __shared__ uint32_t s_last;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int tr = t & (kTcM - 1), hf = t / kTcM;  // weight row of the tile, share of the row
+  const int tr = t;  // the weight row of the tile
   const int rank = static_cast<int>(cluster_rank());
   const bool q8 = a.fmt == kFmtQ8;
   // this rank's K range: whole 32-wide blocks, split as evenly as the cluster size allows
@@ -304,16 +292,12 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   const int kc0 = 32 * ((rank * nbk) / a.cs), KR = 32 * (((rank + 1) * nbk) / a.cs) - kc0;
   const int PK = q8 ? kPassBytes : kPassBytes / 2;  // K per pass
   const int npass = (KR + PK - 1) / PK;
-  const int tiles = (a.rows + kTcM - 1) / kTcM;
-  const int tile0 = a.cs > 1 ? static_cast<int>(blockIdx.x) / a.cs : static_cast<int>(blockIdx.x);
-  const int tstride = a.cs > 1 ? tiles : static_cast<int>(gridDim.x);
-  const int ntile = tile0 < tiles ? (tiles - 1 - tile0) / tstride + 1 : 0;
-  const int total = ntile * npass;  // passes of this CTA, over all its tiles
-  auto pass_tile = [&](int g) { return tile0 + (g / npass) * tstride; };
+  const int tile = static_cast<int>(blockIdx.x) / a.cs;  // the cluster's tile
+  const int total = npass;                               // passes of this CTA
   // weight quants of pass g for all 128 rows -> raw stage g % STAGES
   auto issue_raw = [&](int g) {
-    const int row0 = pass_tile(g) * kTcM;
-    const int k0 = kc0 + (g % npass) * PK, pk = min(PK, kc0 + KR - k0);
+    const int row0 = tile * kTcM;
+    const int k0 = kc0 + g * PK, pk = min(PK, kc0 + KR - k0);
     const int chunks = (q8 ? pk : 2 * pk) / 16;
     unsigned char* dst = sm + (g % STAGES) * kRawBytes;
     for (int c = t; c < kTcM * 8; c += NT) {
@@ -328,19 +312,19 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   };
   // f16 scale bits of this thread's row for the blocks of pass g
   auto load_scales = [&](int g, uint16_t (&sb)[4]) {
-    const int row = pass_tile(g) * kTcM + tr;
-    const int k0 = kc0 + (g % npass) * PK, nblk = min(PK, kc0 + KR - k0) / 32;
+    const int row = tile * kTcM + tr;
+    const int k0 = kc0 + g * PK, nblk = min(PK, kc0 + KR - k0) / 32;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       sb[i] = (q8 && g < total && row < a.rows && i < nblk)
                   ? ld_weights_u16(a.W + static_cast<size_t>(row) * a.rb + a.K + 2 * (k0 / 32 + i))
                   : static_cast<uint16_t>(0);
   };
-  // split-K over a cluster (one tile per CTA): every rank sends its partial
-  // sums of the rows rank q owns straight into q's shared memory with st.async,
-  // and q waits on rbar for all of them (no cluster-wide barrier after the
-  // MMAs); rows [own0, own0 + own) of the tile are this rank's
-  const bool push = a.cs > 1 && NH == 1;
+  // split-K over a cluster: every rank sends its partial sums of the rows
+  // rank q owns straight into q's shared memory with st.async, and q waits on
+  // rbar for all of them (no cluster-wide barrier after the MMAs); rows
+  // [own0, own0 + own) of the tile are this rank's
+  const bool push = a.cs > 1;
   const int own0 = pair_row0(rank, a.cs), own = pair_row0(rank + 1, a.cs) - own0;
   if (t == 0) {
     mbar_init(&bars[0], 1);
@@ -379,8 +363,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   for (int b = 0; b < kTcN; ++b) acc[b] = 0.f;
   bool ok = true;
   const int b_ep = t & (kTcN - 1);  // the sequence this thread's epilogue items belong to
-  float ssum = 0.f, bv = -INFINITY;
-  int bi = INT_MAX;
+  float ssum = 0.f;
   float* recv = reinterpret_cast<float*>(sm + CFG::recv);
   // kEpiResid: the residual of this thread's first epilogue item, loaded with
   // the activations (one round trip) instead of after the reduction
@@ -394,13 +377,12 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
     if (odd) ph1 ^= 1u;
     else ph0 ^= 1u;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t base = lane_addr + (DBL && odd ? 256 : 0);
     const int nbq = odd ? nb1 : nb0;
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk) {
-      if (blk % NH != hf || blk >= nbq) continue;
+      if (blk >= nbq) break;
       float v[16];
-      tmem_block_sum(base + blk * kTcN3, v);
+      tmem_block_sum(lane_addr + blk * kTcN3, v);
       const float scale = odd ? sc1[blk] : sc0[blk];
 #pragma unroll
       for (int b = 0; b < kTcN; ++b) acc[b] = fmaf(scale, v[b], acc[b]);
@@ -411,12 +393,12 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   // the rows another CTA owns into that CTA's shared memory) and apply the
   // epilogue; thread t handles row pairs (2m, 2m+1) of the rows this CTA owns
   // for sequence t % 16, summing the partials in rank order
-  auto epilogue = [&](int tile, bool more) {
+  auto epilogue = [&]() {
     const int rs = recv_stride(a.cs), row0 = tile * kTcM;
     {
       const int q = ((tr / 2 + 1) * a.cs - 1) / (kTcM / 2);  // the rank that owns row tr
       const int lr = tr - pair_row0(q, a.cs);
-      const uint32_t dst = mapa_u32(recv + ((rank * NH + hf) * rs + lr) * kTcN, static_cast<uint32_t>(q));
+      const uint32_t dst = mapa_u32(recv + (rank * rs + lr) * kTcN, static_cast<uint32_t>(q));
       if (push) {
         const uint32_t qbar = mapa_u32(&rbar, static_cast<uint32_t>(q));
 #pragma unroll
@@ -439,7 +421,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
     for (int idx = t; idx < own * (kTcN / 2); idx += NT) {
       const int lr = 2 * (idx / kTcN);
       float v0 = 0.f, v1 = 0.f;
-      for (int q = 0; q < a.cs * NH; ++q) {
+      for (int q = 0; q < a.cs; ++q) {
         v0 += recv[(q * rs + lr) * kTcN + b_ep];
         v1 += recv[(q * rs + lr + 1) * kTcN + b_ep];
       }
@@ -450,14 +432,6 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
       const bool ok1 = r1 < a.rows;
       if (a.epi == kEpiSwiGLU) {
         a.Y[static_cast<size_t>(b_ep) * a.ldy + (r0 >> 1)] = silu_mul(v0, v1);
-      } else if (a.epi == kEpiArgmax) {
-        float* lg = a.seqs[b_ep].logits;
-        lg[r0] = v0;
-        argmax_merge(bv, bi, v0, r0);
-        if (ok1) {
-          lg[r1] = v1;
-          argmax_merge(bv, bi, v1, r1);
-        }
       } else {
         float* y = a.Y + static_cast<size_t>(b_ep) * a.ldy;
         if (a.epi == kEpiResid) {
@@ -471,13 +445,12 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
         if (ok1) y[r1] = v1;
       }
     }
-    if (more) cluster_sync();  // this tile's partials are read before the next tile's arrive
   };
   // wait for pass g's weights and dequantise them into A (this thread's row,
   // both sub-chunks); with one A / tensor-memory buffer the previous pass is
   // read out first
   auto load_pass = [&](int g) {
-    const int k0 = kc0 + (g % npass) * PK, pk = min(PK, kc0 + KR - k0);
+    const int k0 = kc0 + g * PK, pk = min(PK, kc0 + KR - k0);
     if (g & 1) {
       nb1 = pk / 32;
 #pragma unroll
@@ -495,14 +468,11 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
     else cp_async_commit();
     cp_async_wait<STAGES - 1>();
     __syncthreads();
-    if (!DBL && g > 0) {
-      readout(g - 1);
-      if ((g - 1) % npass == npass - 1) epilogue(pass_tile(g - 1), true);
-    }
+    if (g > 0) readout(g - 1);
     const unsigned char* raw = sm + (g % STAGES) * kRawBytes + tr * kPassBytes;
-    unsigned char* A = sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
+    unsigned char* A = sm + CFG::a;
     if (q8) {
-      for (int ch = hf; ch < pk / 16; ch += NH) {
+      for (int ch = 0; ch < pk / 16; ++ch) {
         const uint4 w = *reinterpret_cast<const uint4*>(raw + ((ch ^ (tr & 7)) << 4));
         uint32_t o[8];
         i8x4_to_bf16x4(w.x, o[0], o[1]);
@@ -515,7 +485,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
         *reinterpret_cast<uint4*>(As + core_off16(tr, kk + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     } else {
-      for (int ch = hf; ch < pk / 8; ch += NH)
+      for (int ch = 0; ch < pk / 8; ++ch)
         *reinterpret_cast<uint4*>(A + core_off16(tr, ch * 8)) =
             *reinterpret_cast<const uint4*>(raw + ((ch ^ (tr & 7)) << 4));
     }
@@ -523,8 +493,8 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   // a CTA with two passes of one tile dequantises its second pass before the
   // wait too: that pass's quants are read from raw stage 1 into registers, and
   // after a barrier its bf16 A is written over both raw stages (A's size)
-  const bool pre2 = !DBL && STAGES == 2 && NH == 1 && ntile == 1 && npass == 2;
-  static_assert(DBL || CFG::a >= kAPassBytes || STAGES != 2, "pass-1 A fits the raw stages");
+  const bool pre2 = STAGES == 2 && npass == 2;
+  static_assert(CFG::a >= kAPassBytes || STAGES != 2, "pass-1 A fits the raw stages");
   auto prep_pass1 = [&]() {
     const int k0 = kc0 + PK, pk = min(PK, kc0 + KR - k0);
     nb1 = pk / 32;
@@ -577,9 +547,9 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
     for (int u = 0; u < 4; ++u)
       sv[u] = t + u * NT < n4 ? __ldcg(ss4 + t + u * NT) : make_float4(0.f, 0.f, 0.f, 0.f);
     const int nsubs = (KR + kSubK - 1) / kSubK;
-    const bool parts = !DBL && a.part_o != nullptr;  // the split projections only
-    if (a.epi == kEpiResid && ntile == 1 && t < own * (kTcN / 2)) {
-      const int r0 = tile0 * kTcM + own0 + 2 * (t / kTcN);
+    const bool parts = a.part_o != nullptr;
+    if (a.epi == kEpiResid && t < own * (kTcN / 2)) {
+      const int r0 = tile * kTcM + own0 + 2 * (t / kTcN);
       if (b_ep < a.n && r0 < a.rows) {
         const float* y = a.Y + static_cast<size_t>(b_ep) * a.ldy;
         res0 = __ldcg(y + r0);
@@ -588,15 +558,14 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
       }
     }
     const int b = (t >> 3) & (kTcN - 1), k8 = (t & 7) * 8;
-    // thread share hf builds sub-chunks hf, hf + NH, ...
-    for (int s0 = hf; s0 < nsubs; s0 += 4 * NH) {
+    for (int s0 = 0; s0 < nsubs; s0 += 4) {  // sub-chunks s0 .. s0 + 3
       // every load of the round first (activations, gains), arithmetic after
       float4 xv[4][2], gv[4][2];
       bool vld[4];
       const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f), one4 = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int sidx = s0 + i * NH;
+        const int sidx = s0 + i;
         vld[i] = sidx < nsubs && b < a.n && k8 < min(kSubK, KR - sidx * kSubK);
         if (parts) continue;
         const float4* src = reinterpret_cast<const float4*>(
@@ -614,7 +583,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
         int dd[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int k = kc0 + (s0 + i * NH) * kSubK + k8, h = k / a.hd;
+          const int k = kc0 + (s0 + i) * kSubK + k8, h = k / a.hd;
           dd[i] = k - h * a.hd;
           base[i] = (static_cast<size_t>(b) * (a.K / a.hd) + h) * a.nch;
           M[i] = -INFINITY;
@@ -669,7 +638,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const bool gl = a.gain && vld[i];
-        const float4* gp = reinterpret_cast<const float4*>(gl ? a.gain + kc0 + (s0 + i * NH) * kSubK + k8 : a.gain);
+        const float4* gp = reinterpret_cast<const float4*>(gl ? a.gain + kc0 + (s0 + i) * kSubK + k8 : a.gain);
         gv[i][0] = gl ? __ldg(gp) : one4;
         gv[i][1] = gl ? __ldg(gp + 1) : one4;
       }
@@ -680,7 +649,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int sidx = s0 + i * NH;
+        const int sidx = s0 + i;
         if (sidx >= nsubs) break;
         const float x[8] = {xv[i][0].x, xv[i][0].y, xv[i][0].z, xv[i][0].w,
                             xv[i][1].x, xv[i][1].y, xv[i][1].z, xv[i][1].w};
@@ -736,23 +705,15 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
     __syncthreads();
     if (t == 0) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int k0 = kc0 + (g % npass) * PK;
-      unsigned char* A = pre2 && g == 1 ? sm : sm + CFG::a + (DBL ? (g & 1) : 0) * kAPassBytes;
-      const unsigned char* Bp = sm + CFG::b + ((k0 - kc0) / kSubK) * kBBytes;
-      const uint32_t col0 = DBL ? (g & 1) * 256 : 0;
-      mma_pass<false>(dt + col0, kTcN3, smem_desc(A, 128, (kSubK / 8) * 128), smem_desc(Bp, 128, (kSubK / 8) * 128),
+      unsigned char* A = pre2 && g == 1 ? sm : sm + CFG::a;
+      const unsigned char* Bp = sm + CFG::b + (g * PK / kSubK) * kBBytes;
+      mma_pass<false>(dt, kTcN3, smem_desc(A, 128, (kSubK / 8) * 128), smem_desc(Bp, 128, (kSubK / 8) * 128),
                       kBBytes, (g & 1) ? nb1 : nb0);
       mma_commit(&bars[g & 1]);
     }
-    if (DBL && g > 0) {
-      readout(g - 1);
-      if ((g - 1) % npass == npass - 1) epilogue(pass_tile(g - 1), true);
-    }
   }
-  if (total > 0) {
-    readout(total - 1);
-    epilogue(pass_tile(total - 1), false);
-  }
+  if (total > 0) readout(total - 1);
+  epilogue();  // every rank takes part in the cluster's reduction
   cp_async_wait<0>();
   __syncthreads();
   if (warp == 0) {  // the tensor memory is released on every path
@@ -771,56 +732,6 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
     }
     return;
   }
-  if (a.epi != kEpiArgmax) return;
-  // lm_head: this block's candidate per sequence, then the last block to
-  // arrive picks every sequence's winner
-  {
-    const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, 16);
-    const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, 16);
-    argmax_merge(bv, bi, ov, oi);
-    if (lane < kTcN) {
-      wred_v[warp][lane] = bv;
-      wred_i[warp][lane] = bi;
-    }
-  }
-  __syncthreads();
-  if (t < a.n) {
-    float cv = -INFINITY;
-    int ci = INT_MAX;
-    for (int w = 0; w < NW; ++w) argmax_merge(cv, ci, wred_v[w][t], wred_i[w][t]);
-    a.seqs[t].amax_v[blockIdx.x] = cv;
-    a.seqs[t].amax_i[blockIdx.x] = ci;
-  }
-  __syncthreads();
-  if (t == 0) {
-    __threadfence();
-    const uint32_t old = atomicAdd(a.count, 1u);
-    s_last = old == gridDim.x - 1u;
-    if (s_last) __threadfence();
-  }
-  __syncthreads();
-  if (!s_last) return;
-  // one warp per sequence reduces the blocks' candidates
-  for (int q = warp; q < a.n; q += NW) {
-    const DevSeq& s = a.seqs[q];
-    float cv = -INFINITY;
-    int ci = INT_MAX;
-    for (int k = lane; k < static_cast<int>(gridDim.x); k += 32)
-      argmax_merge(cv, ci, __ldcg(s.amax_v + k), __ldcg(s.amax_i + k));
-    warp_argmax(cv, ci);
-    if (lane == 0) {
-      const uint32_t pos = s.state->pos;
-      int next = ci;
-      if (ci == INT_MAX) {
-        atomicOr(&s.state->err, kErrAllNaN);
-        next = -1;
-      }
-      if (pos + 1 <= static_cast<uint32_t>(a.max_seq)) s.tokens[pos + 1] = next;
-      s.state->pos = pos + 1;
-      s.state->steps += 1;
-    }
-  }
-  if (t == 0) *a.count = 0u;
 }
 
 // ---------------------------------------------------------------- lm_head
@@ -995,12 +906,11 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
   // dequantisation and the first scales happen before the wait
   __syncthreads();  // the barriers are initialised
   uint2 sc0 = make_uint2(0u, 0u), sc1 = sc0, sc2 = sc0, sc3 = sc0;
-  bool ok = true;
   if (issuer) {
     for (int g = 0; g < kHdStages; ++g) issue_pass(g);
   } else if (loader) {
     if (total > 0) {
-      if (!mbar_wait_bounded(&full[0], 0u, a.err)) ok = false;
+      mbar_wait_bounded(&full[0], 0u, a.err);
       dequant(0);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&aready[0]);
@@ -1092,10 +1002,9 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
   const uint32_t dt = tmem_base;
   if (loader) {
     for (int g = 1; g < total; ++g) {
-      if (!mbar_wait_bounded(&full[g % kHdStages], (g / kHdStages) & 1u, a.err)) ok = false;
+      mbar_wait_bounded(&full[g % kHdStages], (g / kHdStages) & 1u, a.err);
       // the MMAs of pass g - kHdABufs have read this pass's A buffer
-      if (g >= kHdABufs && !mbar_wait_bounded(&afree[g % kHdABufs], ((g - kHdABufs) / kHdABufs) & 1u, a.err))
-        ok = false;
+      if (g >= kHdABufs) mbar_wait_bounded(&afree[g % kHdABufs], ((g - kHdABufs) / kHdABufs) & 1u, a.err);
       dequant(g);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&aready[g % kHdABufs]);
@@ -1105,11 +1014,10 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
     const uint64_t dB0 = smem_desc(sm + HeadSm::b, 128, (kSubK / 8) * 128);
     for (int g = 0; g < total; ++g) {
       // every row of pass g is in its A buffer, so its stage is free
-      if (!mbar_wait_bounded(&aready[g % kHdABufs], (g / kHdABufs) & 1u, a.err)) ok = false;
+      mbar_wait_bounded(&aready[g % kHdABufs], (g / kHdABufs) & 1u, a.err);
       issue_pass(g + kHdStages);
       // the pass's tensor-memory region has been read out (pass g - kHdRegions)
-      if (g >= kHdRegions && !mbar_wait_bounded(&tfree[g % kHdRegions], ((g - kHdRegions) / kHdRegions) & 1u, a.err))
-        ok = false;
+      if (g >= kHdRegions) mbar_wait_bounded(&tfree[g % kHdRegions], ((g - kHdRegions) / kHdRegions) & 1u, a.err);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int k0 = pass_k0(g), nb = min(PK, a.K - k0) / 32;
       mma_pass<true>(dt + (g % kHdRegions) * (4 * kHdN), kHdN,
@@ -1130,7 +1038,7 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
     const uint32_t lane_addr = dt + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     for (int g = 0; g < total; ++g) {
       const int h = g % kHdRegions, nb = min(PK, a.K - pass_k0(g)) / 32;
-      if (!mbar_wait_bounded(&afull[h], (g / kHdRegions) & 1u, a.err)) ok = false;
+      mbar_wait_bounded(&afull[h], (g / kHdRegions) & 1u, a.err);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const float s[4] = {__half2float(__ushort_as_half(static_cast<uint16_t>(sc0.x & 0xFFFFu))),
                           __half2float(__ushort_as_half(static_cast<uint16_t>(sc0.x >> 16))),
@@ -1184,7 +1092,7 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
       a.seqs[t].amax_i[bx] = ci;
     }
   }
-  (void)ok;  // a timed-out wait has set the error word; the host reports it
+  // a timed-out wait has set the error word; the host reports it
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0) {  // every MMA has completed (its half was read out) and every read-out is done
