@@ -181,7 +181,8 @@ int32_t tqd_generate(tqd_model* model, int32_t seq, int32_t first_token, int32_t
 /* One greedy step for sequences 0 .. n_seq-1 together (n_seq <= 16 and
  * <= max_batch): sequence b feeds tokens[b] at pos[b] (its next position).
  * The projections run as tensor-core contractions over the batch (tcgen05,
- * f32-accurate through exact tf32 splits), attention per sequence.  next_out[b]
+ * f32-accurate: exact int8 weight operands, activations split into bf16 or f16
+ * parts), attention per sequence.  next_out[b]
  * receives sequence b's argmax.  Errors: as tqd_decode_step, plus
  * UNSUPPORTED_CONFIG when the model has no batched step (max_batch == 1).
  * ("Metal LLM decode", the batched prefill+decode arm: sequences share one

@@ -3,12 +3,14 @@
 // fifth-generation tensor cores (tcgen05, accumulator in tensor memory), and
 // attention runs per sequence as a streaming split-K flash decode.
 //
-// Numerics: a Q8_0 weight w = scale * quant is exact in f32 (8-bit quant times
-// an 11-bit significand), and splits exactly into two tf32 values w_hi + w_lo;
-// an activation x splits into x_hi + x_lo (22 significant bits).  Three tf32
-// products w_hi x_hi + w_hi x_lo + w_lo x_hi, each exact in f32 and summed in
-// f32, give f32-level dot products (the dropped w_lo x_lo term is ~2^-22 of
-// the product).  bf16 weights are exact in tf32, so two products suffice.
+// Numerics (kind::f16, f32 accumulation): a Q8_0 quant is an integer in
+// [-127, 127], exact in bf16 and in f16, so the weights enter as A unchanged;
+// every 32-wide block accumulates into its own tensor-memory columns and its
+// f16 scale multiplies the block's sums at read-out.  The activations enter as
+// B split into parts: three bf16 parts in the projections (24 significant
+// bits: each product is exact and the sums are f32 sums), two f16 parts in the
+// lm_head, whose input is the bounded RMSNorm output (22 significant bits).
+// bf16 weights are exact in bf16 (scale 1); the lm_head stores them as f16.
 //
 // What is computed is the decode step of the inferno.rs blog, "IV.4: One
 // command buffer per token", for several sequences sharing one sweep of the
