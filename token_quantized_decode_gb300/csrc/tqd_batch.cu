@@ -1499,6 +1499,38 @@ bool batch_supported(const DevModel& m) {
          split_ok(m.I) && m.H <= kHeadMaxK && attn_batch_smem(m) <= 227 * 1024;
 }
 
+namespace {
+
+// Host-supplied tokens of one batched step: tok[b] becomes sequence b's input
+// token at its next position (one upload for all sequences).
+__global__ void k_batch_tokens_in(const DevSeq* seqs, int n, const int32_t* tok) {
+  const int b = static_cast<int>(threadIdx.x);
+  if (b < n) seqs[b].tokens[seqs[b].state->pos] = tok[b];
+}
+
+// After a step: out[b] = sequence b's argmax (its input token at the new
+// position), out[n + b] = its error word (one readback for all sequences).
+__global__ void k_batch_tokens_out(const DevSeq* seqs, int n, int32_t* out) {
+  const int b = static_cast<int>(threadIdx.x);
+  if (b < n) {
+    const DevSeq& s = seqs[b];
+    out[b] = s.tokens[s.state->pos];
+    out[n + b] = static_cast<int32_t>(s.state->err);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_batch_tokens_in(const DevSeq* seqs, int n, const int32_t* tok, cudaStream_t st) {
+  k_batch_tokens_in<<<1, kTcN, 0, st>>>(seqs, n, tok);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_batch_tokens_out(const DevSeq* seqs, int n, int32_t* out, cudaStream_t st) {
+  k_batch_tokens_out<<<1, kTcN, 0, st>>>(seqs, n, out);
+  return cudaGetLastError();
+}
+
 cudaError_t batch_setup(const DevModel& m) {
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_mm16<SplitCfg>),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -75,6 +75,7 @@ struct tqd_model {
   uint32_t* bcount = nullptr;
   float* bss = nullptr;
   uint8_t* blm = nullptr;  // the lm_head in the batched step's tile-pass order
+  int32_t* bio = nullptr;  // a batched step's tokens in [16], argmax out and error words [2 x 16]
   int batch_nch = 1;
   cudaGraphExec_t bgraph[17] = {};
 };
@@ -462,7 +463,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   }
   // batched-step buffers (only for models holding several sequences)
   const int bmax = batch_max();
-  size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0, o_blm = 0;
+  size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0, o_blm = 0,
+         o_bio = 0;
   if (cfg->max_batch > 1) {
     o_bx = take(4ull * bmax * H);
     o_bqkv = take(4ull * bmax * (qw + 2 * kvw));
@@ -473,6 +475,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     o_bcount = take(4);
     o_bss = take(4ull * 2 * batch_ss_slots(H) * bmax);
     o_blm = take(batch_head_bytes(V, H, fmt));
+    o_bio = take(4ull * 3 * bmax);
   }
   m->arena_bytes = off;
   cudaError_t ce = cudaMalloc(&m->arena, m->arena_bytes);
@@ -651,6 +654,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     m->bcount = reinterpret_cast<uint32_t*>(base + o_bcount);
     m->bss = reinterpret_cast<float*>(base + o_bss);
     m->blm = base + o_blm;
+    m->bio = reinterpret_cast<int32_t*>(base + o_bio);
     std::vector<DevSeq> hs(cfg->max_batch);
     for (int b = 0; b < cfg->max_batch; ++b) hs[b] = m->seqs[b].d;
     if ((e = cudaMemcpy(m->dseqs, hs.data(), sizeof(DevSeq) * cfg->max_batch,
@@ -921,18 +925,17 @@ int32_t tqd_decode_step_batch(tqd_model* m, int32_t n_seq, const int32_t* tokens
       return TQD_ERR_CAPACITY;
     }
   }
-  for (int b = 0; b < n_seq; ++b) {
-    m->h_tokens[b] = tokens[b];
-    CK(cudaMemcpyAsync(m->seqs[b].d.tokens + pos[b], m->h_tokens + b, 4, cudaMemcpyHostToDevice,
-                       m->stream),
-       "write token");
-  }
+  // one upload of the tokens, the step, one readback of the argmaxes and error words
+  memcpy(m->h_tokens, tokens, 4ull * n_seq);
+  CK(cudaMemcpyAsync(m->bio, m->h_tokens, 4ull * n_seq, cudaMemcpyHostToDevice, m->stream), "write tokens");
+  CK(launch_batch_tokens_in(m->dseqs, n_seq, m->bio, m->stream), "place tokens");
   if ((rc = run_batch(m, n_seq, 1))) return rc;
+  CK(launch_batch_tokens_out(m->dseqs, n_seq, m->bio + batch_max(), m->stream), "gather tokens");
+  CK(cudaMemcpyAsync(m->h_tokens + 64, m->bio + batch_max(), 8ull * n_seq, cudaMemcpyDeviceToHost, m->stream),
+     "read next tokens");
+  CK(cudaStreamSynchronize(m->stream), "synchronize");
   for (int b = 0; b < n_seq; ++b)
-    CK(cudaMemcpyAsync(m->h_tokens + 64 + b, m->seqs[b].d.tokens + pos[b] + 1, 4,
-                       cudaMemcpyDeviceToHost, m->stream),
-       "read next token");
-  if ((rc = finish_batch(m, n_seq))) return rc;
+    if (m->h_tokens[64 + n_seq + b] != 0) return finish_batch(m, n_seq);  // reports and clears the error
   for (int b = 0; b < n_seq; ++b) {
     m->seqs[b].next_pos = pos[b] + 1;
     next_out[b] = m->h_tokens[64 + b];

@@ -105,6 +105,11 @@ cudaError_t batch_setup(const DevModel& m);
 size_t batch_head_bytes(int rows, int K, int fmt);
 cudaError_t launch_head_tile(const uint8_t* rows_src, size_t rb, int rows, int K, int fmt, uint8_t* dst,
                              cudaStream_t st);
+// One upload of a step's host tokens for all sequences (tok[b] -> sequence b's
+// input at its next position), and one readback of every sequence's argmax and
+// error word after the step (out[b], out[n + b]).
+cudaError_t launch_batch_tokens_in(const DevSeq* seqs, int n, const int32_t* tok, cudaStream_t st);
+cudaError_t launch_batch_tokens_out(const DevSeq* seqs, int n, int32_t* out, cudaStream_t st);
 // PO / PML: the attention's chunk partials, [n][nq][nch][hd] and [n][nq][nch][2].
 cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const uint8_t* lm_tiled,
                                const DevSeq* seqs, int n, int nch, float* X, float* QKV, float* PO, float* PML,
