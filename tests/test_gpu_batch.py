@@ -71,6 +71,37 @@ def test_batch_sixteen_tiny_sequences(tqd):
     assert batched_vs_oracle(tqd, synth.TINY, 16, 6, 2, 12) < 1e-4
 
 
+def test_batch_ragged_positions(tqd):
+    """Sequences at different positions in one step (histories of 1 to 23
+    rows): each sequence's attention split and the O projection's merge of its
+    chunks follow its own length; three teacher-forced steps vs the oracle."""
+    cfg = synth.TINY
+    model = synth.make_model(cfg, 2)
+    lens = [1, 4, 9, 16, 23]
+    n, steps, max_seq = len(lens), 3, 32
+    dec = tqd.Decoder(model, max_seq, n)
+    oms, toks, pos = [], [], []
+    for b, P in enumerate(lens):
+        ids = synth.token_ids(1000, 20 + b, P, cfg.vocab)
+        om = oracle.OracleModel(model, max_seq)
+        tok, _ = om.prefill(ids)
+        assert dec.prefill(ids, seq=b) == tok
+        oms.append(om)
+        toks.append(tok)
+        pos.append(P)
+    worst = 0.0
+    for i in range(steps):
+        refs = [oms[b].step(toks[b], pos[b]) for b in range(n)]
+        got = dec.decode_step_batch(np.array(toks), np.array(pos))
+        for b in range(n):
+            worst = max(worst, check_step(dec.logits(seq=b), int(got[b]), refs[b][1], refs[b][0],
+                                          f"step {i} seq {b} pos {pos[b]}"))
+        toks = [r[0] for r in refs]
+        pos = [p + 1 for p in pos]
+    assert worst < 1e-4
+    dec.close()
+
+
 def test_batch_matches_single_sequence_path(tqd):
     cfg = synth.TINY
     model = synth.make_model(cfg, 5)
