@@ -270,7 +270,19 @@ struct MmArgs {
   const float* part_o;
   const float* part_ml;
   int nch, hd;
+  // the next kernel's weights, prefetched into L2 before the dependency wait
+  // (its CTAs that start only as this kernel ends then find them there)
+  const uint8_t* pf;
+  size_t pf_bytes;
 };
+
+// This CTA's share of an L2 prefetch of [p, p + bytes), 128-byte lines.
+__device__ __forceinline__ void prefetch_share(const uint8_t* p, size_t bytes, int nt) {
+  if (!p) return;
+  const size_t lines = bytes >> 7, stride = static_cast<size_t>(gridDim.x) * nt;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * nt + threadIdx.x; i < lines; i += stride)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p + (i << 7)));
+}
 
 // Thread t of the CTA works on weight row t of its tile (tensor-memory lane
 // t); the cluster's ranks split the tile's K, and each rank owns a range of
@@ -338,6 +350,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   if (a.gain) {  // the RMSNorm gain of this rank's K range, into L2 ahead of the dependency wait
     for (int i = t; i < KR / 32; i += NT) prefetch_l2(a.gain + kc0 + 32 * i);
   }
+  prefetch_share(a.pf, a.pf_bytes, NT);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tmem_base)), "n"(CFG::tmem)
@@ -1253,6 +1266,11 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
       bulk_g2s(dst + static_cast<size_t>(rpp) * HD * 4u, s.vcache + head + static_cast<size_t>(a0) * HD, bytes,
                full + slot);
     }
+    {  // the O projection's weights into L2, this CTA's share of their 128-byte lines
+      const uint8_t* p = m.layers[layer].wo;
+      const size_t lines = (m.row_bytes_qw * m.H) >> 7;
+      for (size_t i = blockIdx.x; i < lines; i += gridDim.x) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + (i << 7)));
+    }
     return;
   }
   if (threadIdx.x > kAT) return;
@@ -1590,13 +1608,15 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
   if (e != cudaSuccess) return e;
   auto mm = [&](const uint8_t* W, size_t rb, int K, int rows, const float* Xin, int ldx, const float* gain,
                 const float* ss, int nss, int epi, float* Y, int ldy, float* ss_out, bool split,
-                bool from_parts = false) {
+                bool from_parts = false, const uint8_t* pf = nullptr, size_t pf_bytes = 0) {
     MmArgs a{};
     a.W = W; a.rb = rb; a.K = K; a.rows = rows; a.fmt = fmt;
     a.cs = split ? mm_cluster(K, rows, num_sms) : 1;
     a.X = Xin; a.ldx = ldx; a.n = n; a.gain = gain; a.ss = ss; a.nss = nss; a.eps = m.eps;
     a.epi = epi; a.Y = Y; a.ldy = ldy; a.ss_out = ss_out;
     a.seqs = seqs; a.count = count; a.err = err; a.max_seq = m.max_seq;
+    a.pf = pf;
+    a.pf_bytes = pf_bytes;
     if (from_parts) {  // X is the attention's chunk partials, merged while B is built
       a.part_o = PO; a.part_ml = PML; a.nch = nch; a.hd = m.hd;
     }
@@ -1627,13 +1647,14 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
       if ((e = cudaLaunchKernelExC(&ca, attn_fn, args)) != cudaSuccess) return e;
     }
     if ((e = mm(L.wo, m.row_bytes_qw, m.qw, m.H, nullptr, m.qw, nullptr, nullptr, 0, kEpiResid, X, m.H, ss_mid,
-                true, true)) != cudaSuccess)
+                true, true, L.wgu, m.row_bytes_h * 2 * m.I)) != cudaSuccess)
       return e;
     if ((e = mm(L.wgu, m.row_bytes_h, m.H, 2 * m.I, X, m.H, L.ffn_norm, ss_mid, nss_mid, kEpiSwiGLU, H, m.I,
-                nullptr, true)) != cudaSuccess)
+                nullptr, true, false, L.wd, m.row_bytes_i * m.H)) != cudaSuccess)
       return e;
-    if ((e = mm(L.wd, m.row_bytes_i, m.I, m.H, H, m.I, nullptr, nullptr, 0, kEpiResid, X, m.H, ss_x, true)) !=
-        cudaSuccess)
+    const bool more = l + 1 < m.n_layers;
+    if ((e = mm(L.wd, m.row_bytes_i, m.I, m.H, H, m.I, nullptr, nullptr, 0, kEpiResid, X, m.H, ss_x, true, false,
+                more ? host_layers[l + 1].wqkv : nullptr, more ? m.row_bytes_h * lqkv : 0)) != cudaSuccess)
       return e;
   }
   return mm(lm_tiled, m.row_bytes_h, m.H, m.V, X, m.H, m.out_norm, ss_x, nss_x, kEpiArgmax, nullptr, 0,
