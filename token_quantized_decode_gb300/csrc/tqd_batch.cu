@@ -340,24 +340,10 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   // [own0, own0 + own) of the tile are this rank's
   const bool push = a.cs > 1;
   const int own0 = pair_row0(rank, a.cs), own = pair_row0(rank + 1, a.cs) - own0;
-  if (t == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    mbar_init(&rbar, 1);
-    if (push) mbar_arrive_expect_tx(&rbar, static_cast<uint32_t>(a.cs * own * kTcN * 4));
-    fence_mbar_init();
-  }
-  if (a.gain) {  // the RMSNorm gain of this rank's K range, into L2 ahead of the dependency wait
-    for (int i = t; i < KR / 32; i += NT) prefetch_l2(a.gain + kc0 + 32 * i);
-  }
-  prefetch_share(a.pf, a.pf_bytes, NT);
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(&tmem_base)), "n"(CFG::tmem)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  // weights never depend on earlier kernels: their loads start before the wait
+  // weights never depend on earlier kernels: their loads are issued first,
+  // before the dependency wait and before the setup below, whose latency they
+  // then overlap (a CTA that starts only as the previous kernel ends would
+  // otherwise pay both)
   for (int g = 0; g < STAGES - 1; ++g) {
     if (g < total) issue_raw(g);
     else cp_async_commit();  // empty groups keep the group count uniform
@@ -366,6 +352,23 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   uint16_t sc_next[4], sc_next2[4];
   load_scales(0, sc_next);
   load_scales(1, sc_next2);
+  if (t == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    mbar_init(&rbar, 1);
+    if (push) mbar_arrive_expect_tx(&rbar, static_cast<uint32_t>(a.cs * own * kTcN * 4));
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base)), "n"(CFG::tmem)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (a.gain) {  // the RMSNorm gain of this rank's K range, into L2 ahead of the dependency wait
+    for (int i = t; i < KR / 32; i += NT) prefetch_l2(a.gain + kc0 + 32 * i);
+  }
+  prefetch_share(a.pf, a.pf_bytes, NT);
   // per-pass state of the two passes in flight, kept in registers (even and
   // odd passes as separate variables: an array indexed by the pass parity
   // would live in local memory, which misses the small L1 left beside the
