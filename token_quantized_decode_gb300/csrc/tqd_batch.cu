@@ -201,6 +201,12 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -418,6 +424,7 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
       const int lr = tr - pair_row0(q, a.cs);
       const uint32_t dst = mapa_u32(recv + (rank * rs + lr) * kTcN, static_cast<uint32_t>(q));
       if (push) {
+        cluster_wait();
         const uint32_t qbar = mapa_u32(&rbar, static_cast<uint32_t>(q));
 #pragma unroll
         for (int i = 0; i < kTcN / 4; ++i)
@@ -548,7 +555,9 @@ __global__ void __launch_bounds__(CFG::threads, 1) k_mm16(MmArgs a) {
   // the first pass's weights are dequantised before the wait as well
   if (total > 0) load_pass(0);
   if (pre2) prep_pass1();
-  if (push) cluster_sync();  // every rank's rbar is initialised before any partial is sent
+  // every rank's rbar is initialised before any partial is sent: arrive now,
+  // wait just before sending (by then every rank has long arrived)
+  if (push) cluster_arrive();
   pdl_wait();
   pdl_launch_dependents();
   // inputs of the previous kernel: the RMSNorm sums of squares and B for the
