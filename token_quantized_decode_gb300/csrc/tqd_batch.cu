@@ -1039,19 +1039,41 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
   } else if (issuer) {
     const uint64_t dA0 = smem_desc(sm + HeadSm::a, 128, (kSubK / 8) * 128);
     const uint64_t dB0 = smem_desc(sm + HeadSm::b, 128, (kSubK / 8) * 128);
+    // running counters instead of divisions by the pass count: this thread
+    // paces the passes.  isrc / ip: the pass issued next (kHdStages ahead) and
+    // its pass within its tile; mp: the K pass multiplied; abuf / aph: its A
+    // buffer and that buffer's phase
+    const uint8_t* isrc = kHdStages < total ? pass_src(kHdStages) : a.W;
+    int ip = kHdStages % npass, mp = 0, abuf = 0;
+    uint32_t aph = 0u;
+    const size_t tile_step = (static_cast<size_t>(gx) * npass - npass + 1) * kHdPassBytes;
     for (int g = 0; g < total; ++g) {
       // every row of pass g is in its A buffer, so its stage is free
-      mbar_wait_bounded(&aready[g % kHdABufs], (g / kHdABufs) & 1u, a.err);
-      issue_pass(g + kHdStages);
+      mbar_wait_bounded(&aready[abuf], aph, a.err);
+      if (g + kHdStages < total) {
+        uint64_t* bar = &full[g % kHdStages];  // the stage of pass g, reused by pass g + kHdStages
+        mbar_arrive_expect_tx(bar, kRawBytes);
+        bulk_g2s(sm + HeadSm::raw + (g % kHdStages) * kRawBytes, isrc, kRawBytes, bar);
+        if (++ip == npass) {
+          ip = 0;
+          isrc += tile_step;
+        } else {
+          isrc += kHdPassBytes;
+        }
+      }
       // the pass's tensor-memory region has been read out (pass g - kHdRegions)
       if (g >= kHdRegions) mbar_wait_bounded(&tfree[g % kHdRegions], ((g - kHdRegions) / kHdRegions) & 1u, a.err);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int k0 = pass_k0(g), nb = min(PK, a.K - k0) / 32;
-      mma_pass<true>(dt + (g % kHdRegions) * (4 * kHdN), kHdN,
-                     dA0 + (((g % kHdABufs) * kAPassBytes) >> 4), dB0 + (((k0 / kSubK) * kHdBBytes) >> 4), kHdBBytes,
-                     nb);
+      const int k0 = mp * PK, nb = min(PK, a.K - k0) / 32;
+      mma_pass<true>(dt + (g % kHdRegions) * (4 * kHdN), kHdN, dA0 + ((abuf * kAPassBytes) >> 4),
+                     dB0 + (((k0 / kSubK) * kHdBBytes) >> 4), kHdBBytes, nb);
       mma_commit(&afull[g % kHdRegions]);
-      mma_commit(&afree[g % kHdABufs]);
+      mma_commit(&afree[abuf]);
+      if (++mp == npass) mp = 0;
+      if (++abuf == kHdABufs) {
+        abuf = 0;
+        aph ^= 1u;
+      }
     }
   } else if (t < kTcM) {
     float acc[kTcN], bv[kTcN];
