@@ -67,6 +67,15 @@ def test_batch_tiny_bf16(tqd):
     assert w < 1e-4
 
 
+def test_batch_odd_shape(tqd):
+    """Hidden 320 (ten 32-wide blocks: uneven cluster K splits, a half last pass
+    of the lm_head) and vocabulary 4000 (a last lm_head tile of 32 rows,
+    zero-padded in the tile-pass copy)."""
+    cfg = synth.ModelConfig(2, 320, 4, 2, 64, 640, 4000, True, "q8_0", 1e6)
+    w = batched_vs_oracle(tqd, cfg, 6, 9, 3, 16)
+    assert w < 1e-4
+
+
 def test_batch_sixteen_tiny_sequences(tqd):
     assert batched_vs_oracle(tqd, synth.TINY, 16, 6, 2, 12) < 1e-4
 
