@@ -262,6 +262,16 @@ int32_t tqd_op_attention(const float* q, const float* K, const float* V, int32_t
 size_t tqd_attention_scratch_bytes(int32_t n_heads, int32_t n_kv, int32_t head_dim,
                                    int32_t n_chunks);
 
+/* Failure detection without a GPU fault: runs one block whose bounded device
+ * waits cannot complete (an mbarrier no thread arrives at, and a counter that
+ * nothing increments, polled the way a grid barrier is); each gives up after
+ * its 2 s limit, records its error bit and returns.  *err_bits_out receives
+ * the bits (1: counter wait, 2: mbarrier wait); the status is
+ * TQD_ERR_DEVICE_TIMEOUT when any is set.  The CUDA context stays usable.
+ * Takes about 2 s ("One command buffer per token", "The seam": a failed step
+ * is reported, not hung on). */
+int32_t tqd_op_wait_selftest(void* stream, uint32_t* err_bits_out);
+
 /* out = silu(g) * u elementwise, silu(z) = z / (1 + e^-z)
  * ("Eight kernels", silu_hadamard). */
 int32_t tqd_op_silu_mul(const float* g, const float* u, int64_t n, float* out, void* stream);

@@ -238,3 +238,25 @@ def test_argmax_nan_and_edges(ops):
     x = synth.uniform_f32(9, 9, 300001)
     x[[5, 299999, 123456]] = 2.0  # equal maxima far apart
     assert gpu_argmax(ops, x) == 5
+
+
+def test_bounded_waits_report_a_timeout_and_the_context_survives(ops):
+    """Failure detection without a fault: a wait on an mbarrier nothing arrives
+    at and a wait on a counter nothing increments each give up after their
+    limit, set their error bits, and the host reads TQD_ERR_DEVICE_TIMEOUT;
+    the device then runs another operator normally."""
+    import time
+    import token_quantized_decode_gb300 as tqd
+    t0 = time.perf_counter()
+    status, bits = ops.tqd_op_wait_selftest()
+    elapsed = time.perf_counter() - t0
+    assert tqd.tqd_status_name(status) == "TQD_ERR_DEVICE_TIMEOUT"
+    assert bits == 3  # counter wait (1) and mbarrier wait (2)
+    assert 1.5 < elapsed < 30.0
+    g = torch.randn(1000, device="cuda")
+    u = torch.randn(1000, device="cuda")
+    out = torch.empty(1000, device="cuda")
+    ops.tqd_op_silu_mul(g, u, 1000, out)
+    torch.cuda.synchronize()
+    ref = (g / (1 + torch.exp(-g))) * u
+    assert torch.allclose(out, ref, rtol=1e-5, atol=1e-6)

@@ -89,6 +89,7 @@ def lib():
         "tqd_op_rope": (i32, [vp, i32, i32, i32, vp, vp]),
         "tqd_op_attention": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
         "tqd_attention_scratch_bytes": (sz, [i32, i32, i32, i32]),
+        "tqd_op_wait_selftest": (i32, [vp, P(ctypes.c_uint32)]),
         "tqd_op_silu_mul": (i32, [vp, vp, i64, vp, vp]),
         "tqd_op_argmax": (i32, [vp, i64, vp, vp, vp]),
         "tqd_argmax_scratch_bytes": (sz, []),
@@ -111,7 +112,7 @@ def exported_symbols():
         "tqd_generate_batch", "tqd_read_logits",
         "tqd_phase_count", "tqd_step_bytes", "tqd_op_q8_0_repack", "tqd_op_q8_0_matvec",
         "tqd_op_bf16_matvec", "tqd_op_rmsnorm", "tqd_op_rope_table", "tqd_op_rope", "tqd_op_attention",
-        "tqd_attention_scratch_bytes", "tqd_op_silu_mul", "tqd_op_argmax", "tqd_argmax_scratch_bytes",
+        "tqd_attention_scratch_bytes", "tqd_op_wait_selftest", "tqd_op_silu_mul", "tqd_op_argmax", "tqd_argmax_scratch_bytes",
         "tqd_op_attention_noalloc", "tqd_op_attention_noalloc_max_scratch",
     ]
 

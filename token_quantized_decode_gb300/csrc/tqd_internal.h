@@ -115,6 +115,10 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
                                const DevSeq* seqs, int n, int nch, float* X, float* QKV, float* PO, float* PML,
                                float* H, float* SS, uint32_t* count, uint32_t* err, cudaStream_t st);
 
+// The bounded-wait self-test (tqd_op_wait_selftest): runs it on st and
+// returns the error bits its waits set.
+cudaError_t run_wait_selftest(uint32_t* err_bits, cudaStream_t st);
+
 // Record the text tqd_last_error() returns on this thread.
 void set_last_error(const char* msg);
 

@@ -445,4 +445,46 @@ cudaError_t launch_op_argmax(const float* x, int64_t n, int32_t* out, float* can
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- wait self-test
+// Failure detection without a GPU fault: warp 0 waits on an mbarrier no thread
+// arrives at (the bounded wait the ring and tensor-core kernels use); thread 32
+// polls a counter nothing increments, the way a grid barrier does.  Both give
+// up after kWaitLimitNs, set their error bits and return, and the context
+// stays usable.
+__device__ uint32_t g_wait_err;
+__device__ unsigned long long g_wait_ctr;  // never incremented
+
+__global__ void k_wait_selftest() {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    g_wait_err = 0u;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    mbar_wait_bounded(&bar, 0u, &g_wait_err);
+  } else if (threadIdx.x == 32) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(&g_wait_ctr) : "memory");
+      if (v >= 1ull) break;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(&g_wait_err, kErrGridBarrier);
+        break;
+      }
+    }
+  }
+}
+
+cudaError_t run_wait_selftest(uint32_t* err_bits, cudaStream_t st) {
+  k_wait_selftest<<<1, 64, 0, st>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbolAsync(err_bits, g_wait_err, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(st);
+}
+
 }  // namespace tqd

@@ -101,6 +101,15 @@ int32_t tqd_op_attention(const float* q, const float* K, const float* V, int32_t
                                        cnt, static_cast<cudaStream_t>(stream)));
 }
 
+int32_t tqd_op_wait_selftest(void* stream, uint32_t* err_bits_out) {
+  if (!err_bits_out) return TQD_ERR_BAD_ARG;
+  uint32_t bits = 0u;
+  const cudaError_t e = run_wait_selftest(&bits, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return status_of(e);
+  *err_bits_out = bits;
+  return bits ? TQD_ERR_DEVICE_TIMEOUT : TQD_OK;
+}
+
 int32_t tqd_op_silu_mul(const float* g, const float* u, int64_t n, float* out, void* stream) {
   if (!g || !u || !out || n <= 0) return TQD_ERR_BAD_ARG;
   return status_of(launch_op_silu_mul(g, u, n, out, static_cast<cudaStream_t>(stream)));

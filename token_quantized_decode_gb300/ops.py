@@ -63,6 +63,15 @@ def tqd_op_attention_noalloc_max_scratch() -> int:
     return int(lib().tqd_op_attention_noalloc_max_scratch())
 
 
+def tqd_op_wait_selftest(stream=None):
+    """Run the bounded-wait self-test; returns (status, error bits) without
+    raising (the expected status is TQD_ERR_DEVICE_TIMEOUT)."""
+    import ctypes
+    bits = ctypes.c_uint32(0)
+    status = lib().tqd_op_wait_selftest(_s(stream), ctypes.byref(bits))
+    return int(status), int(bits.value)
+
+
 def tqd_op_silu_mul(g, u, n: int, out, stream=None):
     check(lib().tqd_op_silu_mul(g.data_ptr(), u.data_ptr(), n, out.data_ptr(), _s(stream)), "tqd_op_silu_mul")
 
