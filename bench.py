@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--kv-source", choices=["prefill", "upload"], default="prefill",
                    help="prefill the prompt on the GPU, or upload a seeded stand-in KV history of the same "
                         "length (for profiling captures that should not include the prefill launches)")
+    p.add_argument("--prefill", choices=["tiles", "steps"], default="tiles",
+                   help="prefill in tiles of 16 positions (tqd_prefill_batch) or position by position "
+                        "(tqd_prefill); batch-1 runs time both after the decode measurement")
     return p.parse_args()
 
 
@@ -233,6 +236,65 @@ def run_reference(args, wl, world, rank):
     return line
 
 
+def prefill(dec, ids, seq, tiles):
+    """The prompt through tqd_prefill_batch (tiles), or tqd_prefill where the
+    shape has no batched step or steps were asked for."""
+    import token_quantized_decode_gb300 as tqd
+    if tiles:
+        try:
+            return dec.prefill_batch(ids, seq=seq)
+        except tqd.TQDError as e:
+            if e.name != "TQD_ERR_UNSUPPORTED_CONFIG":
+                raise
+    return dec.prefill(ids, seq=seq)
+
+
+def time_prefill(dec, wl, stream, kv_pos, w_and_row, emb_row):
+    """Prompt throughput of one sequence's prefill through the C ABI (prompt
+    upload and next-token readback included): tiles (median of 3 after one
+    warm-up call that instantiates the tile graphs) and position by position
+    (one call).  Algorithmic bytes of the tiled prefill: per tile, the layers'
+    weights once, one embedding row per position, the K/V rows the tile
+    attends to (each once) and the rows it writes; the lm_head once."""
+    import torch
+    import token_quantized_decode_gb300 as tqd
+    cfg, P = wl.model, wl.prompt_len
+    ids = synth.prompt(wl, seq=0)
+
+    def once(fn):
+        dec.truncate(0)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn(ids)
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e)
+
+    try:
+        once(dec.prefill_batch)
+    except tqd.TQDError as e:
+        if e.name != "TQD_ERR_UNSUPPORTED_CONFIG":
+            raise
+        return None
+    tiles_ms = float(np.median([once(dec.prefill_batch) for _ in range(3)]))
+    steps_ms = once(dec.prefill)
+    row_h = cfg.hidden * 17 // 16 if cfg.weight_type == "q8_0" else 2 * cfg.hidden
+    head = cfg.vocab * row_h + 4 * cfg.hidden                  # lm_head rows + final norm
+    layers = w_and_row - emb_row - head
+    nbytes, p0 = head, 0
+    while p0 < P:
+        n = min(16, P - p0)
+        nbytes += layers + n * emb_row + kv_pos * (p0 + n) + kv_pos * n
+        p0 += n
+    hbm, kind = peaks()
+    return {"value": P / (tiles_ms / 1000.0), "unit": "prompt tokens/s", "tokens": P,
+            "ms": tiles_ms, "tiles": (P + 15) // 16, "api": "tqd_prefill_batch (tiles of 16 positions)",
+            "roofline_frac": nbytes / (tiles_ms / 1000.0) / 1e9 / hbm, "algorithmic_bytes": nbytes,
+            "peak_kind": f"{kind} copy bandwidth",
+            "stepwise": {"value": P / (steps_ms / 1000.0), "ms": steps_ms, "api": "tqd_prefill (one decode step per position)"}}
+
+
 def run_tqd(args, wl, world, rank, local, pg):
     import torch
     import token_quantized_decode_gb300 as tqd
@@ -249,7 +311,7 @@ def run_tqd(args, wl, world, rank, local, pg):
     for b in range(B):
         ids = synth.prompt(wl, seq=b)
         if args.kv_source == "prefill":
-            firsts.append(dec.prefill(ids, seq=b))
+            firsts.append(prefill(dec, ids, b, args.prefill == "tiles"))
         else:
             k, v = synth.kv_fill(cfg, 7, b, P, -1.0, 1.0)
             dec.kv_upload(k, v, seq=b)
@@ -336,6 +398,9 @@ def run_tqd(args, wl, world, rank, local, pg):
     e2e_s = time.perf_counter() - t0
     e2e_val = sum_over_ranks(pg, n_e2e * B) / max_over_ranks(pg, e2e_s)
 
+    prefill_line = (time_prefill(dec, wl, stream, kv_pos, w_and_row, emb_row)
+                    if B == 1 and args.kv_source == "prefill" else None)
+
     hbm, kind = peaks()
     achieved = per_launch_bytes / (per_launch_ms / 1000.0) / 1e9
     mean_step_bytes = total_bytes / steps
@@ -353,7 +418,7 @@ def run_tqd(args, wl, world, rank, local, pg):
         "config": {"workload": wl.name, "prompt_len": P, "decode_positions": f"{P}..{P + D - 1}",
                    "batch": B, "schedule": args.schedule if B == 1 else "batched graph",
                    "weights": ("Q8_0 (34-byte blocks)" if cfg.weight_type == "q8_0" else "bf16") + ", resident",
-                   "kv_history": args.kv_source,
+                   "kv_history": args.kv_source + (f" ({args.prefill})" if args.kv_source == "prefill" else ""),
                    "l2": "inputs larger than L2: each step streams %.0f MB vs 129 MB L2" % (mean_step_bytes / 1e6),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -369,6 +434,8 @@ def run_tqd(args, wl, world, rank, local, pg):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if prefill_line:
+        line["prefill"] = prefill_line
     dec.close()
     return line
 

@@ -155,6 +155,20 @@ int32_t tqd_next_pos(tqd_model* model, int32_t seq, int32_t* pos_out);
 int32_t tqd_prefill(tqd_model* model, int32_t seq, const int32_t* ids, int32_t n,
                     int32_t* next_out);
 
+/* The same result as tqd_prefill (the prompt at next_pos .. next_pos+n-1,
+ * then the greedy next token in *next_out), computed in tiles of up to 16
+ * prompt positions: each tile is one batched step whose slots are the tile's
+ * positions, so the projections sweep the weights once per tile on the tensor
+ * cores (as tqd_decode_step_batch) and every slot attends to the cache rows
+ * up to its own position, the tile's earlier rows included; the lm_head runs
+ * for the prompt's last position only.  A longer prompt runs tile after tile,
+ * each writing the next slice of the KV cache at its own offset ("Metal LLM
+ * decode", the batched prefill+decode arm: prefill_batch, chunked calls at
+ * position offsets).  Any max_batch; errors: as tqd_prefill, plus
+ * UNSUPPORTED_CONFIG for a shape the batched kernels do not cover. */
+int32_t tqd_prefill_batch(tqd_model* model, int32_t seq, const int32_t* ids, int32_t n,
+                          int32_t* next_out);
+
 /* Replace sequence seq's KV cache with n_pos host rows: k, v are f32
  * [n_layers][n_pos][n_kv_heads*head_dim] holding post-RoPE keys and values
  * ("One command buffer per token", section "The cache comes over once").

@@ -193,8 +193,8 @@ def reference_run(model, ids, max_seq, n_steps):
     return out
 
 
-def replay(dec, ids, ref):
-    got = dec.prefill(ids)
+def replay(dec, ids, ref, tiles=False):
+    got = dec.prefill_batch(ids) if tiles else dec.prefill(ids)
     check_step(dec.logits(), got, ref[0][2], ref[0][3], "prefill")
     for i, (tok, pos, lg, nxt) in enumerate(ref[1:]):
         got = dec.decode_step(tok, pos)
@@ -217,6 +217,16 @@ def test_qwen3_shape_full_size(tqd, qwen3_reference, schedule):
     wl, model, ids, ref = qwen3_reference
     dec = tqd.Decoder(model, wl.prompt_len + wl.decode_steps, 1, sched(tqd, schedule))
     replay(dec, ids, ref)
+    dec.close()
+
+
+def test_qwen3_shape_prefill_tiles_full_size(tqd, qwen3_reference):
+    """The same 511-token prompt prefilled in tiles of 16 (31 full tiles and
+    one of 15) on the one-sequence persistent model the benchmark times, then
+    the three teacher-forced decode steps over the cache the tiles wrote."""
+    wl, model, ids, ref = qwen3_reference
+    dec = tqd.Decoder(model, wl.prompt_len + wl.decode_steps, 1, tqd.TQD_SCHED_PERSISTENT)
+    replay(dec, ids, ref, tiles=True)
     dec.close()
 
 

@@ -18,7 +18,7 @@ from ._lib import (TQD_SCHED_GRAPH, TQD_SCHED_PERSISTENT, TQD_WEIGHT_BF16, TQD_W
 __all__ = [
     "TQDError", "TQD_SCHED_GRAPH", "TQD_SCHED_PERSISTENT", "TQD_WEIGHT_Q8_0", "TQD_WEIGHT_BF16",
     "make_config", "make_host_weights", "tqd_status_name", "tqd_create", "tqd_destroy", "tqd_reset",
-    "tqd_truncate", "tqd_next_pos", "tqd_prefill", "tqd_kv_upload", "tqd_decode_step", "tqd_generate",
+    "tqd_truncate", "tqd_next_pos", "tqd_prefill", "tqd_prefill_batch", "tqd_kv_upload", "tqd_decode_step", "tqd_generate",
     "tqd_decode_step_batch", "tqd_generate_batch", "tqd_read_logits", "tqd_phase_count", "tqd_step_bytes",
     "Decoder",
 ]
@@ -124,6 +124,14 @@ def tqd_prefill(handle, seq: int, ids) -> int:
     return nxt.value
 
 
+def tqd_prefill_batch(handle, seq: int, ids) -> int:
+    """The prompt in tiles of up to 16 positions through the batched step."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    nxt = ctypes.c_int32()
+    check(lib().tqd_prefill_batch(handle, seq, ids.ctypes.data, ids.size, ctypes.byref(nxt)), "tqd_prefill_batch")
+    return nxt.value
+
+
 def tqd_kv_upload(handle, seq: int, k, v) -> None:
     """k, v float32 [n_layers, n_pos, kv_width] host arrays."""
     k = np.ascontiguousarray(k, dtype=np.float32)
@@ -200,6 +208,9 @@ class Decoder:
 
     def prefill(self, ids, seq: int = 0) -> int:
         return tqd_prefill(self.handle, seq, ids)
+
+    def prefill_batch(self, ids, seq: int = 0) -> int:
+        return tqd_prefill_batch(self.handle, seq, ids)
 
     def decode_step(self, token: int, pos: int, seq: int = 0) -> int:
         return tqd_decode_step(self.handle, seq, token, pos)

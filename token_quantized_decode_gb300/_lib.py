@@ -73,6 +73,7 @@ def lib():
         "tqd_truncate": (i32, [vp, i32, i32]),
         "tqd_next_pos": (i32, [vp, i32, P(i32)]),
         "tqd_prefill": (i32, [vp, i32, vp, i32, P(i32)]),
+        "tqd_prefill_batch": (i32, [vp, i32, vp, i32, P(i32)]),
         "tqd_kv_upload": (i32, [vp, i32, i32, vp, vp]),
         "tqd_decode_step": (i32, [vp, i32, i32, i32, P(i32)]),
         "tqd_generate": (i32, [vp, i32, i32, i32, vp]),
@@ -108,7 +109,7 @@ def exported_symbols():
     """Names the C ABI declares, in header order."""
     return [
         "tqd_status_name", "tqd_last_error", "tqd_create", "tqd_destroy", "tqd_reset", "tqd_truncate", "tqd_next_pos",
-        "tqd_prefill", "tqd_kv_upload", "tqd_decode_step", "tqd_generate", "tqd_decode_step_batch",
+        "tqd_prefill", "tqd_prefill_batch", "tqd_kv_upload", "tqd_decode_step", "tqd_generate", "tqd_decode_step_batch",
         "tqd_generate_batch", "tqd_read_logits",
         "tqd_phase_count", "tqd_step_bytes", "tqd_op_q8_0_repack", "tqd_op_q8_0_matvec",
         "tqd_op_bf16_matvec", "tqd_op_rmsnorm", "tqd_op_rope_table", "tqd_op_rope", "tqd_op_attention",

@@ -268,6 +268,7 @@ struct MmArgs {
   float* ss_out;        // kEpiResid: [gridDim.x][16] partial sums of squares of the new rows, or nullptr
   const DevSeq* seqs;   // kEpiArgmax: per-sequence logits, candidates, state
   uint32_t* count;      // kEpiArgmax: arrivals of all blocks
+  int out0;             // kEpiArgmax: the first batch row whose logits and next token are kept
   uint32_t* err;
   int max_seq;
   // X given as split-K attention partials instead (nullptr: plain X): per
@@ -923,7 +924,7 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
     for (int i = 0; i < kHdStages; ++i) mbar_init(&full[i], 1);
     fence_mbar_init();
   }
-  if (t < kTcN) s_logits[t] = t < a.n ? a.seqs[t].logits : nullptr;
+  if (t < kTcN) s_logits[t] = t < a.n && t >= a.out0 ? a.seqs[t].logits : nullptr;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_addr(&tmem_base))
                  : "memory");
@@ -1116,7 +1117,7 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
         for (int b = 0; b < kTcN; ++b) {
           const float val = acc[b] * inv_rms[b];
           acc[b] = 0.f;
-          if (b < a.n && row < a.rows) {
+          if (b < a.n && b >= a.out0 && row < a.rows) {
             s_logits[b][row] = val;
             argmax_merge(bv[b], bi[b], val, row);
           }
@@ -1133,7 +1134,7 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
       }
     }
     named_sync(2, kTcM);
-    if (t < a.n) {
+    if (t < a.n && t >= a.out0) {
       float cv = -INFINITY;
       int ci = INT_MAX;
       for (int w = 0; w < kTcM / 32; ++w) argmax_merge(cv, ci, wred_v[w][t], wred_i[w][t]);
@@ -1157,7 +1158,7 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
   }
   __syncthreads();
   if (!s_last) return;
-  for (int q = warp; q < a.n; q += NW) {
+  for (int q = a.out0 + warp; q < a.n; q += NW) {
     const DevSeq& s = a.seqs[q];
     float cv = -INFINITY;
     int ci = INT_MAX;
@@ -1266,9 +1267,13 @@ constexpr uint32_t kASlotBytes = 32 * 1024;
 
 __device__ __forceinline__ void async() { asm volatile("bar.sync 1, %0;" ::"n"(kAT) : "memory"); }
 
+// fresh: the step's own K/V row comes from qkv (normalised, rotated and
+// appended here); otherwise every row up to the position is already in the
+// cache (a prefill tile's rows, appended by k_kv_append_batch) and the
+// producer waits for that kernel before copying.
 template <int HD, int G>
 __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, int g, int c, int nch,
-                                const float* qkv, float* po, float* pml, unsigned char* sm) {
+                                const float* qkv, float* po, float* pml, unsigned char* sm, bool fresh) {
   constexpr int NJ = HD / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kASlots * kASlotBytes);
@@ -1281,13 +1286,14 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
   const int S = static_cast<int>(pos) + 1;
   const int cs = (S + nch - 1) / nch;
   const int t0 = min(S, c * cs), t1 = min(S, t0 + cs);
-  const bool has_new = t0 <= static_cast<int>(pos) && static_cast<int>(pos) < t1;
-  const int tc = min(t1, static_cast<int>(pos));
+  const bool has_new = fresh && t0 <= static_cast<int>(pos) && static_cast<int>(pos) < t1;
+  const int tc = fresh ? min(t1, static_cast<int>(pos)) : t1;
   const int rpp = static_cast<int>(kASlotBytes / (2u * 4u * HD));
   const size_t head = (static_cast<size_t>(layer) * m.nkv + g) * m.max_seq * HD;
   uint32_t* err = &s.state->err;
   if (threadIdx.x == kAT) {
     // producer
+    if (!fresh) pdl_wait();  // this tile's rows are written by the previous kernel
     uint32_t n = 0;
     for (int a0 = t0; a0 < tc; a0 += rpp, ++n) {
       const int cnt = min(rpp, tc - a0);
@@ -1476,9 +1482,41 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
   }
 }
 
+// A prefill tile's K/V rows: for slot b (one block) and kv head g (one warp),
+// k after QK-norm and RoPE at the slot's position, and v, into the cache rows
+// that the attention kernel then reads (the tile's slots attend to each
+// other's rows, so they are written before any slot's attention starts).
+template <int HD>
+__global__ void __launch_bounds__(1024) k_kv_append_batch(DevModel m, const DevSeq* seqs, int layer, const float* QKV) {
+  constexpr int NJ = HD / 32;
+  pdl_wait();  // this layer's QKV projection is complete
+  pdl_launch_dependents();
+  const int b = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (g >= m.nkv) return;
+  const DevSeq& s = seqs[b];
+  const uint32_t pos = s.state->pos;
+  if (pos >= static_cast<uint32_t>(m.max_seq)) return;  // flagged by the embedding
+  const float* qkv = QKV + static_cast<size_t>(b) * (m.qw + 2 * m.kvw);
+  float kv[NJ], vv[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    kv[j] = __ldcg(qkv + m.qw + g * HD + lane + 32 * j);
+    vv[j] = __ldcg(qkv + m.qw + m.kvw + g * HD + lane + 32 * j);
+  }
+  head_norm_rope<HD>(kv, m.qk_norm ? m.layers[layer].k_norm : nullptr, m.rope + static_cast<size_t>(pos) * (HD / 2),
+                     m.eps);
+  const size_t r = ((static_cast<size_t>(layer) * m.nkv + g) * m.max_seq + pos) * HD;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    s.kcache[r + lane + 32 * j] = kv[j];
+    s.vcache[r + lane + 32 * j] = vv[j];
+  }
+}
+
 template <int HD, int G>
 __global__ void __launch_bounds__(kAT + 32, 2)
-    k_attn_batch(DevModel m, const DevSeq* seqs, int layer, int nch, const float* QKV, float* PO, float* PML) {
+    k_attn_batch(DevModel m, const DevSeq* seqs, int layer, int nch, const float* QKV, float* PO, float* PML,
+                 int fresh) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int per_seq = m.nkv * nch;
   const int b = blockIdx.x / per_seq, item = blockIdx.x - b * per_seq;
@@ -1497,7 +1535,7 @@ __global__ void __launch_bounds__(kAT + 32, 2)
   const float* qkv = QKV + static_cast<size_t>(b) * (m.qw + 2 * m.kvw);
   float* po = PO + static_cast<size_t>(b) * m.nq * nch * HD;
   float* pml = PML + static_cast<size_t>(b) * m.nq * nch * 2;
-  attn_batch_item<HD, G>(m, s, layer, g, c, nch, qkv, po, pml, sm);
+  attn_batch_item<HD, G>(m, s, layer, g, c, nch, qkv, po, pml, sm, fresh != 0);
 }
 
 // The attention kernel instantiated for the model's head_dim and group size.
@@ -1547,7 +1585,7 @@ int batch_ss_slots(int H) { return ((H + kTcM - 1) / kTcM) * kMaxCluster; }
 bool batch_supported(const DevModel& m) {
   const int G = m.nq / m.nkv;
   auto split_ok = [](int K) { return K % 64 == 0 && mm_cluster(K, kTcM, 1) > 0; };
-  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && split_ok(m.H) && split_ok(m.qw) &&
+  return G >= 1 && G <= 4 && m.nkv <= 32 && (m.hd == 64 || m.hd == 128) && split_ok(m.H) && split_ok(m.qw) &&
          split_ok(m.I) && m.H <= kHeadMaxK && attn_batch_smem(m) <= 227 * 1024;
 }
 
@@ -1571,6 +1609,29 @@ __global__ void k_batch_tokens_out(const DevSeq* seqs, int n, int32_t* out) {
   }
 }
 
+// A prefill tile: slot b is the sequence at position p0 + b, p0 being the
+// sequence's next position.  slots[0 .. kTcN) share the sequence's tokens and
+// KV cache, each with a state word of its own; slots[kTcN] is the sequence.
+__global__ void k_prefill_tile_begin(const DevSeq* slots, int n) {
+  const int b = static_cast<int>(threadIdx.x);
+  if (b < n) slots[b].state->pos = slots[kTcN].state->pos + static_cast<uint32_t>(b);
+}
+
+// After a tile: the sequence advances by n positions and takes over the
+// slots' error bits.
+__global__ void k_prefill_tile_end(const DevSeq* slots, int n) {
+  if (threadIdx.x != 0) return;
+  DevState* seq = slots[kTcN].state;
+  uint32_t err = 0u;
+  for (int b = 0; b < n; ++b) {
+    err |= slots[b].state->err;
+    slots[b].state->err = 0u;
+  }
+  seq->err |= err;
+  seq->pos += static_cast<uint32_t>(n);
+  seq->steps += static_cast<uint32_t>(n);
+}
+
 }  // namespace
 
 cudaError_t launch_batch_tokens_in(const DevSeq* seqs, int n, const int32_t* tok, cudaStream_t st) {
@@ -1580,6 +1641,16 @@ cudaError_t launch_batch_tokens_in(const DevSeq* seqs, int n, const int32_t* tok
 
 cudaError_t launch_batch_tokens_out(const DevSeq* seqs, int n, int32_t* out, cudaStream_t st) {
   k_batch_tokens_out<<<1, kTcN, 0, st>>>(seqs, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tile_begin(const DevSeq* slots, int n, cudaStream_t st) {
+  k_prefill_tile_begin<<<1, kTcN, 0, st>>>(slots, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tile_end(const DevSeq* slots, int n, cudaStream_t st) {
+  k_prefill_tile_end<<<1, 32, 0, st>>>(slots, n);
   return cudaGetLastError();
 }
 
@@ -1604,9 +1675,14 @@ cudaError_t batch_setup(const DevModel& m) {
 // [slots][16]).  Every kernel is launched with programmatic dependent launch:
 // it starts streaming its weights (or cached K/V rows) while its predecessor
 // finishes, and waits for it before touching activations.
+// tile: seqs are the slots of one sequence's prefill tile (positions p0 ..
+// p0 + n - 1), which attend to each other's rows: each layer's K/V rows are
+// appended by their own kernel before the attention.  out0: the first slot
+// whose logits and argmax are produced; out0 >= n skips the lm_head.
 cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const uint8_t* lm_tiled,
                                const DevSeq* seqs, int n, int nch, float* X, float* QKV, float* PO, float* PML,
-                               float* H, float* SS, uint32_t* count, uint32_t* err, cudaStream_t st) {
+                               float* H, float* SS, uint32_t* count, uint32_t* err, cudaStream_t st, bool tile,
+                               int out0) {
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1648,7 +1724,7 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
     a.cs = split ? mm_cluster(K, rows, num_sms) : 1;
     a.X = Xin; a.ldx = ldx; a.n = n; a.gain = gain; a.ss = ss; a.nss = nss; a.eps = m.eps;
     a.epi = epi; a.Y = Y; a.ldy = ldy; a.ss_out = ss_out;
-    a.seqs = seqs; a.count = count; a.err = err; a.max_seq = m.max_seq;
+    a.seqs = seqs; a.count = count; a.err = err; a.max_seq = m.max_seq; a.out0 = out0;
     a.pf = pf;
     a.pf_bytes = pf_bytes;
     if (from_parts) {  // X is the attention's chunk partials, merged while B is built
@@ -1669,15 +1745,21 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
     if ((e = mm(L.wqkv, m.row_bytes_h, m.H, lqkv, X, m.H, L.attn_norm, ss_x, nss_x, kEpiStore, QKV, lqkv,
                 nullptr, true)) != cudaSuccess)
       return e;
+    if (tile) {
+      cudaLaunchConfig_t cp = config(n, 32 * m.nkv, 0, 1);
+      e = m.hd == 128 ? cudaLaunchKernelEx(&cp, k_kv_append_batch<128>, m, seqs, l, static_cast<const float*>(QKV))
+                      : cudaLaunchKernelEx(&cp, k_kv_append_batch<64>, m, seqs, l, static_cast<const float*>(QKV));
+      if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t ca = config(n * m.nkv * nch, kAT + 32, attn_batch_smem(m), 1);
     {
       DevModel mm_ = m;
       const DevSeq* sq = seqs;
-      int layer = l, nc = nch;
+      int layer = l, nc = nch, fresh = tile ? 0 : 1;
       const float* q = QKV;
       float* po = PO;
       float* pml = PML;
-      void* args[] = {&mm_, &sq, &layer, &nc, &q, &po, &pml};
+      void* args[] = {&mm_, &sq, &layer, &nc, &q, &po, &pml, &fresh};
       if ((e = cudaLaunchKernelExC(&ca, attn_fn, args)) != cudaSuccess) return e;
     }
     if ((e = mm(L.wo, m.row_bytes_qw, m.qw, m.H, nullptr, m.qw, nullptr, nullptr, 0, kEpiResid, X, m.H, ss_mid,
@@ -1691,6 +1773,7 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
                 more ? host_layers[l + 1].wqkv : nullptr, more ? m.row_bytes_h * lqkv : 0)) != cudaSuccess)
       return e;
   }
+  if (out0 >= n) return cudaSuccess;
   return mm(lm_tiled, m.row_bytes_h, m.H, m.V, X, m.H, m.out_norm, ss_x, nss_x, kEpiArgmax, nullptr, 0,
             nullptr, false);
 }

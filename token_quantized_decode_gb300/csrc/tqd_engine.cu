@@ -78,6 +78,13 @@ struct tqd_model {
   int32_t* bio = nullptr;  // a batched step's tokens in [16], argmax out and error words [2 x 16]
   int batch_nch = 1;
   cudaGraphExec_t bgraph[17] = {};
+  // prefill tiles: batch_max() slot descriptors and the sequence's own (the
+  // device copy and its host image), the slots' state words, and one graph per
+  // (tile size, whether the tile ends the prompt)
+  DevSeq* pslots = nullptr;
+  std::vector<DevSeq> pslots_host;
+  DevState* pstates = nullptr;
+  cudaGraphExec_t pgraph[17][2] = {};
 };
 
 namespace {
@@ -337,6 +344,9 @@ void tqd_destroy(tqd_model* m) {
   }
   for (cudaGraphExec_t& g : m->bgraph)
     if (g) cudaGraphExecDestroy(g);
+  for (auto& row : m->pgraph)
+    for (cudaGraphExec_t& g : row)
+      if (g) cudaGraphExecDestroy(g);
   if (m->arena) cudaFree(m->arena);
   if (m->h_tokens) cudaFreeHost(m->h_tokens);
   if (m->h_state) cudaFreeHost(m->h_state);
@@ -461,11 +471,15 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].gbar = take(sizeof(DevBarrier) * 16 * nkv);  // two per group, 128 bytes apart
     so[b].opart = take(4ull * nkv * H);
   }
-  // batched-step buffers (only for models holding several sequences)
+  // batched-step buffers (several sequences per step, or a prompt's tiles),
+  // for every shape the batched kernels support
   const int bmax = batch_max();
   size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0, o_blm = 0,
-         o_bio = 0;
-  if (cfg->max_batch > 1) {
+         o_bio = 0, o_pslots = 0, o_pstates = 0;
+  DevModel shape{};
+  shape.H = H; shape.nq = nq; shape.nkv = nkv; shape.hd = hd; shape.I = I; shape.qw = qw;
+  const bool batched = batch_supported(shape) && (V + 127) / 128 <= kMaxArgmaxBlocks;
+  if (batched) {
     o_bx = take(4ull * bmax * H);
     o_bqkv = take(4ull * bmax * (qw + 2 * kvw));
     o_bpo = take(4ull * bmax * nq * nch * hd);  // attention chunk partials (at most n_chunks chunks)
@@ -476,6 +490,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     o_bss = take(4ull * 2 * batch_ss_slots(H) * bmax);
     o_blm = take(batch_head_bytes(V, H, fmt));
     o_bio = take(4ull * 3 * bmax);
+    o_pslots = take(sizeof(DevSeq) * (bmax + 1));
+    o_pstates = take(sizeof(DevState) * bmax);
   }
   m->arena_bytes = off;
   cudaError_t ce = cudaMalloc(&m->arena, m->arena_bytes);
@@ -597,7 +613,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     if (tmp) cudaFree(tmp);
     return fail(e, "upload head weights");
   }
-  if (cfg->max_batch > 1 &&
+  if (batched &&
       ((e = launch_head_tile(base + o_lm, rbh, V, H, fmt, base + o_blm, st)) != cudaSuccess ||
        (e = cudaStreamSynchronize(st)) != cudaSuccess)) {
     if (tmp) cudaFree(tmp);
@@ -644,7 +660,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.gbar = reinterpret_cast<DevBarrier*>(base + so[b].gbar);
     d.opart = reinterpret_cast<float*>(base + so[b].opart);
   }
-  if (cfg->max_batch > 1 && batch_supported(dm) && (V + 127) / 128 <= kMaxArgmaxBlocks) {
+  if (batched) {
     m->bx = reinterpret_cast<float*>(base + o_bx);
     m->bqkv = reinterpret_cast<float*>(base + o_bqkv);
     m->bpo = reinterpret_cast<float*>(base + o_bpo);
@@ -655,6 +671,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     m->bss = reinterpret_cast<float*>(base + o_bss);
     m->blm = base + o_blm;
     m->bio = reinterpret_cast<int32_t*>(base + o_bio);
+    m->pslots = reinterpret_cast<DevSeq*>(base + o_pslots);
+    m->pstates = reinterpret_cast<DevState*>(base + o_pstates);
     std::vector<DevSeq> hs(cfg->max_batch);
     for (int b = 0; b < cfg->max_batch; ++b) hs[b] = m->seqs[b].d;
     if ((e = cudaMemcpy(m->dseqs, hs.data(), sizeof(DevSeq) * cfg->max_batch,
@@ -850,7 +868,7 @@ namespace {
 int32_t check_batch(tqd_model* m, int32_t n_seq) {
   int32_t rc = check_model(m, 0);
   if (rc) return rc;
-  if (!m->batch_ok) {
+  if (!m->batch_ok || m->cfg.max_batch < 2) {
     set_error("this model has no batched step (max_batch must be > 1 and the shape supported)");
     return TQD_ERR_UNSUPPORTED_CONFIG;
   }
@@ -875,7 +893,7 @@ int32_t run_batch(tqd_model* m, int n, int steps) {
     CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
     cudaError_t e = enqueue_batch_step(m->dm, m->host_layers.data(), m->blm, m->dseqs, n, nch, m->bx, m->bqkv,
                                        m->bpo, m->bpml, m->bh, m->bss, m->bcount, &m->seqs[0].d.state->err,
-                                       m->stream);
+                                       m->stream, false, 0);
     cudaError_t e2 = cudaStreamEndCapture(m->stream, &graph);
     if (e != cudaSuccess) {
       if (graph) cudaGraphDestroy(graph);
@@ -887,6 +905,38 @@ int32_t run_batch(tqd_model* m, int n, int steps) {
     if (e != cudaSuccess) return fail_cuda(m, e, "instantiate batched graph");
   }
   for (int i = 0; i < steps; ++i) CK(cudaGraphLaunch(g, m->stream), "batched graph launch");
+  return TQD_OK;
+}
+
+// Enqueue one prefill tile of n positions for the sequence in m->pslots:
+// slot positions, the batched step in tile mode (the lm_head on the last
+// slot only where the tile ends the prompt), the sequence's advance.  One
+// graph per (n, last).
+int32_t run_prefill_tile(tqd_model* m, int n, bool last) {
+  cudaGraphExec_t& g = m->pgraph[n][last ? 1 : 0];
+  if (!g) {
+    int nch = 2 * m->num_sms / (n * m->dm.nkv);
+    if (nch > m->dm.n_chunks) nch = m->dm.n_chunks;
+    if (nch < 1) nch = 1;
+    cudaGraph_t graph = nullptr;
+    CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
+    cudaError_t e = launch_prefill_tile_begin(m->pslots, n, m->stream);
+    if (e == cudaSuccess)
+      e = enqueue_batch_step(m->dm, m->host_layers.data(), m->blm, m->pslots, n, nch, m->bx, m->bqkv, m->bpo,
+                             m->bpml, m->bh, m->bss, m->bcount, &m->pstates[0].err, m->stream, true,
+                             last ? n - 1 : n);
+    if (e == cudaSuccess) e = launch_prefill_tile_end(m->pslots, n, m->stream);
+    cudaError_t e2 = cudaStreamEndCapture(m->stream, &graph);
+    if (e != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      return fail_cuda(m, e, "capture prefill tile");
+    }
+    if (e2 != cudaSuccess) return fail_cuda(m, e2, "end capture");
+    e = cudaGraphInstantiate(&g, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail_cuda(m, e, "instantiate prefill tile");
+  }
+  CK(cudaGraphLaunch(g, m->stream), "prefill tile launch");
   return TQD_OK;
 }
 
@@ -979,6 +1029,49 @@ int32_t tqd_generate_batch(tqd_model* m, int32_t n_seq, const int32_t* first_tok
   }
   if ((rc = finish_batch(m, n_seq))) return rc;
   for (int b = 0; b < n_seq; ++b) m->seqs[b].next_pos += n_steps;
+  return TQD_OK;
+}
+
+int32_t tqd_prefill_batch(tqd_model* m, int32_t seq, const int32_t* ids, int32_t n, int32_t* next_out) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!m->batch_ok) {
+    set_error("this model's shape has no batched step, so no prefill tiles");
+    return TQD_ERR_UNSUPPORTED_CONFIG;
+  }
+  if (!ids || !next_out || n <= 0) {
+    set_error("prefill_batch needs ids, next_out and n > 0");
+    return TQD_ERR_BAD_ARG;
+  }
+  SeqSlot& s = m->seqs[seq];
+  const int32_t pos = s.next_pos;
+  if (static_cast<int64_t>(pos) + n > m->cfg.max_seq) {
+    set_error("prefill of %d tokens at position %d exceeds max_seq %d", n, pos, m->cfg.max_seq);
+    return TQD_ERR_CAPACITY;
+  }
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= m->cfg.vocab) {
+      set_error("token id %d at index %d outside the vocabulary", ids[i], i);
+      return TQD_ERR_BAD_ARG;
+    }
+  const int bmax = batch_max();
+  // the tile slots: the sequence's descriptor with a state word of their own
+  m->pslots_host.assign(bmax + 1, s.d);
+  for (int b = 0; b < bmax; ++b) m->pslots_host[b].state = m->pstates + b;
+  CK(cudaMemcpyAsync(m->pslots, m->pslots_host.data(), sizeof(DevSeq) * (bmax + 1), cudaMemcpyHostToDevice,
+                     m->stream),
+     "upload tile slots");
+  memcpy(m->h_tokens, ids, 4ull * n);
+  CK(cudaMemcpyAsync(s.d.tokens + pos, m->h_tokens, 4ull * n, cudaMemcpyHostToDevice, m->stream), "upload prompt");
+  for (int done = 0; done < n;) {
+    const int t = std::min(bmax, n - done);
+    if ((rc = run_prefill_tile(m, t, done + t == n))) return rc;
+    done += t;
+  }
+  CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + pos + n, 4, cudaMemcpyDeviceToHost, m->stream), "read next token");
+  if ((rc = finish(m, s))) return rc;
+  s.next_pos = pos + n;
+  *next_out = m->h_tokens[0];
   return TQD_OK;
 }
 

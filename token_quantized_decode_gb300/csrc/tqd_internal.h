@@ -110,10 +110,19 @@ cudaError_t launch_head_tile(const uint8_t* rows_src, size_t rb, int rows, int K
 // error word after the step (out[b], out[n + b]).
 cudaError_t launch_batch_tokens_in(const DevSeq* seqs, int n, const int32_t* tok, cudaStream_t st);
 cudaError_t launch_batch_tokens_out(const DevSeq* seqs, int n, int32_t* out, cudaStream_t st);
+// A prefill tile's slot positions (slot b at the sequence's next position + b)
+// before the tile, and after it the sequence's advance by n and the slots'
+// error bits.  slots: batch_max() + 1 descriptors, the last the sequence's own.
+cudaError_t launch_prefill_tile_begin(const DevSeq* slots, int n, cudaStream_t st);
+cudaError_t launch_prefill_tile_end(const DevSeq* slots, int n, cudaStream_t st);
 // PO / PML: the attention's chunk partials, [n][nq][nch][hd] and [n][nq][nch][2].
+// tile: seqs are the slots of one sequence's prefill tile (K/V rows appended
+// before the attention); out0: the first slot whose logits and argmax are
+// produced (0 for a decode step; >= n skips the lm_head).
 cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, const uint8_t* lm_tiled,
                                const DevSeq* seqs, int n, int nch, float* X, float* QKV, float* PO, float* PML,
-                               float* H, float* SS, uint32_t* count, uint32_t* err, cudaStream_t st);
+                               float* H, float* SS, uint32_t* count, uint32_t* err, cudaStream_t st, bool tile,
+                               int out0);
 
 // The bounded-wait self-test (tqd_op_wait_selftest): runs it on st and
 // returns the error bits its waits set.
