@@ -51,7 +51,8 @@ typedef enum tqd_status {
   TQD_ERR_POS_MISMATCH = 7,        /* pos is not the sequence's next position */
   TQD_ERR_DEVICE_TIMEOUT = 8,      /* a bounded device-side wait gave up (model poisoned) */
   TQD_ERR_NUMERIC = 9,             /* every logit was NaN: no argmax exists */
-  TQD_ERR_POISONED = 10            /* an earlier fatal error; only tqd_destroy is valid */
+  TQD_ERR_POISONED = 10,           /* an earlier fatal error; only tqd_destroy is valid */
+  TQD_ERR_NOT_PREFILLED = 11       /* no step has produced logits for the sequence's next position */
 } tqd_status;
 
 enum { TQD_WEIGHT_Q8_0 = 0, TQD_WEIGHT_BF16 = 1 };
@@ -209,6 +210,50 @@ int32_t tqd_decode_step_batch(tqd_model* model, int32_t n_seq, const int32_t* to
  * receives step i's id of sequence b. */
 int32_t tqd_generate_batch(tqd_model* model, int32_t n_seq, const int32_t* first_tokens,
                            int32_t n_steps, int32_t* ids_out);
+
+/* Controls of seeded sampling ("Metal LLM decode", the sampled arm of the
+ * batched prefill+decode section, which names them and fixes that
+ * temperature <= 0 falls back to the greedy token and top_k = 1 reproduces
+ * it).  The draw, in this order: the penalties on the distinct tokens among
+ * the sequence's inputs so far (count c): l = l > 0 ? l / repeat : l * repeat,
+ * then l -= presence, then l -= frequency * c; z = l / temperature; top_k
+ * keeps the top_k largest z (ties to the lower index); top_p keeps, of those
+ * in the order (z descending, index ascending), the shortest prefix whose
+ * probability reaches top_p of their total; min_p keeps z - z_max >=
+ * ln(min_p); the token is drawn from the kept probabilities exp(z - z_max)
+ * by inverting their running sum in index order at u = the top 24 bits of
+ * splitmix64's output number `position` from `seed`, times 2^-24, where
+ * position is the drawn token's position.  Every float step is f32; the
+ * probabilities are summed as integers in units of 2^-32 of the most likely
+ * token's, so a draw is deterministic. */
+typedef struct tqd_sampling {
+  float temperature;        /* <= 0: the greedy token */
+  int32_t top_k;            /* 0: off; 1: the greedy token of the penalised logits */
+  float top_p;              /* (0, 1]; 1: off */
+  float min_p;              /* [0, 1]; 0: off */
+  float repeat_penalty;     /* > 0; 1: off */
+  float presence_penalty;   /* 0: off */
+  float frequency_penalty;  /* 0: off */
+  uint64_t seed;
+} tqd_sampling;
+
+/* Draw the token for sequence seq's next position from its last step's
+ * logits (after a prefill or a decode step) and make it the sequence's input
+ * there; *token_out receives it.  Errors: BAD_ARG (controls out of range,
+ * non-finite), NOT_PREFILLED (no logits for the next position: nothing run
+ * since create, reset, truncate or kv_upload). */
+int32_t tqd_sample(tqd_model* model, int32_t seq, const tqd_sampling* sampling, int32_t* token_out);
+
+/* As tqd_generate, with every step's token drawn under `sampling` instead of
+ * the argmax, on the device (one sampling block after each step; no host
+ * round trip between steps). */
+int32_t tqd_generate_sampled(tqd_model* model, int32_t seq, int32_t first_token, int32_t n_steps,
+                             const tqd_sampling* sampling, int32_t* ids_out);
+
+/* As tqd_generate_batch, with every sequence's token drawn under `sampling`
+ * (one sampling block per sequence after each batched step). */
+int32_t tqd_generate_batch_sampled(tqd_model* model, int32_t n_seq, const int32_t* first_tokens,
+                                   int32_t n_steps, const tqd_sampling* sampling, int32_t* ids_out);
 
 /* Copy the logits of sequence seq's last step (f32 [vocab]) to host_out.
  * A debugging and parity hook, off the decode path ("One command buffer per

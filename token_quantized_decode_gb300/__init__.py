@@ -13,13 +13,14 @@ import ctypes
 import numpy as np
 
 from ._lib import (TQD_SCHED_GRAPH, TQD_SCHED_PERSISTENT, TQD_WEIGHT_BF16, TQD_WEIGHT_Q8_0, TQDError,
-                   check, lib, tqd_config, tqd_host_weights, tqd_layer_weights)
+                   check, lib, tqd_config, tqd_host_weights, tqd_layer_weights, tqd_sampling)
 
 __all__ = [
     "TQDError", "TQD_SCHED_GRAPH", "TQD_SCHED_PERSISTENT", "TQD_WEIGHT_Q8_0", "TQD_WEIGHT_BF16",
     "make_config", "make_host_weights", "tqd_status_name", "tqd_create", "tqd_destroy", "tqd_reset",
     "tqd_truncate", "tqd_next_pos", "tqd_prefill", "tqd_prefill_batch", "tqd_kv_upload", "tqd_decode_step", "tqd_generate",
-    "tqd_decode_step_batch", "tqd_generate_batch", "tqd_read_logits", "tqd_phase_count", "tqd_step_bytes",
+    "tqd_decode_step_batch", "tqd_generate_batch", "tqd_sample", "tqd_generate_sampled",
+    "tqd_generate_batch_sampled", "sampling", "tqd_read_logits", "tqd_phase_count", "tqd_step_bytes",
     "Decoder",
 ]
 
@@ -169,6 +170,36 @@ def tqd_generate_batch(handle, first_tokens, n_steps: int) -> np.ndarray:
     return out
 
 
+def sampling(temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0, min_p: float = 0.0,
+             repeat_penalty: float = 1.0, presence_penalty: float = 0.0, frequency_penalty: float = 0.0,
+             seed: int = 0) -> tqd_sampling:
+    """The controls of seeded sampling (neutral values switch a stage off)."""
+    return tqd_sampling(temperature, top_k, top_p, min_p, repeat_penalty, presence_penalty, frequency_penalty,
+                        seed & ((1 << 64) - 1))
+
+
+def tqd_sample(handle, seq: int, params: tqd_sampling) -> int:
+    tok = ctypes.c_int32()
+    check(lib().tqd_sample(handle, seq, ctypes.byref(params), ctypes.byref(tok)), "tqd_sample")
+    return tok.value
+
+
+def tqd_generate_sampled(handle, seq: int, first_token: int, n_steps: int, params: tqd_sampling) -> np.ndarray:
+    out = np.empty(n_steps, dtype=np.int32)
+    check(lib().tqd_generate_sampled(handle, seq, first_token, n_steps, ctypes.byref(params), out.ctypes.data),
+          "tqd_generate_sampled")
+    return out
+
+
+def tqd_generate_batch_sampled(handle, first_tokens, n_steps: int, params: tqd_sampling) -> np.ndarray:
+    """Returns ids [n_steps, n_seq]."""
+    first = np.ascontiguousarray(first_tokens, dtype=np.int32)
+    out = np.empty((n_steps, first.size), dtype=np.int32)
+    check(lib().tqd_generate_batch_sampled(handle, first.size, first.ctypes.data, int(n_steps),
+                                           ctypes.byref(params), out.ctypes.data), "tqd_generate_batch_sampled")
+    return out
+
+
 def tqd_read_logits(handle, seq: int, vocab: int, out=None) -> np.ndarray:
     logits = out if out is not None else np.empty(vocab, dtype=np.float32)
     check(lib().tqd_read_logits(handle, seq, logits.ctypes.data), "tqd_read_logits")
@@ -223,6 +254,15 @@ class Decoder:
 
     def generate_batch(self, first_tokens, n_steps: int) -> np.ndarray:
         return tqd_generate_batch(self.handle, first_tokens, n_steps)
+
+    def sample(self, params: tqd_sampling, seq: int = 0) -> int:
+        return tqd_sample(self.handle, seq, params)
+
+    def generate_sampled(self, first_token: int, n_steps: int, params: tqd_sampling, seq: int = 0) -> np.ndarray:
+        return tqd_generate_sampled(self.handle, seq, first_token, n_steps, params)
+
+    def generate_batch_sampled(self, first_tokens, n_steps: int, params: tqd_sampling) -> np.ndarray:
+        return tqd_generate_batch_sampled(self.handle, first_tokens, n_steps, params)
 
     def logits(self, seq: int = 0) -> np.ndarray:
         return tqd_read_logits(self.handle, seq, self.cfg.vocab)

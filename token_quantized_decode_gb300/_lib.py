@@ -15,7 +15,7 @@ TQD_OK = 0
 STATUS_NAMES = [
     "TQD_OK", "TQD_ERR_BAD_ARG", "TQD_ERR_UNSUPPORTED_CONFIG", "TQD_ERR_NO_DEVICE", "TQD_ERR_CUDA",
     "TQD_ERR_OOM", "TQD_ERR_CAPACITY", "TQD_ERR_POS_MISMATCH", "TQD_ERR_DEVICE_TIMEOUT",
-    "TQD_ERR_NUMERIC", "TQD_ERR_POISONED",
+    "TQD_ERR_NUMERIC", "TQD_ERR_POISONED", "TQD_ERR_NOT_PREFILLED",
 ]
 for _i, _n in enumerate(STATUS_NAMES):
     globals()[_n] = _i
@@ -41,6 +41,13 @@ class tqd_layer_weights(ctypes.Structure):
 class tqd_host_weights(ctypes.Structure):
     _fields_ = [("layers", ctypes.POINTER(tqd_layer_weights)), ("out_norm", ctypes.c_void_p),
                 ("lm_head", ctypes.c_void_p), ("embed", ctypes.c_void_p)]
+
+
+class tqd_sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+                ("min_p", ctypes.c_float), ("repeat_penalty", ctypes.c_float),
+                ("presence_penalty", ctypes.c_float), ("frequency_penalty", ctypes.c_float),
+                ("seed", ctypes.c_uint64)]
 
 
 class TQDError(RuntimeError):
@@ -79,6 +86,9 @@ def lib():
         "tqd_generate": (i32, [vp, i32, i32, i32, vp]),
         "tqd_decode_step_batch": (i32, [vp, i32, vp, vp, vp]),
         "tqd_generate_batch": (i32, [vp, i32, vp, i32, vp]),
+        "tqd_sample": (i32, [vp, i32, P(tqd_sampling), P(i32)]),
+        "tqd_generate_sampled": (i32, [vp, i32, i32, i32, P(tqd_sampling), vp]),
+        "tqd_generate_batch_sampled": (i32, [vp, i32, vp, i32, P(tqd_sampling), vp]),
         "tqd_read_logits": (i32, [vp, i32, vp]),
         "tqd_phase_count": (i32, [vp, P(i32)]),
         "tqd_step_bytes": (i32, [vp, i32, P(i64)]),
@@ -110,7 +120,8 @@ def exported_symbols():
     return [
         "tqd_status_name", "tqd_last_error", "tqd_create", "tqd_destroy", "tqd_reset", "tqd_truncate", "tqd_next_pos",
         "tqd_prefill", "tqd_prefill_batch", "tqd_kv_upload", "tqd_decode_step", "tqd_generate", "tqd_decode_step_batch",
-        "tqd_generate_batch", "tqd_read_logits",
+        "tqd_generate_batch", "tqd_sample", "tqd_generate_sampled", "tqd_generate_batch_sampled",
+        "tqd_read_logits",
         "tqd_phase_count", "tqd_step_bytes", "tqd_op_q8_0_repack", "tqd_op_q8_0_matvec",
         "tqd_op_bf16_matvec", "tqd_op_rmsnorm", "tqd_op_rope_table", "tqd_op_rope", "tqd_op_attention",
         "tqd_attention_scratch_bytes", "tqd_op_wait_selftest", "tqd_op_silu_mul", "tqd_op_argmax", "tqd_argmax_scratch_bytes",

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtqd.so")
 
-SOURCES = ["tqd_kernels.cu", "tqd_persist.cu", "tqd_engine.cu", "tqd_ops.cu", "tqd_noalloc.cu", "tqd_batch.cu"]
+SOURCES = ["tqd_kernels.cu", "tqd_persist.cu", "tqd_engine.cu", "tqd_ops.cu", "tqd_noalloc.cu", "tqd_batch.cu",
+           "tqd_sample.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]

@@ -44,6 +44,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct SeqSlot {
   DevSeq d{};
   int32_t next_pos = 0;
+  int32_t logits_pos = -1;  // next_pos when the logits buffer was last written (they predict it)
   cudaGraphExec_t g_full = nullptr;
   cudaGraphExec_t g_layers = nullptr;
 };
@@ -329,6 +330,7 @@ const char* tqd_status_name(int32_t s) {
     case TQD_ERR_DEVICE_TIMEOUT: return "TQD_ERR_DEVICE_TIMEOUT";
     case TQD_ERR_NUMERIC: return "TQD_ERR_NUMERIC";
     case TQD_ERR_POISONED: return "TQD_ERR_POISONED";
+    case TQD_ERR_NOT_PREFILLED: return "TQD_ERR_NOT_PREFILLED";
     default: return "TQD_UNKNOWN_STATUS";
   }
 }
@@ -447,7 +449,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const size_t o_rope = take(sizeof(float2) * static_cast<size_t>(S) * (hd / 2));
   const size_t o_layers = take(sizeof(DevLayer) * L);
   const size_t weights_end = off;
-  struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar, gbar, opart; };
+  struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar, gbar,
+                  opart, sz, scnt; };
   std::vector<SeqOff> so(cfg->max_batch);
   const size_t kv_bytes = sizeof(float) * static_cast<size_t>(L) * S * kvw;
   for (int b = 0; b < cfg->max_batch; ++b) {
@@ -470,12 +473,15 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].bar = take(sizeof(DevBarrier));
     so[b].gbar = take(sizeof(DevBarrier) * 16 * nkv);  // two per group, 128 bytes apart
     so[b].opart = take(4ull * nkv * H);
+    so[b].sz = take(4 * static_cast<size_t>(V));
+    so[b].scnt = take(4 * static_cast<size_t>(V));
   }
+  const size_t o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);  // the descriptors, for kernels over sequences
   // batched-step buffers (several sequences per step, or a prompt's tiles),
   // for every shape the batched kernels support
   const int bmax = batch_max();
-  size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_dseqs = 0, o_bcount = 0, o_bss = 0, o_blm = 0,
-         o_bio = 0, o_pslots = 0, o_pstates = 0;
+  size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_bcount = 0, o_bss = 0, o_blm = 0, o_bio = 0,
+         o_pslots = 0, o_pstates = 0;
   DevModel shape{};
   shape.H = H; shape.nq = nq; shape.nkv = nkv; shape.hd = hd; shape.I = I; shape.qw = qw;
   const bool batched = batch_supported(shape) && (V + 127) / 128 <= kMaxArgmaxBlocks;
@@ -485,7 +491,6 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     o_bpo = take(4ull * bmax * nq * nch * hd);  // attention chunk partials (at most n_chunks chunks)
     o_bpml = take(4ull * bmax * nq * nch * 2);
     o_bh = take(4ull * bmax * I);
-    o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);
     o_bcount = take(4);
     o_bss = take(4ull * 2 * batch_ss_slots(H) * bmax);
     o_blm = take(batch_head_bytes(V, H, fmt));
@@ -659,6 +664,16 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.bar = reinterpret_cast<DevBarrier*>(base + so[b].bar);
     d.gbar = reinterpret_cast<DevBarrier*>(base + so[b].gbar);
     d.opart = reinterpret_cast<float*>(base + so[b].opart);
+    d.sz = reinterpret_cast<float*>(base + so[b].sz);
+    d.scnt = reinterpret_cast<uint32_t*>(base + so[b].scnt);
+  }
+  m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
+  {
+    std::vector<DevSeq> hs(cfg->max_batch);
+    for (int b = 0; b < cfg->max_batch; ++b) hs[b] = m->seqs[b].d;
+    if ((e = cudaMemcpy(m->dseqs, hs.data(), sizeof(DevSeq) * cfg->max_batch, cudaMemcpyHostToDevice)) !=
+        cudaSuccess)
+      return fail(e, "upload sequence descriptors");
   }
   if (batched) {
     m->bx = reinterpret_cast<float*>(base + o_bx);
@@ -666,19 +681,13 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     m->bpo = reinterpret_cast<float*>(base + o_bpo);
     m->bpml = reinterpret_cast<float*>(base + o_bpml);
     m->bh = reinterpret_cast<float*>(base + o_bh);
-    m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
     m->bcount = reinterpret_cast<uint32_t*>(base + o_bcount);
     m->bss = reinterpret_cast<float*>(base + o_bss);
     m->blm = base + o_blm;
     m->bio = reinterpret_cast<int32_t*>(base + o_bio);
     m->pslots = reinterpret_cast<DevSeq*>(base + o_pslots);
     m->pstates = reinterpret_cast<DevState*>(base + o_pstates);
-    std::vector<DevSeq> hs(cfg->max_batch);
-    for (int b = 0; b < cfg->max_batch; ++b) hs[b] = m->seqs[b].d;
-    if ((e = cudaMemcpy(m->dseqs, hs.data(), sizeof(DevSeq) * cfg->max_batch,
-                        cudaMemcpyHostToDevice)) != cudaSuccess ||
-        (e = batch_setup(dm)) != cudaSuccess)
-      return fail(e, "batched-step set-up");
+    if ((e = batch_setup(dm)) != cudaSuccess) return fail(e, "batched-step set-up");
     m->batch_ok = true;
   }
   m->blocks_qkv = matvec_blocks(fmt, qw + 2 * kvw, H, m->num_sms, 0);
@@ -708,6 +717,7 @@ int32_t tqd_reset(tqd_model* m, int32_t seq) {
   CK(cudaMemsetAsync(s.d.state, 0, sizeof(DevState), m->stream), "reset state");
   CK(cudaStreamSynchronize(m->stream), "synchronize");
   s.next_pos = 0;
+  s.logits_pos = -1;
   return TQD_OK;
 }
 
@@ -725,6 +735,7 @@ int32_t tqd_truncate(tqd_model* m, int32_t seq, int32_t n_pos) {
   CK(cudaMemcpyAsync(s.d.state, m->h_state, sizeof(DevState), cudaMemcpyHostToDevice, m->stream),
      "set position");
   CK(cudaStreamSynchronize(m->stream), "synchronize");
+  if (n_pos != s.next_pos) s.logits_pos = -1;
   s.next_pos = n_pos;
   return TQD_OK;
 }
@@ -766,6 +777,7 @@ int32_t tqd_prefill(tqd_model* m, int32_t seq, const int32_t* ids, int32_t n, in
      "read next token");
   if ((rc = finish(m, s))) return rc;
   s.next_pos = pos + n;
+  s.logits_pos = s.next_pos;
   *next_out = m->h_tokens[0];
   return TQD_OK;
 }
@@ -805,6 +817,7 @@ int32_t tqd_kv_upload(tqd_model* m, int32_t seq, int32_t n_pos, const float* k, 
      "set position");
   CK(cudaStreamSynchronize(m->stream), "synchronize");
   s.next_pos = n_pos;
+  s.logits_pos = -1;
   return TQD_OK;
 }
 
@@ -832,12 +845,48 @@ int32_t tqd_decode_step(tqd_model* m, int32_t seq, int32_t token, int32_t pos, i
      "read next token");
   if ((rc = finish(m, s))) return rc;
   s.next_pos = pos + 1;
+  s.logits_pos = s.next_pos;
   *next_out = m->h_tokens[1];
   return TQD_OK;
 }
 
-int32_t tqd_generate(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_steps,
-                     int32_t* ids_out) {
+namespace {
+
+// Check the caller's sampling controls and turn them into kernel arguments;
+// *greedy when the temperature asks for the argmax.
+int32_t sample_args(const tqd_sampling* p, SampleArgs& a, bool* greedy) {
+  if (!p) {
+    set_error("sampling controls are NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  if (!std::isfinite(p->temperature) || !std::isfinite(p->top_p) || !std::isfinite(p->min_p) ||
+      !std::isfinite(p->repeat_penalty) || !std::isfinite(p->presence_penalty) ||
+      !std::isfinite(p->frequency_penalty)) {
+    set_error("sampling controls must be finite");
+    return TQD_ERR_BAD_ARG;
+  }
+  if (p->top_k < 0 || !(p->top_p > 0.f) || p->top_p > 1.f || p->min_p < 0.f || p->min_p > 1.f ||
+      !(p->repeat_penalty > 0.f)) {
+    set_error("sampling controls out of range: top_k >= 0, top_p in (0, 1], min_p in [0, 1], repeat_penalty > 0");
+    return TQD_ERR_BAD_ARG;
+  }
+  *greedy = p->temperature <= 0.f;
+  a.temperature = p->temperature;
+  a.top_k = p->top_k;
+  a.top_p = p->top_p;
+  a.ln_min_p = p->min_p > 0.f ? static_cast<float>(std::log(static_cast<double>(p->min_p))) : -INFINITY;
+  a.repeat = p->repeat_penalty;
+  a.presence = p->presence_penalty;
+  a.frequency = p->frequency_penalty;
+  a.penalize = p->repeat_penalty != 1.f || p->presence_penalty != 0.f || p->frequency_penalty != 0.f;
+  a.seed = p->seed;
+  return TQD_OK;
+}
+
+// n_steps device-chained steps of one sequence; with sa, each step's token is
+// drawn by the sampler instead of the argmax.
+int32_t generate_impl(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_steps, int32_t* ids_out,
+                      const SampleArgs* sa) {
   int32_t rc = check_model(m, seq);
   if (rc) return rc;
   if (!ids_out || n_steps <= 0 || first_token < 0 || first_token >= m->cfg.vocab) {
@@ -853,13 +902,60 @@ int32_t tqd_generate(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_s
   m->h_tokens[0] = first_token;
   CK(cudaMemcpyAsync(s.d.tokens + pos, m->h_tokens, 4, cudaMemcpyHostToDevice, m->stream),
      "write token");
-  if ((rc = run_steps(m, s, n_steps, 0))) return rc;
+  if (!sa) {
+    if ((rc = run_steps(m, s, n_steps, 0))) return rc;
+  } else {
+    for (int i = 0; i < n_steps; ++i) {
+      if ((rc = run_steps(m, s, 1, 0))) return rc;
+      CK(launch_sample(m->dseqs + seq, 1, m->cfg.vocab, m->cfg.max_seq, *sa, m->stream), "sampler launch");
+    }
+  }
   CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + pos + 1, 4ull * n_steps, cudaMemcpyDeviceToHost,
                      m->stream),
      "read tokens");
   if ((rc = finish(m, s))) return rc;
   s.next_pos = pos + n_steps;
+  s.logits_pos = s.next_pos;
   memcpy(ids_out, m->h_tokens, 4ull * n_steps);
+  return TQD_OK;
+}
+
+}  // namespace
+
+int32_t tqd_generate(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_steps, int32_t* ids_out) {
+  return generate_impl(m, seq, first_token, n_steps, ids_out, nullptr);
+}
+
+int32_t tqd_generate_sampled(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_steps,
+                             const tqd_sampling* sampling, int32_t* ids_out) {
+  SampleArgs a{};
+  bool greedy = false;
+  const int32_t rc = sample_args(sampling, a, &greedy);
+  if (rc) return rc;
+  return generate_impl(m, seq, first_token, n_steps, ids_out, greedy ? nullptr : &a);
+}
+
+int32_t tqd_sample(tqd_model* m, int32_t seq, const tqd_sampling* sampling, int32_t* token_out) {
+  int32_t rc = check_model(m, seq);
+  if (rc) return rc;
+  SampleArgs a{};
+  bool greedy = false;
+  if ((rc = sample_args(sampling, a, &greedy))) return rc;
+  if (!token_out) {
+    set_error("token_out is NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  SeqSlot& s = m->seqs[seq];
+  if (s.next_pos == 0 || s.logits_pos != s.next_pos) {
+    set_error("sequence %d has no logits for its next position %d: run a prefill or a step first", seq,
+              s.next_pos);
+    return TQD_ERR_NOT_PREFILLED;
+  }
+  if (!greedy)
+    CK(launch_sample(m->dseqs + seq, 1, m->cfg.vocab, m->cfg.max_seq, a, m->stream), "sampler launch");
+  CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + s.next_pos, 4, cudaMemcpyDeviceToHost, m->stream), "read token");
+  if ((rc = finish(m, s))) return rc;
+  *token_out = m->h_tokens[0];
   return TQD_OK;
 }
 
@@ -988,13 +1084,16 @@ int32_t tqd_decode_step_batch(tqd_model* m, int32_t n_seq, const int32_t* tokens
     if (m->h_tokens[64 + n_seq + b] != 0) return finish_batch(m, n_seq);  // reports and clears the error
   for (int b = 0; b < n_seq; ++b) {
     m->seqs[b].next_pos = pos[b] + 1;
+    m->seqs[b].logits_pos = m->seqs[b].next_pos;
     next_out[b] = m->h_tokens[64 + b];
   }
   return TQD_OK;
 }
 
-int32_t tqd_generate_batch(tqd_model* m, int32_t n_seq, const int32_t* first_tokens, int32_t n_steps,
-                           int32_t* ids_out) {
+namespace {
+
+int32_t generate_batch_impl(tqd_model* m, int32_t n_seq, const int32_t* first_tokens, int32_t n_steps,
+                            int32_t* ids_out, const SampleArgs* sa) {
   int32_t rc = check_batch(m, n_seq);
   if (rc) return rc;
   if (!first_tokens || !ids_out || n_steps <= 0) {
@@ -1018,7 +1117,14 @@ int32_t tqd_generate_batch(tqd_model* m, int32_t n_seq, const int32_t* first_tok
                        cudaMemcpyHostToDevice, m->stream),
        "write token");
   }
-  if ((rc = run_batch(m, n_seq, n_steps))) return rc;
+  if (!sa) {
+    if ((rc = run_batch(m, n_seq, n_steps))) return rc;
+  } else {
+    for (int i = 0; i < n_steps; ++i) {
+      if ((rc = run_batch(m, n_seq, 1))) return rc;
+      CK(launch_sample(m->dseqs, n_seq, m->cfg.vocab, m->cfg.max_seq, *sa, m->stream), "sampler launch");
+    }
+  }
   CK(cudaStreamSynchronize(m->stream), "synchronize");
   for (int b = 0; b < n_seq; ++b) {
     CK(cudaMemcpyAsync(m->h_tokens, m->seqs[b].d.tokens + m->seqs[b].next_pos + 1, 4ull * n_steps,
@@ -1028,8 +1134,27 @@ int32_t tqd_generate_batch(tqd_model* m, int32_t n_seq, const int32_t* first_tok
     for (int i = 0; i < n_steps; ++i) ids_out[static_cast<size_t>(i) * n_seq + b] = m->h_tokens[i];
   }
   if ((rc = finish_batch(m, n_seq))) return rc;
-  for (int b = 0; b < n_seq; ++b) m->seqs[b].next_pos += n_steps;
+  for (int b = 0; b < n_seq; ++b) {
+    m->seqs[b].next_pos += n_steps;
+    m->seqs[b].logits_pos = m->seqs[b].next_pos;
+  }
   return TQD_OK;
+}
+
+}  // namespace
+
+int32_t tqd_generate_batch(tqd_model* m, int32_t n_seq, const int32_t* first_tokens, int32_t n_steps,
+                           int32_t* ids_out) {
+  return generate_batch_impl(m, n_seq, first_tokens, n_steps, ids_out, nullptr);
+}
+
+int32_t tqd_generate_batch_sampled(tqd_model* m, int32_t n_seq, const int32_t* first_tokens, int32_t n_steps,
+                                   const tqd_sampling* sampling, int32_t* ids_out) {
+  SampleArgs a{};
+  bool greedy = false;
+  const int32_t rc = sample_args(sampling, a, &greedy);
+  if (rc) return rc;
+  return generate_batch_impl(m, n_seq, first_tokens, n_steps, ids_out, greedy ? nullptr : &a);
 }
 
 int32_t tqd_prefill_batch(tqd_model* m, int32_t seq, const int32_t* ids, int32_t n, int32_t* next_out) {
@@ -1071,6 +1196,7 @@ int32_t tqd_prefill_batch(tqd_model* m, int32_t seq, const int32_t* ids, int32_t
   CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + pos + n, 4, cudaMemcpyDeviceToHost, m->stream), "read next token");
   if ((rc = finish(m, s))) return rc;
   s.next_pos = pos + n;
+  s.logits_pos = s.next_pos;
   *next_out = m->h_tokens[0];
   return TQD_OK;
 }

@@ -124,6 +124,19 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
                                float* H, float* SS, uint32_t* count, uint32_t* err, cudaStream_t st, bool tile,
                                int out0);
 
+// Seeded sampling (tqd_sample.cu): one block per sequence draws the token for
+// its next position from its last logits and writes it there as the input.
+struct SampleArgs {
+  float temperature;   // > 0
+  int top_k;           // 1 <= top_k < V, else off
+  float top_p;         // < 1, else off
+  float ln_min_p;      // f32(ln(min_p)), -inf when off
+  float repeat, presence, frequency;
+  int penalize;        // any penalty differs from neutral
+  unsigned long long seed;
+};
+cudaError_t launch_sample(const DevSeq* seqs, int n, int V, int max_seq, const SampleArgs& a, cudaStream_t st);
+
 // The bounded-wait self-test (tqd_op_wait_selftest): runs it on st and
 // returns the error bits its waits set.
 cudaError_t run_wait_selftest(uint32_t* err_bits, cudaStream_t st);
