@@ -295,6 +295,40 @@ def time_prefill(dec, wl, stream, kv_pos, w_and_row, emb_row):
             "stepwise": {"value": P / (steps_ms / 1000.0), "ms": steps_ms, "api": "tqd_prefill (one decode step per position)"}}
 
 
+SAMPLING = dict(temperature=0.8, top_k=40, top_p=0.95, min_p=0.02, repeat_penalty=1.1, seed=1234)
+
+
+def time_sampling(dec, wl, stream, firsts, greedy_ms):
+    """Decode steps with a seeded draw after each (tqd_generate_sampled, or
+    the batched form), timed like the greedy window: tokens/s and the added
+    time per step against the greedy steps."""
+    import torch
+    import token_quantized_decode_gb300 as tqd
+    P, D, B = wl.prompt_len, wl.decode_steps, wl.batch
+    params = tqd.sampling(**SAMPLING)
+
+    def window():
+        for b in range(B):
+            dec.truncate(P, seq=b)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        if B == 1:
+            dec.generate_sampled(firsts[0], D, params)
+        else:
+            dec.generate_batch_sampled(np.array(firsts), D, params)
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e)
+
+    window()
+    ms = float(np.median([window() for _ in range(3)]))
+    return {"value": D * B / (ms / 1000.0), "unit": UNIT, "controls": SAMPLING, "ms_per_step": ms / D,
+            "added_ms_per_step": ms / D - greedy_ms,
+            "api": "tqd_generate_sampled" if B == 1 else "tqd_generate_batch_sampled",
+            "note": "one sampling block per sequence after each step; steps launched one by one"}
+
+
 def run_tqd(args, wl, world, rank, local, pg):
     import torch
     import token_quantized_decode_gb300 as tqd
@@ -398,6 +432,7 @@ def run_tqd(args, wl, world, rank, local, pg):
     e2e_s = time.perf_counter() - t0
     e2e_val = sum_over_ranks(pg, n_e2e * B) / max_over_ranks(pg, e2e_s)
 
+    sampling_line = time_sampling(dec, wl, stream, firsts, t_max / steps)
     prefill_line = (time_prefill(dec, wl, stream, kv_pos, w_and_row, emb_row)
                     if B == 1 and args.kv_source == "prefill" else None)
 
@@ -434,6 +469,7 @@ def run_tqd(args, wl, world, rank, local, pg):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    line["sampling"] = sampling_line
     if prefill_line:
         line["prefill"] = prefill_line
     dec.close()

@@ -463,7 +463,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].qkv = take(4 * (qw + 2 * kvw));
     so[b].attn = take(4 * qw);
     so[b].h = take(4 * I);
-    so[b].logits = take(4 * static_cast<size_t>(V));
+    so[b].logits = take(4 * align_up(static_cast<size_t>(V), 4));  // read as float4 groups by the sampler
     so[b].po = take(4 * static_cast<size_t>(nq) * nch * hd);
     so[b].pml = take(4 * static_cast<size_t>(nq) * nch * 2);
     so[b].acnt = take(4 * nkv);
@@ -473,7 +473,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].bar = take(sizeof(DevBarrier));
     so[b].gbar = take(sizeof(DevBarrier) * 16 * nkv);  // two per group, 128 bytes apart
     so[b].opart = take(4ull * nkv * H);
-    so[b].sz = take(4 * static_cast<size_t>(V));
+    so[b].sz = take(4 * align_up(static_cast<size_t>(V), 4));
     so[b].scnt = take(4 * static_cast<size_t>(V));
   }
   const size_t o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);  // the descriptors, for kernels over sequences

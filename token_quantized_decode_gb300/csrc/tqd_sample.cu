@@ -28,8 +28,8 @@ namespace {
 
 constexpr int kSThreads = 512;
 constexpr int kSWarps = kSThreads / 32;
-constexpr int kSBins = 2048;                // value bins of a boundary search
-constexpr int kSCand = 2048;                // tokens of a boundary bin sorted exactly
+constexpr int kSBins = 1024;                // value bins of a boundary search
+constexpr int kSCand = 4096;                // tokens sorted exactly in shared memory
 constexpr float kFix = 4294967296.0f;       // 2^32: the mass of the most likely token
 constexpr unsigned long long kGolden = 0x9E3779B97F4A7C15ull;
 
@@ -41,7 +41,7 @@ struct SampleSm {
   float fa[kSWarps], fb[kSWarps];
   unsigned int ncand;
   int bin;
-  unsigned long long above_bin;
+  unsigned long long above_bin, need, r64;
   unsigned int cnt_bin;
   float zb;
   int ib;
@@ -109,20 +109,59 @@ __device__ void block_maxmin(float& a, float& b, SampleSm& sm) {
   }
 }
 
+// f(v, z[v]) for every v < V.  z is padded to whole float4 groups; a thread
+// takes groups t, t + T, t + 2T, t + 3T per round, four loads in flight.
+template <class F>
+__device__ __forceinline__ void each4(const float* z, int V, F&& f) {
+  const int n4 = (V + 3) >> 2;
+  const float4* z4 = reinterpret_cast<const float4*>(z);
+  for (int g0 = threadIdx.x; g0 < n4; g0 += 4 * kSThreads) {
+    float4 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * kSThreads;
+      q[u] = g < n4 ? z4[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * kSThreads;
+      if (g < n4) {
+        const int v = 4 * g;
+        f(v, q[u].x);
+        if (v + 1 < V) f(v + 1, q[u].y);
+        if (v + 2 < V) f(v + 2, q[u].z);
+        if (v + 3 < V) f(v + 3, q[u].w);
+      }
+    }
+  }
+}
+
 // The smallest v < V whose running weight (over 0..v, index order) exceeds
-// thresh; V when the total does not.
+// thresh, with that running weight in sm.r64; V when the total does not.
+// A thread takes four consecutive float4 groups of each chunk.
 template <class Wt>
 __device__ int first_over(const float* z, int V, Wt weight, unsigned long long thresh, SampleSm& sm) {
-  constexpr int E = 4;
+  constexpr int G = 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n4 = (V + 3) >> 2;
+  const float4* z4 = reinterpret_cast<const float4*>(z);
   unsigned long long run = 0;
-  for (int base = 0; base < V; base += kSThreads * E) {
-    const int v0 = base + static_cast<int>(threadIdx.x) * E;
-    unsigned long long w[E], s = 0;
+  for (int c0 = 0; c0 < n4; c0 += kSThreads * G) {
+    const int g0 = c0 + static_cast<int>(threadIdx.x) * G;
+    float q[4 * G];
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      w[e] = v0 + e < V ? weight(v0 + e, z[v0 + e]) : 0ull;
-      s += w[e];
+    for (int u = 0; u < G; ++u) {
+      const float4 f4 = g0 + u < n4 ? z4[g0 + u] : make_float4(0.f, 0.f, 0.f, 0.f);
+      q[4 * u] = f4.x;
+      q[4 * u + 1] = f4.y;
+      q[4 * u + 2] = f4.z;
+      q[4 * u + 3] = f4.w;
+    }
+    unsigned long long s = 0;
+#pragma unroll
+    for (int e = 0; e < 4 * G; ++e) {
+      const int v = 4 * g0 + e;
+      if (v < V) s += weight(v, q[e]);
     }
     unsigned long long x = s;
 #pragma unroll
@@ -143,11 +182,13 @@ __device__ int first_over(const float* z, int V, Wt weight, unsigned long long t
       const unsigned long long ex = run + wpre + x - s;
       if (ex <= thresh && thresh < ex + s) {
         unsigned long long acc = ex;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          acc += w[e];
+        for (int e = 0; e < 4 * G; ++e) {
+          const int v = 4 * g0 + e;
+          if (v >= V) break;
+          acc += weight(v, q[e]);
           if (acc > thresh) {
-            sm.ib = v0 + e;
+            sm.ib = v;
+            sm.r64 = acc;
             break;
           }
         }
@@ -160,21 +201,101 @@ __device__ int first_over(const float* z, int V, Wt weight, unsigned long long t
   return V;
 }
 
-// The boundary (zb, ib) of the first `need` weight units of the tokens that
-// pass `in`, in the order (z descending, index ascending): those tokens are
-// exactly the ones passing `in` with z > zb, or z == zb and index <= ib.
-// hi: the set's largest value; lo: a lower bound of its finite values;
-// 1 <= need <= the set's weight.
+// The float an order key came from.
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Bitonic sort of sm.cand[0, P) (P a power of two), descending or ascending.
+__device__ void sort_cand(int P, bool descending, SampleSm& sm) {
+  for (int k = 2; k <= P; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P; i += kSThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = sm.cand[i], b = sm.cand[ixj];
+          if ((((i & k) == 0) == descending) ? (a < b) : (a > b)) {
+            sm.cand[i] = b;
+            sm.cand[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+}
+
+// The first i < n at which the running weight (over 0..i) reaches thr, and
+// the running weight there (sm.r64); n - 1 if it never does.  Warp 0 scans
+// contiguous slices of the list; the result is broadcast.
+template <class Wt>
+__device__ int list_first_ge(int n, Wt weight_at, unsigned long long thr, SampleSm& sm) {
+  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x >> 5) == 0) {
+    const int per = (n + 31) / 32, i0 = min(n, lane * per), i1 = min(n, i0 + per);
+    unsigned long long s = 0;
+    for (int i = i0; i < i1; ++i) s += weight_at(i);
+    unsigned long long x = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    const unsigned ball = __ballot_sync(0xFFFFFFFFu, x >= thr);
+    const int L = ball ? __ffs(ball) - 1 : 31;
+    if (lane == L) {
+      unsigned long long acc = x - s;
+      int found = n - 1;
+      for (int i = i0; i < i1; ++i) {
+        acc += weight_at(i);
+        if (acc >= thr) {
+          found = i;
+          break;
+        }
+      }
+      if (!ball) acc = x;
+      sm.ib = found;
+      sm.r64 = acc;
+    }
+  }
+  __syncthreads();
+  const int r = sm.ib;
+  __syncthreads();
+  return r;
+}
+
+struct Sel {
+  float zb;
+  int ib;                   // the boundary: z > zb, or z == zb and index <= ib
+  unsigned long long wsel;  // the selected tokens' weight (mass mode)
+};
+
+// The first `need` weight units of the tokens that pass `in`, in the order
+// (z descending, index ascending), as a boundary.  need = need_abs if
+// nonzero, else ceil(frac * the set's weight) (at least 1).  hi: the set's
+// largest value; lo: a lower bound of its finite values.  A histogram of the
+// values in [lo, hi] finds the bin where the running weight reaches need; the
+// bin's tokens are sorted exactly, or, when too many, the search zooms into
+// the bin's own range; a single remaining value is cut in index order.
 template <class In, class Wt>
-__device__ void select_top(const float* z, int V, In in, Wt weight, unsigned long long need, float hi, float lo,
-                           SampleSm& sm, float& zb, int& ib) {
+__device__ Sel select_top(const float* z, int V, In in, Wt weight, unsigned long long need_abs, float frac,
+                          float hi, float lo, SampleSm& sm) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   unsigned long long above = 0;  // weight of the set's tokens above hi
+  unsigned long long need = need_abs;
+  if (!(hi > lo) && need == 0ull) {  // one value only: the set's weight directly
+    unsigned long long w = 0;
+    each4(z, V, [&](int v, float zv) {
+      if (zv > -INFINITY && in(v, zv)) w += weight(v, zv);
+    });
+    w = block_sum(w, sm);
+    need = static_cast<unsigned long long>(ceil(static_cast<double>(frac) * static_cast<double>(w)));
+    need = need < 1ull ? 1ull : (need > w ? w : need);
+  }
   for (int round = 0; round < 8 && hi > lo; ++round) {
-    const float width = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(kSBins));
-    if (!(width > 0.f)) break;
-    auto bin_of = [&](float zv) {
-      const float q = __fdiv_rn(__fsub_rn(hi, zv), width);
+    const float inv_w = __fdiv_rn(static_cast<float>(kSBins), __fsub_rn(hi, lo));
+    if (!(inv_w > 0.f) || !(inv_w < INFINITY)) break;
+    auto bin_of = [&](float zv) {  // monotone in zv: the same value always lands in the same bin
+      const float q = __fmul_rn(__fsub_rn(hi, zv), inv_w);
       return q >= static_cast<float>(kSBins - 1) ? kSBins - 1 : (q > 0.f ? static_cast<int>(q) : 0);
     };
     for (int i = t; i < kSBins; i += kSThreads) {
@@ -182,14 +303,12 @@ __device__ void select_top(const float* z, int V, In in, Wt weight, unsigned lon
       sm.hc[i] = 0u;
     }
     __syncthreads();
-    for (int v = t; v < V; v += kSThreads) {
-      const float zv = z[v];
+    each4(z, V, [&](int v, float zv) {
       if (zv <= hi && zv >= lo && in(v, zv)) {
         const int b = bin_of(zv);
         atomicAdd(&sm.hw[b], weight(v, zv));
-        atomicAdd(&sm.hc[b], 1u);
       }
-    }
+    });
     __syncthreads();
     if (warp == 0) {  // the first bin (from the top) where the running weight reaches need
       constexpr int PER = kSBins / 32;
@@ -201,7 +320,13 @@ __device__ void select_top(const float* z, int V, In in, Wt weight, unsigned lon
         const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
         if (lane >= o) x += y;
       }
-      const unsigned ball = __ballot_sync(0xFFFFFFFFu, above + x >= need);
+      unsigned long long nd = need;
+      if (nd == 0ull) {  // fraction of the set's weight, all of it in this first histogram
+        const unsigned long long w = __shfl_sync(0xFFFFFFFFu, x, 31);
+        nd = static_cast<unsigned long long>(ceil(static_cast<double>(frac) * static_cast<double>(w)));
+        nd = nd < 1ull ? 1ull : (nd > w ? w : nd);
+      }
+      const unsigned ball = __ballot_sync(0xFFFFFFFFu, above + x >= nd);
       if (ball == 0u) {  // the finite values hold less than need: the boundary is at -inf
         if (lane == 31) {
           sm.bin = -1;
@@ -212,7 +337,7 @@ __device__ void select_top(const float* z, int V, In in, Wt weight, unsigned lon
         int b = lane * PER + PER - 1;
         for (int i = 0; i < PER; ++i) {
           const int bb = lane * PER + i;
-          if (acc + sm.hw[bb] >= need) {
+          if (acc + sm.hw[bb] >= nd) {
             b = bb;
             break;
           }
@@ -220,57 +345,48 @@ __device__ void select_top(const float* z, int V, In in, Wt weight, unsigned lon
         }
         sm.bin = b;
         sm.above_bin = acc;
-        sm.cnt_bin = sm.hc[b];
       }
+      if (lane == 0) sm.need = nd;
     }
     __syncthreads();
     const int B = sm.bin;
     const unsigned long long aB = sm.above_bin;
-    const unsigned int cB = sm.cnt_bin;
+    need = sm.need;
     __syncthreads();
     if (B < 0) {
-      zb = -INFINITY;
-      ib = first_over(z, V, [&](int v, float zv) { return zv == -INFINITY && in(v, zv) ? weight(v, zv) : 0ull; },
-                      need - aB - 1, sm);
-      return;
+      Sel r;
+      r.zb = -INFINITY;
+      r.ib = first_over(z, V, [&](int v, float zv) { return zv == -INFINITY && in(v, zv) ? weight(v, zv) : 0ull; },
+                        need - aB - 1, sm);
+      r.wsel = need;
+      __syncthreads();
+      return r;
     }
-    if (cB <= static_cast<unsigned>(kSCand)) {  // sort the bin's tokens exactly
-      if (t == 0) sm.ncand = 0u;
-      __syncthreads();
-      for (int v = t; v < V; v += kSThreads) {
-        const float zv = z[v];
-        if (zv <= hi && zv >= lo && in(v, zv) && bin_of(zv) == B) {
-          const unsigned slot = atomicAdd(&sm.ncand, 1u);
-          if (slot < static_cast<unsigned>(kSCand))
-            sm.cand[slot] = (static_cast<unsigned long long>(order_key(zv)) << 32) |
-                            (0xFFFFFFFFull - static_cast<unsigned>(v));
-        }
+    if (t == 0) sm.ncand = 0u;
+    __syncthreads();
+    each4(z, V, [&](int v, float zv) {  // the bin's tokens, to sort exactly if they fit
+      if (zv <= hi && zv >= lo && in(v, zv) && bin_of(zv) == B) {
+        const unsigned slot = atomicAdd(&sm.ncand, 1u);
+        if (slot < static_cast<unsigned>(kSCand))
+          sm.cand[slot] = (static_cast<unsigned long long>(order_key(zv)) << 32) |
+                          (0xFFFFFFFFull - static_cast<unsigned>(v));
       }
-      __syncthreads();
-      const int n = static_cast<int>(min(sm.ncand, static_cast<unsigned>(kSCand)));
+    });
+    __syncthreads();
+    const unsigned cB = sm.ncand;
+    __syncthreads();
+    if (cB <= static_cast<unsigned>(kSCand)) {
+      const int n = static_cast<int>(cB);
       int P = 1;
       while (P < n) P <<= 1;
       for (int i = n + t; i < P; i += kSThreads) sm.cand[i] = 0ull;
-      __syncthreads();
-      for (int k = 2; k <= P; k <<= 1)  // bitonic sort, descending
-        for (int j = k >> 1; j > 0; j >>= 1) {
-          for (int i = t; i < P; i += kSThreads) {
-            const int ixj = i ^ j;
-            if (ixj > i) {
-              const unsigned long long a = sm.cand[i], b = sm.cand[ixj];
-              if (((i & k) == 0) ? (a < b) : (a > b)) {
-                sm.cand[i] = b;
-                sm.cand[ixj] = a;
-              }
-            }
-          }
-          __syncthreads();
-        }
       if (t == 0) {  // the bin holds at least one token of positive weight; a default all the same
         sm.zb = hi;
         sm.ib = INT_MAX;
+        sm.r64 = aB;
       }
       __syncthreads();
+      sort_cand(P, true, sm);
       if (warp == 0 && n > 0) {  // the first sorted token at which the running weight reaches need
         const int per = (n + 31) / 32, i0 = min(n, lane * per), i1 = min(n, i0 + per);
         unsigned long long s = 0;
@@ -300,23 +416,22 @@ __device__ void select_top(const float* z, int V, In in, Wt weight, unsigned lon
           const int v = static_cast<int>(0xFFFFFFFFull - (sm.cand[last] & 0xFFFFFFFFull));
           sm.zb = z[v];
           sm.ib = v;
+          sm.r64 = acc;
         }
       }
       __syncthreads();
-      zb = sm.zb;
-      ib = sm.ib;
+      Sel r{sm.zb, sm.ib, sm.r64};
       __syncthreads();
-      return;
+      return r;
     }
     // too many tokens in the bin: zoom into its own range
     float bmax = -INFINITY, bmin = INFINITY;
-    for (int v = t; v < V; v += kSThreads) {
-      const float zv = z[v];
+    each4(z, V, [&](int v, float zv) {
       if (zv <= hi && zv >= lo && in(v, zv) && bin_of(zv) == B) {
         bmax = fmaxf(bmax, zv);
         bmin = fminf(bmin, zv);
       }
-    }
+    });
     block_maxmin(bmax, bmin, sm);
     above = aB;
     hi = bmax;
@@ -324,9 +439,109 @@ __device__ void select_top(const float* z, int V, In in, Wt weight, unsigned lon
   }
   // one value left: its tokens in index order
   const float h = hi;
-  zb = h;
-  ib = first_over(z, V, [&](int v, float zv) { return zv == h && in(v, zv) ? weight(v, zv) : 0ull; },
-                  need - above - 1, sm);
+  Sel r;
+  r.zb = h;
+  r.ib = first_over(z, V, [&](int v, float zv) { return zv == h && in(v, zv) ? weight(v, zv) : 0ull; },
+                    need - above - 1, sm);
+  r.wsel = above + sm.r64;
+  __syncthreads();
+  return r;
+}
+
+// top_k <= kSCand: every token at or above the top_k boundary's value bin,
+// sorted (z descending, index ascending) into sm.cand[0, n); its first top_k
+// entries are the kept set.  A count histogram over [zmin, zmax] (one atomic
+// per distinct bin per warp) finds the bin; -1 when the tokens down to that
+// bin do not fit (or the finite values hold fewer than top_k tokens).
+__device__ int topk_list(const float* z, int V, int k, float hi, float lo_all, SampleSm& sm) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    // first the top quarter of the value range (few tokens to bin), else all of it
+    const float lo = attempt == 0 ? __fsub_rn(hi, __fmul_rn(__fsub_rn(hi, lo_all), 0.25f)) : lo_all;
+    const float inv_w = __fdiv_rn(static_cast<float>(kSBins), __fsub_rn(hi, lo));
+    if (!(inv_w > 0.f) || !(inv_w < INFINITY)) return -1;
+    auto bin_of = [&](float zv) {  // monotone in zv
+      const float q = __fmul_rn(__fsub_rn(hi, zv), inv_w);
+      return q >= static_cast<float>(kSBins - 1) ? kSBins - 1 : (q > 0.f ? static_cast<int>(q) : 0);
+    };
+    for (int i = t; i < kSBins; i += kSThreads) sm.hc[i] = 0u;
+    __syncthreads();
+    const int n4 = (V + 3) >> 2;
+    const float4* z4 = reinterpret_cast<const float4*>(z);
+    for (int g0 = t; g0 - lane < n4; g0 += 4 * kSThreads) {  // whole warps take every round
+      float4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int g = g0 + u * kSThreads;
+        q[u] = g < n4 ? z4[g] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float e4[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int v = 4 * (g0 + u * kSThreads) + e;
+          const bool in = v < V && e4[e] >= lo;
+          if (__any_sync(0xFFFFFFFFu, in)) {  // one atomic per distinct bin of the warp
+            const int b = in ? bin_of(e4[e]) : -1;
+            const unsigned m = __match_any_sync(0xFFFFFFFFu, b);
+            if (in && lane == __ffs(m) - 1) atomicAdd(&sm.hc[b], static_cast<unsigned>(__popc(m)));
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {  // the first bin (from the top) where the running count reaches k
+      constexpr int PER = kSBins / 32;
+      unsigned s = 0;
+      for (int i = 0; i < PER; ++i) s += sm.hc[lane * PER + i];
+      unsigned x = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      const unsigned ball = __ballot_sync(0xFFFFFFFFu, x >= static_cast<unsigned>(k));
+      if (!ball) {
+        if (lane == 0) sm.bin = -2;  // fewer than k tokens in the range
+      } else if (lane == __ffs(ball) - 1) {
+        unsigned acc = x - s;
+        int b = lane * PER + PER - 1;
+        for (int i = 0; i < PER; ++i) {
+          const int bb = lane * PER + i;
+          if (acc + sm.hc[bb] >= static_cast<unsigned>(k)) {
+            b = bb;
+            break;
+          }
+          acc += sm.hc[bb];
+        }
+        sm.bin = acc + sm.hc[b] <= static_cast<unsigned>(kSCand) ? b : -1;
+      }
+    }
+    __syncthreads();
+    const int B = sm.bin;
+    if (t == 0) sm.ncand = 0u;
+    __syncthreads();
+    if (B == -2) continue;
+    if (B < 0) return -1;
+    each4(z, V, [&](int v, float zv) {
+      if (zv >= lo && bin_of(zv) <= B) {
+        const unsigned slot = atomicAdd(&sm.ncand, 1u);
+        if (slot < static_cast<unsigned>(kSCand))
+          sm.cand[slot] = (static_cast<unsigned long long>(order_key(zv)) << 32) |
+                          (0xFFFFFFFFull - static_cast<unsigned>(v));
+      }
+    });
+    __syncthreads();
+    const int n = static_cast<int>(min(sm.ncand, static_cast<unsigned>(kSCand)));
+    int P = 1;
+    while (P < n) P <<= 1;
+    for (int i = n + t; i < P; i += kSThreads) sm.cand[i] = 0ull;
+    __syncthreads();
+    sort_cand(P, true, sm);
+    return n >= k ? n : -1;
+  }
+  return -1;
 }
 
 __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int V, int max_seq, SampleArgs a) {
@@ -345,9 +560,33 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
       const int x = tok[i];
       if (x >= 0 && x < V) atomicAdd(&cnt[x], 1u);
     }
-  for (int v = t; v < V; v += kSThreads) {
-    const float l = lg[v];
-    z[v] = isnan(l) ? -INFINITY : __fdiv_rn(l, a.temperature);
+  float zmax = -INFINITY, zmin = INFINITY;
+  {  // z = l / T, four float4 groups in flight per thread; the padding gets -inf
+    const int n4 = (V + 3) >> 2;
+    const float4* l4 = reinterpret_cast<const float4*>(lg);
+    float4* z4 = reinterpret_cast<float4*>(z);
+    auto tz = [&](float l, int v) {
+      const float r = v < V && !isnan(l) ? __fdiv_rn(l, a.temperature) : -INFINITY;
+      zmax = fmaxf(zmax, r);
+      if (r > -INFINITY) zmin = fminf(zmin, r);
+      return r;
+    };
+    for (int g0 = t; g0 < n4; g0 += 4 * kSThreads) {
+      float4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int g = g0 + u * kSThreads;
+        q[u] = g < n4 ? l4[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int g = g0 + u * kSThreads;
+        if (g < n4) {
+          const int v = 4 * g;
+          z4[g] = make_float4(tz(q[u].x, v), tz(q[u].y, v + 1), tz(q[u].z, v + 2), tz(q[u].w, v + 3));
+        }
+      }
+    }
   }
   __syncthreads();
   if (a.penalize) {
@@ -363,13 +602,13 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
       l = __fsub_rn(l, __fmul_rn(a.frequency, static_cast<float>(c)));
       z[x] = isnan(l) ? -INFINITY : __fdiv_rn(l, a.temperature);
     }
-  }
-  __syncthreads();
-  float zmax = -INFINITY, zmin = INFINITY;
-  for (int v = t; v < V; v += kSThreads) {
-    const float zv = z[v];
-    zmax = fmaxf(zmax, zv);
-    if (zv > -INFINITY) zmin = fminf(zmin, zv);
+    __syncthreads();
+    zmax = -INFINITY;  // the penalties moved some values: take the extremes again
+    zmin = INFINITY;
+    each4(z, V, [&](int, float zv) {
+      zmax = fmaxf(zmax, zv);
+      if (zv > -INFINITY) zmin = fminf(zmin, zv);
+    });
   }
   block_maxmin(zmax, zmin, sm);
   if (!(zmax > -INFINITY) || !(zmax < INFINITY)) {  // every logit NaN, or z overflowed
@@ -379,45 +618,79 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
     }
     return;
   }
+  const unsigned long long m24 = mix64(a.seed + (static_cast<unsigned long long>(S) + 1ull) * kGolden) >> 40;
   Keep kp{-INFINITY, INT_MAX, -INFINITY, INT_MAX, zmax, a.ln_min_p};
-  if (a.top_k >= 1 && a.top_k < V) {
-    float zb;
-    int ib;
-    select_top(
-        z, V, [](int, float) { return true; }, [](int, float) { return 1ull; },
-        static_cast<unsigned long long>(a.top_k), zmax, zmin, sm, zb, ib);
-    kp.kz = zb;
-    kp.ki = ib;
+  if (a.top_k >= 1 && a.top_k < V && a.top_k <= kSCand) {
+    // the kept tokens fit shared memory: top_p, min_p and the draw on that list
+    const int n = topk_list(z, V, a.top_k, zmax, zmin, sm);
+    if (n >= 0) {
+      const int K = a.top_k;
+      auto w_desc = [&](int i) { return wfix(key_float(static_cast<uint32_t>(sm.cand[i] >> 32)), zmax); };
+      int nk = K;
+      if (a.top_p < 1.f) {
+        unsigned long long wk = 0;
+        for (int i = t; i < K; i += kSThreads) wk += w_desc(i);
+        wk = block_sum(wk, sm);
+        unsigned long long need =
+            static_cast<unsigned long long>(ceil(static_cast<double>(a.top_p) * static_cast<double>(wk)));
+        need = need < 1ull ? 1ull : (need > wk ? wk : need);
+        nk = list_first_ge(K, w_desc, need, sm) + 1;
+      }
+      // min_p, then the kept tokens in index order: (index << 32) | key
+      int P = 1;
+      while (P < n) P <<= 1;
+      unsigned long long kept = 0;
+      for (int i = t; i < P; i += kSThreads) {
+        const unsigned long long c = sm.cand[i];
+        bool keep = false;
+        if (i < nk) {
+          const float zv = key_float(static_cast<uint32_t>(c >> 32));
+          keep = __fsub_rn(zv, zmax) >= a.ln_min_p;
+        }
+        const unsigned long long v = 0xFFFFFFFFull - (c & 0xFFFFFFFFull);
+        sm.cand[i] = keep ? ((v << 32) | (c >> 32)) : ~0ull;
+        kept += keep ? 1ull : 0ull;
+      }
+      const int nkept = static_cast<int>(block_sum(kept, sm));
+      sort_cand(P, false, sm);
+      auto w_idx = [&](int i) { return wfix(key_float(static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull)), zmax); };
+      unsigned long long W = 0;
+      for (int i = t; i < nkept; i += kSThreads) W += w_idx(i);
+      W = block_sum(W, sm);
+      const unsigned long long target = (W >> 24) * m24 + (((W & 0xFFFFFFull) * m24) >> 24);  // floor(u W)
+      const int i = list_first_ge(nkept, w_idx, target + 1ull, sm);
+      if (t == 0) tok[S] = static_cast<int32_t>(sm.cand[i] >> 32);
+      return;
+    }
   }
+  if (a.top_k >= 1 && a.top_k < V) {
+    const Sel r = select_top(
+        z, V, [](int, float) { return true; }, [](int, float) { return 1ull; },
+        static_cast<unsigned long long>(a.top_k), 0.f, zmax, zmin, sm);
+    kp.kz = r.zb;
+    kp.ki = r.ib;
+  }
+  unsigned long long W = 0;
+  bool have_w = false;
   if (a.top_p < 1.f) {
     const float kz = kp.kz;
     const int ki = kp.ki;
-    auto in_k = [kz, ki](int v, float zv) { return zv > kz || (zv == kz && v <= ki); };
-    auto wt = [zmax](int, float zv) { return wfix(zv, zmax); };
-    unsigned long long wk = 0;
-    for (int v = t; v < V; v += kSThreads) {
-      const float zv = z[v];
-      if (in_k(v, zv)) wk += wt(v, zv);
-    }
-    wk = block_sum(wk, sm);
-    unsigned long long need =
-        static_cast<unsigned long long>(ceil(static_cast<double>(a.top_p) * static_cast<double>(wk)));
-    if (need < 1ull) need = 1ull;
-    if (need > wk) need = wk;
-    float zb;
-    int ib;
-    select_top(z, V, in_k, wt, need, zmax, fmaxf(zmin, kz), sm, zb, ib);
-    kp.pz = zb;
-    kp.pi = ib;
+    const Sel r = select_top(
+        z, V, [kz, ki](int v, float zv) { return zv > kz || (zv == kz && v <= ki); },
+        [zmax](int, float zv) { return wfix(zv, zmax); }, 0ull, a.top_p, zmax, fmaxf(zmin, kz), sm);
+    kp.pz = r.zb;
+    kp.pi = r.ib;
+    W = r.wsel;  // the kept mass, unless min_p removes more
+    have_w = !(a.ln_min_p > -INFINITY);
+  }
+  if (!have_w) {
+    W = 0;
+    each4(z, V, [&](int v, float zv) {
+      if (kp(v, zv)) W += wfix(zv, zmax);
+    });
+    W = block_sum(W, sm);
   }
   // the draw
-  unsigned long long W = 0;
-  for (int v = t; v < V; v += kSThreads) {
-    const float zv = z[v];
-    if (kp(v, zv)) W += wfix(zv, zmax);
-  }
-  W = block_sum(W, sm);
-  const unsigned long long m24 = mix64(a.seed + (static_cast<unsigned long long>(S) + 1ull) * kGolden) >> 40;
   const unsigned long long target = (W >> 24) * m24 + (((W & 0xFFFFFFull) * m24) >> 24);  // floor(u W)
   const int v = first_over(
       z, V, [&](int i, float zv) { return kp(i, zv) ? wfix(zv, zmax) : 0ull; }, target, sm);
