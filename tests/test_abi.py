@@ -94,3 +94,33 @@ def test_scratch_size_queries(L):
     assert L.tqd_attention_scratch_bytes(16, 8, 128, 19) == 4 * (16 * 19 * 128 + 16 * 19 * 2 + 8)
     assert L.tqd_attention_scratch_bytes(0, 8, 128, 19) == 0
     assert L.tqd_argmax_scratch_bytes() > 0
+
+
+def _c_layout(struct: str, fields):
+    """sizeof and offsetof of a header struct, from a C program that
+    includes include/tqd.h (compiled with gcc)."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    body = "\n".join(f'  printf("%zu\\n", offsetof({struct}, {f}));' for f in fields)
+    src = ("#include <stddef.h>\n#include <stdio.h>\n#include \"tqd.h\"\n"
+           f"int main(void) {{\n  printf(\"%zu\\n\", sizeof({struct}));\n{body}\n  return 0;\n}}\n")
+    with tempfile.TemporaryDirectory() as d:
+        c, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        open(c, "w").write(src)
+        subprocess.run([cc, "-I", os.path.dirname(HEADER), c, "-o", exe], check=True, capture_output=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split()
+    return int(out[0]), [int(x) for x in out[1:]]
+
+
+@pytest.mark.parametrize("name, cls", [("tqd_config", _lib.tqd_config), ("tqd_sampling", _lib.tqd_sampling),
+                                       ("tqd_layer_weights", _lib.tqd_layer_weights),
+                                       ("tqd_host_weights", _lib.tqd_host_weights)])
+def test_binding_structs_match_the_header_layout(name, cls):
+    fields = [f[0] for f in cls._fields_]
+    size, offsets = _c_layout(name, fields)
+    assert ctypes.sizeof(cls) == size, name
+    assert [getattr(cls, f).offset for f in fields] == offsets, name
