@@ -85,6 +85,8 @@ def test_sample_matches_the_oracle(tqd):
     # are unique
     assert unique >= 0.8 * len(PARAMS) * 12
     assert np.array_equal(dec.logits(), logits)  # drawing reads the logits, never writes them
+    # after draws replaced it, temperature 0 gives the greedy token of the logits again
+    assert dec.sample(tqd.sampling(temperature=0.0)) == S.greedy(logits)
     dec.close()
 
 

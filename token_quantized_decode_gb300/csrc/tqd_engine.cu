@@ -474,7 +474,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].gbar = take(sizeof(DevBarrier) * 16 * nkv);  // two per group, 128 bytes apart
     so[b].opart = take(4ull * nkv * H);
     so[b].sz = take(4 * align_up(static_cast<size_t>(V), 4));
-    so[b].scnt = take(4 * static_cast<size_t>(V));
+    so[b].scnt = take(4 * align_up(static_cast<size_t>(V), 4));
   }
   const size_t o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);  // the descriptors, for kernels over sequences
   // batched-step buffers (several sequences per step, or a prompt's tiles),
@@ -941,6 +941,7 @@ int32_t tqd_sample(tqd_model* m, int32_t seq, const tqd_sampling* sampling, int3
   SampleArgs a{};
   bool greedy = false;
   if ((rc = sample_args(sampling, a, &greedy))) return rc;
+  if (greedy) a.temperature = 0.f;
   if (!token_out) {
     set_error("token_out is NULL");
     return TQD_ERR_BAD_ARG;
@@ -951,8 +952,8 @@ int32_t tqd_sample(tqd_model* m, int32_t seq, const tqd_sampling* sampling, int3
               s.next_pos);
     return TQD_ERR_NOT_PREFILLED;
   }
-  if (!greedy)
-    CK(launch_sample(m->dseqs + seq, 1, m->cfg.vocab, m->cfg.max_seq, a, m->stream), "sampler launch");
+  // (greedy too: an earlier draw may have replaced the step's argmax at this position)
+  CK(launch_sample(m->dseqs + seq, 1, m->cfg.vocab, m->cfg.max_seq, a, m->stream), "sampler launch");
   CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + s.next_pos, 4, cudaMemcpyDeviceToHost, m->stream), "read token");
   if ((rc = finish(m, s))) return rc;
   *token_out = m->h_tokens[0];

@@ -127,7 +127,7 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
 // Seeded sampling (tqd_sample.cu): one block per sequence draws the token for
 // its next position from its last logits and writes it there as the input.
 struct SampleArgs {
-  float temperature;   // > 0
+  float temperature;   // <= 0: the greedy token of the raw logits
   int top_k;           // 1 <= top_k < V, else off
   float top_p;         // < 1, else off
   float ln_min_p;      // f32(ln(min_p)), -inf when off

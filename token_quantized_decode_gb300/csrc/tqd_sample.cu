@@ -555,60 +555,93 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
   uint32_t* cnt = s.scnt;
   int32_t* tok = s.tokens;
   const int n_in = static_cast<int>(S);
+  if (!(a.temperature > 0.f)) {  // the greedy token of the raw logits: ties to the lower index, NaN never wins
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    each4(lg, V, [&](int v, float l) {
+      if (!isnan(l) && (l > bv || (l == bv && v < bi))) {
+        bv = l;
+        bi = v;
+      }
+    });
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((t & 31) == 0) {
+      sm.fa[t >> 5] = bv;
+      sm.cand[t >> 5] = static_cast<unsigned long long>(static_cast<unsigned>(bi));
+    }
+    __syncthreads();
+    if (t == 0) {
+      for (int w = 1; w < kSWarps; ++w) {
+        const float ov = sm.fa[w];
+        const int oi = static_cast<int>(sm.cand[w]);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (bi == INT_MAX) {
+        atomicOr(&s.state->err, kErrAllNaN);
+        bi = -1;
+      }
+      tok[S] = bi;
+    }
+    return;
+  }
   if (a.penalize)
     for (int i = t; i < n_in; i += kSThreads) {
       const int x = tok[i];
       if (x >= 0 && x < V) atomicAdd(&cnt[x], 1u);
     }
+  // z = penalised l / T, four float4 groups in flight per thread; the counts
+  // are read beside the logits and zeroed; the padding gets -inf
+  __syncthreads();
   float zmax = -INFINITY, zmin = INFINITY;
-  {  // z = l / T, four float4 groups in flight per thread; the padding gets -inf
+  {
     const int n4 = (V + 3) >> 2;
     const float4* l4 = reinterpret_cast<const float4*>(lg);
     float4* z4 = reinterpret_cast<float4*>(z);
-    auto tz = [&](float l, int v) {
-      const float r = v < V && !isnan(l) ? __fdiv_rn(l, a.temperature) : -INFINITY;
+    uint4* c4 = reinterpret_cast<uint4*>(cnt);
+    auto tz = [&](float l, unsigned c, int v) {
+      if (v >= V || isnan(l)) return -INFINITY;
+      if (c) {
+        l = l > 0.f ? __fdiv_rn(l, a.repeat) : __fmul_rn(l, a.repeat);
+        l = __fsub_rn(l, a.presence);
+        l = __fsub_rn(l, __fmul_rn(a.frequency, static_cast<float>(c)));
+        if (isnan(l)) return -INFINITY;
+      }
+      const float r = __fdiv_rn(l, a.temperature);
       zmax = fmaxf(zmax, r);
       if (r > -INFINITY) zmin = fminf(zmin, r);
       return r;
     };
     for (int g0 = t; g0 < n4; g0 += 4 * kSThreads) {
       float4 q[4];
+      uint4 cc[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int g = g0 + u * kSThreads;
         q[u] = g < n4 ? l4[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+        cc[u] = g < n4 && a.penalize ? c4[g] : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int g = g0 + u * kSThreads;
         if (g < n4) {
           const int v = 4 * g;
-          z4[g] = make_float4(tz(q[u].x, v), tz(q[u].y, v + 1), tz(q[u].z, v + 2), tz(q[u].w, v + 3));
+          z4[g] = make_float4(tz(q[u].x, cc[u].x, v), tz(q[u].y, cc[u].y, v + 1), tz(q[u].z, cc[u].z, v + 2),
+                              tz(q[u].w, cc[u].w, v + 3));
+          if (cc[u].x | cc[u].y | cc[u].z | cc[u].w) c4[g] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     }
-  }
-  __syncthreads();
-  if (a.penalize) {
-    for (int i = t; i < n_in; i += kSThreads) {
-      const int x = tok[i];
-      if (x < 0 || x >= V) continue;
-      const unsigned c = atomicExch(&cnt[x], 0u);  // one thread per distinct token
-      if (c == 0u) continue;
-      float l = lg[x];
-      if (isnan(l)) continue;
-      l = l > 0.f ? __fdiv_rn(l, a.repeat) : __fmul_rn(l, a.repeat);
-      l = __fsub_rn(l, a.presence);
-      l = __fsub_rn(l, __fmul_rn(a.frequency, static_cast<float>(c)));
-      z[x] = isnan(l) ? -INFINITY : __fdiv_rn(l, a.temperature);
-    }
-    __syncthreads();
-    zmax = -INFINITY;  // the penalties moved some values: take the extremes again
-    zmin = INFINITY;
-    each4(z, V, [&](int, float zv) {
-      zmax = fmaxf(zmax, zv);
-      if (zv > -INFINITY) zmin = fminf(zmin, zv);
-    });
   }
   block_maxmin(zmax, zmin, sm);
   if (!(zmax > -INFINITY) || !(zmax < INFINITY)) {  // every logit NaN, or z overflowed
