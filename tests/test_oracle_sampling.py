@@ -122,3 +122,18 @@ def test_nan_logits_are_never_drawn():
     l = np.log(PROBS).astype(np.float32)
     l[3] = np.nan
     assert all(S.sample(l, [], pos, 1.0, seed=5)[0] != 3 for pos in range(2000))
+
+
+def test_boundaries_inside_ties_follow_the_index_order():
+    # p = (0.2, 0.4, 0.2, 0.2): token 1 first, then the tied 0, 2, 3 in index order
+    l = np.log(np.array([0.2, 0.4, 0.2, 0.2])).astype(np.float32)
+    assert l[0] == l[2] == l[3]
+
+    def ks(**kw):
+        return set(np.nonzero(S.kept(l, [], 1.0, **kw)[1])[0].tolist())
+
+    assert ks(top_k=2) == {1, 0}
+    assert ks(top_k=3) == {1, 0, 2}
+    assert ks(top_p=0.5) == {1, 0}        # 0.4 < 0.5 <= 0.6
+    assert ks(top_p=0.7) == {1, 0, 2}     # 0.6 < 0.7 <= 0.8
+    assert ks(top_k=3, top_p=0.9) == {1, 0, 2}
