@@ -80,6 +80,8 @@ def lib():
         L.orc_kv_get.argtypes = [vp, i32, i64, vp, vp]
         L.orc_kv_load.restype = i32
         L.orc_kv_load.argtypes = [vp, i64, vp, vp]
+        L.orc_set_kv_f16.restype = i32
+        L.orc_set_kv_f16.argtypes = [vp, i32]
         L.orc_next_pos.restype = i64
         L.orc_next_pos.argtypes = [vp]
         L.orc_reset.restype = None
@@ -199,7 +201,7 @@ class OracleModel:
     ``model`` is a ``synth.SynthModel`` (or any object with the same fields);
     its arrays are referenced, not copied, so they must outlive this object."""
 
-    def __init__(self, model, max_seq: int):
+    def __init__(self, model, max_seq: int, kv_f16: bool = False):
         cfg = model.cfg
         self.cfg = cfg
         self._model = model
@@ -217,6 +219,7 @@ class OracleModel:
                                        _p(d["w_up"]), _p(d["w_down"]))
             assert rc == 0
         assert L.orc_model_set_head(self._h, _p(model.lm_head), _p(model.out_norm), None) == 0
+        assert L.orc_set_kv_f16(self._h, int(kv_f16)) == 0
         self.max_seq = max_seq
 
     def __del__(self):

@@ -217,6 +217,7 @@ typedef struct {
   const void* embed;    /* [vocab x hidden]; the lm_head bytes when tied */
   const float* out_norm;
   double *K, *V;        /* [n_layers][max_seq][kv_width] */
+  int kv_f16;           /* cached rows rounded to f16 (the quantized-KV reading) */
   double *x, *xn, *q, *k, *v, *att, *tmp, *gate, *up, *h;
 } orc_model;
 
@@ -264,6 +265,18 @@ orc_model* orc_model_new(int n_layers, int hidden, int n_heads, int n_kv, int he
   }
   return m;
 }
+
+/* Cached K/V rows stored as f16: each element rounded to the nearest f16,
+ * ties to even (IEEE binary16), when it enters the cache.  The pages keep an
+ * f32 cache and list a packed-F16 KV representation as the next step ("Metal
+ * LLM decode", the batched prefill+decode arm); this is that step's reading. */
+int orc_set_kv_f16(orc_model* m, int on) {
+  if (!m) return -1;
+  m->kv_f16 = on ? 1 : 0;
+  return 0;
+}
+
+static double kv_store(const orc_model* m, double x) { return m->kv_f16 ? (double)(_Float16)x : x; }
 
 void orc_model_free(orc_model* m) {
   if (!m) return;
@@ -333,8 +346,10 @@ int orc_step(orc_model* m, int64_t token, int64_t pos, int want_logits, double* 
     }
     orc_rope(m->q, (int)nq, (int)hd, pos, m->theta);
     orc_rope(m->k, (int)nkv, (int)hd, pos, m->theta);
-    memcpy(Kl + pos * kvw, m->k, (size_t)kvw * sizeof(double));  /* append_kv */
-    memcpy(Vl + pos * kvw, m->v, (size_t)kvw * sizeof(double));
+    for (int64_t i = 0; i < kvw; ++i) {  /* append_kv */
+      Kl[pos * kvw + i] = kv_store(m, m->k[i]);
+      Vl[pos * kvw + i] = kv_store(m, m->v[i]);
+    }
     orc_attention(m->q, Kl, Vl, pos + 1, kvw, (int)nq, (int)nkv, (int)hd, m->att);
     matvec(m, L->wo, H, qw, m->att, m->tmp);
     for (int64_t i = 0; i < H; ++i) m->x[i] += m->tmp[i];  /* add_inplace */
@@ -383,8 +398,8 @@ int orc_kv_load(orc_model* m, int64_t n_pos, const float* k, const float* v) {
       for (int64_t i = 0; i < kvw; ++i) {
         int64_t src = ((int64_t)l * n_pos + p) * kvw + i;
         int64_t dst = ((int64_t)l * m->max_seq + p) * kvw + i;
-        m->K[dst] = (double)k[src];
-        m->V[dst] = (double)v[src];
+        m->K[dst] = kv_store(m, (double)k[src]);
+        m->V[dst] = kv_store(m, (double)v[src]);
       }
   m->next_pos = n_pos;
   return 0;
