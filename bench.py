@@ -329,6 +329,41 @@ def time_sampling(dec, wl, stream, firsts, greedy_ms):
             "note": "one sampling block per sequence after each step; steps launched one by one"}
 
 
+def time_kv16(args, wl, model, stream, hbm, kind):
+    """The same batched decode windows on a model whose KV cache holds f16
+    elements (TQD_KV_F16: rows rounded to binary16 as they are appended),
+    after the same prompts prefilled in tiles: tokens/s and the step's
+    algorithmic bytes with two-byte K/V elements."""
+    import torch
+    import token_quantized_decode_gb300 as tqd
+    cfg, P, D, B = wl.model, wl.prompt_len, wl.decode_steps, wl.batch
+    dec = tqd.Decoder(model, P + D, B, stream=stream, kv_type=tqd.TQD_KV_F16)
+    firsts = [dec.prefill_batch(synth.prompt(wl, seq=b), seq=b) for b in range(B)]
+    kv_pos = 2 * cfg.kv_width * 2 * cfg.n_layers
+    w_and_row = dec.step_bytes(0) - 2 * kv_pos
+    emb_row = cfg.hidden * 17 // 16 if cfg.weight_type == "q8_0" else 2 * cfg.hidden
+
+    def window():
+        for b in range(B):
+            dec.truncate(P, seq=b)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        dec.generate_batch(np.array(firsts), D)
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e)
+
+    window()
+    ms = float(np.median([window() for _ in range(3)]))
+    nbytes = sum(w_and_row + (B - 1) * emb_row + B * kv_pos * (p + 2) for p in range(P, P + D)) / D
+    dec.close()
+    return {"value": D * B / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms / D,
+            "step_roofline_frac": nbytes / (hbm * 1e9) / (ms / D / 1000.0), "bytes_per_step": nbytes,
+            "peak_kind": f"{kind} copy bandwidth",
+            "api": "tqd_generate_batch on a TQD_KV_F16 model (prompts prefilled in tiles)"}
+
+
 def run_tqd(args, wl, world, rank, local, pg):
     import torch
     import token_quantized_decode_gb300 as tqd
@@ -340,7 +375,8 @@ def run_tqd(args, wl, world, rank, local, pg):
     P, D, B = wl.prompt_len, wl.decode_steps, wl.batch
     schedule = tqd.TQD_SCHED_PERSISTENT if args.schedule == "persistent" else tqd.TQD_SCHED_GRAPH
     dec = tqd.Decoder(model, P + D, B, schedule, stream=stream)
-    del model
+    if B == 1:
+        del model
     firsts = []
     for b in range(B):
         ids = synth.prompt(wl, seq=b)
@@ -473,6 +509,8 @@ def run_tqd(args, wl, world, rank, local, pg):
     if prefill_line:
         line["prefill"] = prefill_line
     dec.close()
+    if B > 1:
+        line["kv_f16"] = time_kv16(args, wl, model, stream, hbm, kind)
     return line
 
 

@@ -64,6 +64,16 @@ enum { TQD_WEIGHT_Q8_0 = 0, TQD_WEIGHT_BF16 = 1 };
  *                        barriers. */
 enum { TQD_SCHED_GRAPH = 0, TQD_SCHED_PERSISTENT = 1 };
 
+/* Element type of the KV cache.  TQD_KV_F32: the pages' f32 cache.
+ * TQD_KV_F16: every K and V element rounded to the nearest IEEE binary16
+ * (ties to even) when it is appended or uploaded, halving the attention's
+ * bytes (the packed-F16 KV representation "Metal LLM decode" names as the
+ * batched prefill+decode arm's next step).  An f16 cache runs in the batched
+ * step, the prefill tiles and the sampler; the batch-1 schedules read an f32
+ * cache, so tqd_prefill, tqd_decode_step, tqd_generate and
+ * tqd_generate_sampled refuse it with UNSUPPORTED_CONFIG. */
+enum { TQD_KV_F32 = 0, TQD_KV_F16 = 1 };
+
 /* Model hyper-parameters ("One command buffer per token", section "The seam":
  * the plan's hidden, heads, kv heads, head_dim, intermediate, vocab, rms_eps,
  * rope_theta), plus this library's capacity fields. */
@@ -82,6 +92,7 @@ typedef struct tqd_config {
   int32_t max_seq;       /* KV rows per sequence (positions 0 .. max_seq-1) */
   int32_t max_batch;     /* sequences held by the model (each its own KV) */
   int32_t schedule;      /* TQD_SCHED_* */
+  int32_t kv_type;       /* TQD_KV_*; f16 needs a shape the batched step supports */
 } tqd_config;
 
 /* One layer's weights on the host.  Matrices are row-major [rows x cols]:

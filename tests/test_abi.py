@@ -43,8 +43,8 @@ def test_status_names_need_no_device(L):
 
 
 def test_config_struct_layout_matches_header(L):
-    # 11 int32 / float fields before max_seq, then max_seq, max_batch, schedule
-    assert ctypes.sizeof(_lib.tqd_config) == 14 * 4
+    # 11 int32 / float fields before max_seq, then max_seq, max_batch, schedule, kv_type
+    assert ctypes.sizeof(_lib.tqd_config) == 15 * 4
     assert ctypes.sizeof(_lib.tqd_layer_weights) == 11 * ctypes.sizeof(ctypes.c_void_p)
     assert ctypes.sizeof(_lib.tqd_host_weights) == 4 * ctypes.sizeof(ctypes.c_void_p)
 

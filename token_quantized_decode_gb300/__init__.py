@@ -12,11 +12,13 @@ import ctypes
 
 import numpy as np
 
-from ._lib import (TQD_SCHED_GRAPH, TQD_SCHED_PERSISTENT, TQD_WEIGHT_BF16, TQD_WEIGHT_Q8_0, TQDError,
+from ._lib import (TQD_KV_F16, TQD_KV_F32, TQD_SCHED_GRAPH, TQD_SCHED_PERSISTENT, TQD_WEIGHT_BF16,
+                   TQD_WEIGHT_Q8_0, TQDError,
                    check, lib, tqd_config, tqd_host_weights, tqd_layer_weights, tqd_sampling)
 
 __all__ = [
-    "TQDError", "TQD_SCHED_GRAPH", "TQD_SCHED_PERSISTENT", "TQD_WEIGHT_Q8_0", "TQD_WEIGHT_BF16",
+    "TQDError", "TQD_SCHED_GRAPH", "TQD_SCHED_PERSISTENT", "TQD_WEIGHT_Q8_0", "TQD_WEIGHT_BF16", "TQD_KV_F32",
+    "TQD_KV_F16",
     "make_config", "make_host_weights", "tqd_status_name", "tqd_create", "tqd_destroy", "tqd_reset",
     "tqd_truncate", "tqd_next_pos", "tqd_prefill", "tqd_prefill_batch", "tqd_kv_upload", "tqd_decode_step", "tqd_generate",
     "tqd_decode_step_batch", "tqd_generate_batch", "tqd_sample", "tqd_generate_sampled",
@@ -46,7 +48,8 @@ def _stream(stream):
     return int(stream.cuda_stream)
 
 
-def make_config(model_cfg, max_seq: int, max_batch: int = 1, schedule: int = TQD_SCHED_GRAPH) -> tqd_config:
+def make_config(model_cfg, max_seq: int, max_batch: int = 1, schedule: int = TQD_SCHED_GRAPH,
+                kv_type: int = TQD_KV_F32) -> tqd_config:
     """tqd_config from an object with the model's hyper-parameter fields
     (n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab,
     qk_norm, weight_type 'q8_0' | 'bf16', rope_theta, rms_eps)."""
@@ -60,6 +63,7 @@ def make_config(model_cfg, max_seq: int, max_batch: int = 1, schedule: int = TQD
     c.max_seq = int(max_seq)
     c.max_batch = int(max_batch)
     c.schedule = int(schedule)
+    c.kv_type = int(kv_type)
     return c
 
 
@@ -222,9 +226,9 @@ class Decoder:
     """Owns one model handle (tqd_create ... tqd_destroy)."""
 
     def __init__(self, model, max_seq: int, max_batch: int = 1, schedule: int = TQD_SCHED_GRAPH,
-                 stream=None):
+                 stream=None, kv_type: int = TQD_KV_F32):
         self.cfg = model.cfg
-        self.config = make_config(model.cfg, max_seq, max_batch, schedule)
+        self.config = make_config(model.cfg, max_seq, max_batch, schedule, kv_type)
         self._weights = make_host_weights(model)
         self.handle = tqd_create(self.config, self._weights, stream)
         self._weights = None  # uploaded; host copies no longer needed by the library

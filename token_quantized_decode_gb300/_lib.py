@@ -22,6 +22,7 @@ for _i, _n in enumerate(STATUS_NAMES):
 
 TQD_WEIGHT_Q8_0, TQD_WEIGHT_BF16 = 0, 1
 TQD_SCHED_GRAPH, TQD_SCHED_PERSISTENT = 0, 1
+TQD_KV_F32, TQD_KV_F16 = 0, 1
 
 
 class tqd_config(ctypes.Structure):
@@ -30,7 +31,7 @@ class tqd_config(ctypes.Structure):
                 ("intermediate", ctypes.c_int32), ("vocab", ctypes.c_int32), ("qk_norm", ctypes.c_int32),
                 ("weight_type", ctypes.c_int32), ("rope_theta", ctypes.c_float),
                 ("rms_eps", ctypes.c_float), ("max_seq", ctypes.c_int32), ("max_batch", ctypes.c_int32),
-                ("schedule", ctypes.c_int32)]
+                ("schedule", ctypes.c_int32), ("kv_type", ctypes.c_int32)]
 
 
 class tqd_layer_weights(ctypes.Structure):

@@ -1267,13 +1267,27 @@ constexpr uint32_t kASlotBytes = 32 * 1024;
 
 __device__ __forceinline__ void async() { asm volatile("bar.sync 1, %0;" ::"n"(kAT) : "memory"); }
 
+// Four consecutive cache elements as floats: f32 rows, or f16 rows (8 bytes).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __half* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  __half2 lo, hi;
+  memcpy(&lo, &u.x, 4);
+  memcpy(&hi, &u.y, 4);
+  const float2 a = __half22float2(lo), b = __half22float2(hi);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // fresh: the step's own K/V row comes from qkv (normalised, rotated and
 // appended here); otherwise every row up to the position is already in the
 // cache (a prefill tile's rows, appended by k_kv_append_batch) and the
-// producer waits for that kernel before copying.
-template <int HD, int G>
+// producer waits for that kernel before copying.  KV16: the cache holds f16
+// elements (the fresh row is rounded as it is stored and used rounded).
+template <int HD, int G, bool KV16>
 __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, int g, int c, int nch,
                                 const float* qkv, float* po, float* pml, unsigned char* sm, bool fresh) {
+  using KT = typename std::conditional<KV16, __half, float>::type;
+  constexpr uint32_t ES = sizeof(KT);
   constexpr int NJ = HD / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kASlots * kASlotBytes);
@@ -1288,8 +1302,10 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
   const int t0 = min(S, c * cs), t1 = min(S, t0 + cs);
   const bool has_new = fresh && t0 <= static_cast<int>(pos) && static_cast<int>(pos) < t1;
   const int tc = fresh ? min(t1, static_cast<int>(pos)) : t1;
-  const int rpp = static_cast<int>(kASlotBytes / (2u * 4u * HD));
+  const int rpp = static_cast<int>(kASlotBytes / (2u * ES * HD));
   const size_t head = (static_cast<size_t>(layer) * m.nkv + g) * m.max_seq * HD;
+  KT* kc = reinterpret_cast<KT*>(s.kcache);
+  KT* vc = reinterpret_cast<KT*>(s.vcache);
   uint32_t* err = &s.state->err;
   if (threadIdx.x == kAT) {
     // producer
@@ -1299,11 +1315,11 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
       const int cnt = min(rpp, tc - a0);
       const uint32_t slot = n % kASlots, use = n / kASlots;
       if (use > 0 && !mbar_wait_bounded(empty + slot, (use - 1) & 1u, err)) break;
-      const uint32_t bytes = static_cast<uint32_t>(cnt) * HD * 4u;
+      const uint32_t bytes = static_cast<uint32_t>(cnt) * HD * ES;
       unsigned char* dst = sm + slot * kASlotBytes;
       mbar_arrive_expect_tx(full + slot, 2u * bytes);
-      bulk_g2s(dst, s.kcache + head + static_cast<size_t>(a0) * HD, bytes, full + slot);
-      bulk_g2s(dst + static_cast<size_t>(rpp) * HD * 4u, s.vcache + head + static_cast<size_t>(a0) * HD, bytes,
+      bulk_g2s(dst, kc + head + static_cast<size_t>(a0) * HD, bytes, full + slot);
+      bulk_g2s(dst + static_cast<size_t>(rpp) * HD * ES, vc + head + static_cast<size_t>(a0) * HD, bytes,
                full + slot);
     }
     {  // the O projection's weights into L2, this CTA's share of their 128-byte lines
@@ -1337,8 +1353,16 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
     const size_t r = head + static_cast<size_t>(pos) * HD;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      s.kcache[r + lane + 32 * j] = kv[j];
-      s.vcache[r + lane + 32 * j] = vv[j];
+      if constexpr (KV16) {
+        const __half hk = __float2half_rn(kv[j]), hv = __float2half_rn(vv[j]);
+        kc[r + lane + 32 * j] = hk;
+        vc[r + lane + 32 * j] = hv;
+        kv[j] = __half2float(hk);
+        vv[j] = __half2float(hv);
+      } else {
+        kc[r + lane + 32 * j] = kv[j];
+        vc[r + lane + 32 * j] = vv[j];
+      }
       knew[lane + 32 * j] = kv[j];
       vnew[lane + 32 * j] = vv[j];
     }
@@ -1363,11 +1387,12 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
       oo[hh][i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  // one row for this lane's group (all 32 lanes call it; `valid` masks the update)
-  auto row_update = [&](const float* kr, const float* vr, bool valid) {
+  // one row for this lane's group (all 32 lanes call it; `valid` masks the
+  // update); rows of the cache (KT) or the fresh row (f32)
+  auto row_update = [&](const auto* kr, const auto* vr, bool valid) {
     float4 kf[NC4];
 #pragma unroll
-    for (int i = 0; i < NC4; ++i) kf[i] = *reinterpret_cast<const float4*>(kr + 32 * i + 4 * g8);
+    for (int i = 0; i < NC4; ++i) kf[i] = ld4(kr + 32 * i + 4 * g8);
     float sc[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
@@ -1387,7 +1412,7 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
     if (!valid) return;
     float4 vf[NC4];
 #pragma unroll
-    for (int i = 0; i < NC4; ++i) vf[i] = *reinterpret_cast<const float4*>(vr + 32 * i + 4 * g8);
+    for (int i = 0; i < NC4; ++i) vf[i] = ld4(vr + 32 * i + 4 * g8);
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
       float corr = 1.f, p = 1.f;
@@ -1412,8 +1437,8 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
     const int cnt = min(rpp, tc - a0);
     const uint32_t slot = n % kASlots;
     mbar_wait_bounded(full + slot, (n / kASlots) & 1u, err);
-    const float* Ks = reinterpret_cast<const float*>(sm + slot * kASlotBytes);
-    const float* Vs = Ks + static_cast<size_t>(rpp) * HD;
+    const KT* Ks = reinterpret_cast<const KT*>(sm + slot * kASlotBytes);
+    const KT* Vs = Ks + static_cast<size_t>(rpp) * HD;
     for (int r0 = 4 * warp; r0 < cnt; r0 += 4 * kAW) {
       const int r = min(r0 + rg, cnt - 1);
       row_update(Ks + r * HD, Vs + r * HD, r0 + rg < cnt);
@@ -1422,7 +1447,7 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
     if (lane == 0)
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(empty + slot)) : "memory");
   }
-  if (has_new && warp == kAW - 1) row_update(knew, vnew, rg == 0);
+  if (has_new && warp == kAW - 1) row_update(static_cast<const float*>(knew), static_cast<const float*>(vnew), rg == 0);
   // merge the four groups of the warp (lanes g8, g8+8, g8+16, g8+24 hold the
   // same elements), then publish the warp's state
 #pragma unroll
@@ -1486,7 +1511,8 @@ __device__ void attn_batch_item(const DevModel& m, const DevSeq& s, int layer, i
 // k after QK-norm and RoPE at the slot's position, and v, into the cache rows
 // that the attention kernel then reads (the tile's slots attend to each
 // other's rows, so they are written before any slot's attention starts).
-template <int HD>
+// KV16: the rows are stored rounded to f16.
+template <int HD, bool KV16>
 __global__ void __launch_bounds__(1024) k_kv_append_batch(DevModel m, const DevSeq* seqs, int layer, const float* QKV) {
   constexpr int NJ = HD / 32;
   pdl_wait();  // this layer's QKV projection is complete
@@ -1508,12 +1534,17 @@ __global__ void __launch_bounds__(1024) k_kv_append_batch(DevModel m, const DevS
   const size_t r = ((static_cast<size_t>(layer) * m.nkv + g) * m.max_seq + pos) * HD;
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
-    s.kcache[r + lane + 32 * j] = kv[j];
-    s.vcache[r + lane + 32 * j] = vv[j];
+    if constexpr (KV16) {
+      reinterpret_cast<__half*>(s.kcache)[r + lane + 32 * j] = __float2half_rn(kv[j]);
+      reinterpret_cast<__half*>(s.vcache)[r + lane + 32 * j] = __float2half_rn(vv[j]);
+    } else {
+      s.kcache[r + lane + 32 * j] = kv[j];
+      s.vcache[r + lane + 32 * j] = vv[j];
+    }
   }
 }
 
-template <int HD, int G>
+template <int HD, int G, bool KV16>
 __global__ void __launch_bounds__(kAT + 32, 2)
     k_attn_batch(DevModel m, const DevSeq* seqs, int layer, int nch, const float* QKV, float* PO, float* PML,
                  int fresh) {
@@ -1535,26 +1566,32 @@ __global__ void __launch_bounds__(kAT + 32, 2)
   const float* qkv = QKV + static_cast<size_t>(b) * (m.qw + 2 * m.kvw);
   float* po = PO + static_cast<size_t>(b) * m.nq * nch * HD;
   float* pml = PML + static_cast<size_t>(b) * m.nq * nch * 2;
-  attn_batch_item<HD, G>(m, s, layer, g, c, nch, qkv, po, pml, sm, fresh != 0);
+  attn_batch_item<HD, G, KV16>(m, s, layer, g, c, nch, qkv, po, pml, sm, fresh != 0);
 }
 
-// The attention kernel instantiated for the model's head_dim and group size.
-const void* attn_batch_fn(const DevModel& m) {
-  const int G = m.nq / m.nkv;
-  if (m.hd == 128) {
+// The attention kernel instantiated for the model's head_dim, group size and
+// cache element type.
+template <bool KV16>
+const void* attn_batch_fn_t(int hd, int G) {
+  if (hd == 128) {
     switch (G) {
-      case 1: return reinterpret_cast<const void*>(&k_attn_batch<128, 1>);
-      case 2: return reinterpret_cast<const void*>(&k_attn_batch<128, 2>);
-      case 3: return reinterpret_cast<const void*>(&k_attn_batch<128, 3>);
-      default: return reinterpret_cast<const void*>(&k_attn_batch<128, 4>);
+      case 1: return reinterpret_cast<const void*>(&k_attn_batch<128, 1, KV16>);
+      case 2: return reinterpret_cast<const void*>(&k_attn_batch<128, 2, KV16>);
+      case 3: return reinterpret_cast<const void*>(&k_attn_batch<128, 3, KV16>);
+      default: return reinterpret_cast<const void*>(&k_attn_batch<128, 4, KV16>);
     }
   }
   switch (G) {
-    case 1: return reinterpret_cast<const void*>(&k_attn_batch<64, 1>);
-    case 2: return reinterpret_cast<const void*>(&k_attn_batch<64, 2>);
-    case 3: return reinterpret_cast<const void*>(&k_attn_batch<64, 3>);
-    default: return reinterpret_cast<const void*>(&k_attn_batch<64, 4>);
+    case 1: return reinterpret_cast<const void*>(&k_attn_batch<64, 1, KV16>);
+    case 2: return reinterpret_cast<const void*>(&k_attn_batch<64, 2, KV16>);
+    case 3: return reinterpret_cast<const void*>(&k_attn_batch<64, 3, KV16>);
+    default: return reinterpret_cast<const void*>(&k_attn_batch<64, 4, KV16>);
   }
+}
+
+const void* attn_batch_fn(const DevModel& m) {
+  const int G = m.nq / m.nkv;
+  return m.kv16 ? attn_batch_fn_t<true>(m.hd, G) : attn_batch_fn_t<false>(m.hd, G);
 }
 
 size_t attn_batch_smem(const DevModel& m) {
@@ -1747,8 +1784,13 @@ cudaError_t enqueue_batch_step(const DevModel& m, const DevLayer* host_layers, c
       return e;
     if (tile) {
       cudaLaunchConfig_t cp = config(n, 32 * m.nkv, 0, 1);
-      e = m.hd == 128 ? cudaLaunchKernelEx(&cp, k_kv_append_batch<128>, m, seqs, l, static_cast<const float*>(QKV))
-                      : cudaLaunchKernelEx(&cp, k_kv_append_batch<64>, m, seqs, l, static_cast<const float*>(QKV));
+      const float* q = QKV;
+      if (m.kv16)
+        e = m.hd == 128 ? cudaLaunchKernelEx(&cp, k_kv_append_batch<128, true>, m, seqs, l, q)
+                        : cudaLaunchKernelEx(&cp, k_kv_append_batch<64, true>, m, seqs, l, q);
+      else
+        e = m.hd == 128 ? cudaLaunchKernelEx(&cp, k_kv_append_batch<128, false>, m, seqs, l, q)
+                        : cudaLaunchKernelEx(&cp, k_kv_append_batch<64, false>, m, seqs, l, q);
       if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t ca = config(n * m.nkv * nch, kAT + 32, attn_batch_smem(m), 1);

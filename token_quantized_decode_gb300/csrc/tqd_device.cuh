@@ -242,13 +242,14 @@ struct DevModel {
   const uint8_t* embed;
   const float* out_norm;
   const float2* rope;     // [max_seq][hd/2] (cos, sin)
+  int kv16;               // the KV cache holds f16 elements (the batched kernels only)
 };
 
 // Per-sequence buffers.
 struct DevSeq {
   DevState* state;
   int32_t* tokens;        // [max_seq + 1]: input token of each position
-  float* kcache;          // [n_layers][n_kv_heads][max_seq][head_dim]
+  float* kcache;          // [n_layers][n_kv_heads][max_seq][head_dim] (f16 elements when kv16)
   float* vcache;
   float* x;               // [H] residual stream
   float* qkv;             // [qw + 2 kvw] raw projections

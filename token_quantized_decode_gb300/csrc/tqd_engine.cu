@@ -5,6 +5,7 @@
 // split-K / argmax partials.  Weights are uploaded once; a decode step
 // moves four bytes of token id each way ("One command buffer per token",
 // sections "Resident state" and "One command buffer").
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -135,6 +136,7 @@ int32_t validate_config(const tqd_config* c) {
        "weight_type must be TQD_WEIGHT_Q8_0 or TQD_WEIGHT_BF16");
   need(c->max_seq >= 1 && c->max_seq <= (1 << 24), "max_seq must be in [1, 2^24]");
   need(c->max_batch >= 1 && c->max_batch <= 64, "max_batch must be in [1, 64]");
+  need(c->kv_type == TQD_KV_F32 || c->kv_type == TQD_KV_F16, "kv_type must be TQD_KV_F32 or TQD_KV_F16");
   need(c->schedule == TQD_SCHED_GRAPH || c->schedule == TQD_SCHED_PERSISTENT,
        "schedule must be TQD_SCHED_GRAPH or TQD_SCHED_PERSISTENT");
   need(std::isfinite(c->rope_theta) && c->rope_theta > 0.f, "rope_theta must be > 0");
@@ -449,10 +451,20 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const size_t o_rope = take(sizeof(float2) * static_cast<size_t>(S) * (hd / 2));
   const size_t o_layers = take(sizeof(DevLayer) * L);
   const size_t weights_end = off;
+  // the batched kernels' shapes (several sequences per step, prefill tiles, an f16 cache)
+  DevModel shape{};
+  shape.H = H; shape.nq = nq; shape.nkv = nkv; shape.hd = hd; shape.I = I; shape.qw = qw;
+  const bool batched = batch_supported(shape) && (V + 127) / 128 <= kMaxArgmaxBlocks;
+  const bool kv16 = cfg->kv_type == TQD_KV_F16;
+  if (kv16 && !batched) {
+    set_error("an f16 KV cache runs in the batched kernels, which do not support this shape");
+    tqd_destroy(m);
+    return TQD_ERR_UNSUPPORTED_CONFIG;
+  }
   struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar, gbar,
                   opart, sz, scnt; };
   std::vector<SeqOff> so(cfg->max_batch);
-  const size_t kv_bytes = sizeof(float) * static_cast<size_t>(L) * S * kvw;
+  const size_t kv_bytes = (kv16 ? 2 : 4) * static_cast<size_t>(L) * S * kvw;
   for (int b = 0; b < cfg->max_batch; ++b) {
     so[b].state = take(sizeof(DevState));
     so[b].tokens = take(4 * (static_cast<size_t>(S) + 1));
@@ -482,9 +494,6 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const int bmax = batch_max();
   size_t o_bx = 0, o_bqkv = 0, o_bpo = 0, o_bpml = 0, o_bh = 0, o_bcount = 0, o_bss = 0, o_blm = 0, o_bio = 0,
          o_pslots = 0, o_pstates = 0;
-  DevModel shape{};
-  shape.H = H; shape.nq = nq; shape.nkv = nkv; shape.hd = hd; shape.I = I; shape.qw = qw;
-  const bool batched = batch_supported(shape) && (V + 127) / 128 <= kMaxArgmaxBlocks;
   if (batched) {
     o_bx = take(4ull * bmax * H);
     o_bqkv = take(4ull * bmax * (qw + 2 * kvw));
@@ -641,6 +650,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   dm.embed = base + o_embed;
   dm.out_norm = reinterpret_cast<const float*>(base + o_onorm);
   dm.rope = reinterpret_cast<const float2*>(base + o_rope);
+  dm.kv16 = kv16 ? 1 : 0;
 
   m->seqs.resize(cfg->max_batch);
   for (int b = 0; b < cfg->max_batch; ++b) {
@@ -751,9 +761,22 @@ int32_t tqd_next_pos(tqd_model* m, int32_t seq, int32_t* pos_out) {
   return TQD_OK;
 }
 
+namespace {
+
+// The batch-1 schedules (persistent kernel, per-phase graph) read an f32 cache.
+int32_t refuse_kv16(tqd_model* m, const char* what) {
+  if (m->cfg.kv_type != TQD_KV_F16) return TQD_OK;
+  set_error("%s runs the batch-1 schedules, which read an f32 KV cache; this model's cache is f16 "
+            "(tqd_prefill_batch, tqd_decode_step_batch and tqd_generate_batch[_sampled] run it)", what);
+  return TQD_ERR_UNSUPPORTED_CONFIG;
+}
+
+}  // namespace
+
 int32_t tqd_prefill(tqd_model* m, int32_t seq, const int32_t* ids, int32_t n, int32_t* next_out) {
   int32_t rc = check_model(m, seq);
   if (rc) return rc;
+  if ((rc = refuse_kv16(m, "tqd_prefill"))) return rc;
   if (!ids || !next_out || n <= 0) {
     set_error("prefill needs ids, next_out and n > 0");
     return TQD_ERR_BAD_ARG;
@@ -796,19 +819,37 @@ int32_t tqd_kv_upload(tqd_model* m, int32_t seq, int32_t n_pos, const float* k, 
   SeqSlot& s = m->seqs[seq];
   const size_t kvw = static_cast<size_t>(m->dm.kvw);
   if (n_pos > 0) {
-    // host rows [layer][pos][kv head * head_dim] -> device [layer][kv head][pos][head_dim]
-    const size_t hd = static_cast<size_t>(m->dm.hd);
+    // host rows [layer][pos][kv head * head_dim] -> device [layer][kv head][pos][head_dim];
+    // an f16 cache takes the rows rounded to nearest-even binary16
+    const size_t hd = static_cast<size_t>(m->dm.hd), es = m->dm.kv16 ? 2 : 4;
+    std::vector<__half> k16, v16;
+    const uint8_t* ksrc = reinterpret_cast<const uint8_t*>(k);
+    const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(v);
+    if (m->dm.kv16) {
+      const size_t n = static_cast<size_t>(m->cfg.n_layers) * n_pos * kvw;
+      k16.resize(n);
+      v16.resize(n);
+      for (size_t i = 0; i < n; ++i) {
+        k16[i] = __float2half_rn(k[i]);
+        v16[i] = __float2half_rn(v[i]);
+      }
+      ksrc = reinterpret_cast<const uint8_t*>(k16.data());
+      vsrc = reinterpret_cast<const uint8_t*>(v16.data());
+    }
+    uint8_t* kdev = reinterpret_cast<uint8_t*>(s.d.kcache);
+    uint8_t* vdev = reinterpret_cast<uint8_t*>(s.d.vcache);
     for (int l = 0; l < m->cfg.n_layers; ++l)
       for (int g = 0; g < m->dm.nkv; ++g) {
         const size_t src = (static_cast<size_t>(l) * n_pos) * kvw + g * hd;
         const size_t dst = (static_cast<size_t>(l) * m->dm.nkv + g) * m->cfg.max_seq * hd;
-        CK(cudaMemcpy2DAsync(s.d.kcache + dst, 4 * hd, k + src, 4 * kvw, 4 * hd, n_pos,
+        CK(cudaMemcpy2DAsync(kdev + dst * es, es * hd, ksrc + src * es, es * kvw, es * hd, n_pos,
                              cudaMemcpyHostToDevice, m->stream),
            "upload K");
-        CK(cudaMemcpy2DAsync(s.d.vcache + dst, 4 * hd, v + src, 4 * kvw, 4 * hd, n_pos,
+        CK(cudaMemcpy2DAsync(vdev + dst * es, es * hd, vsrc + src * es, es * kvw, es * hd, n_pos,
                              cudaMemcpyHostToDevice, m->stream),
            "upload V");
       }
+    CK(cudaStreamSynchronize(m->stream), "synchronize");  // the converted rows are copied
   }
   DevState st{};
   st.pos = static_cast<uint32_t>(n_pos);
@@ -824,6 +865,7 @@ int32_t tqd_kv_upload(tqd_model* m, int32_t seq, int32_t n_pos, const float* k, 
 int32_t tqd_decode_step(tqd_model* m, int32_t seq, int32_t token, int32_t pos, int32_t* next_out) {
   int32_t rc = check_model(m, seq);
   if (rc) return rc;
+  if ((rc = refuse_kv16(m, "tqd_decode_step"))) return rc;
   if (!next_out || token < 0 || token >= m->cfg.vocab) {
     set_error("decode_step needs next_out and a token in [0, vocab)");
     return TQD_ERR_BAD_ARG;
@@ -889,6 +931,7 @@ int32_t generate_impl(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_
                       const SampleArgs* sa) {
   int32_t rc = check_model(m, seq);
   if (rc) return rc;
+  if ((rc = refuse_kv16(m, "tqd_generate"))) return rc;
   if (!ids_out || n_steps <= 0 || first_token < 0 || first_token >= m->cfg.vocab) {
     set_error("generate needs ids_out, n_steps > 0 and a first token in [0, vocab)");
     return TQD_ERR_BAD_ARG;
@@ -965,7 +1008,7 @@ namespace {
 int32_t check_batch(tqd_model* m, int32_t n_seq) {
   int32_t rc = check_model(m, 0);
   if (rc) return rc;
-  if (!m->batch_ok || m->cfg.max_batch < 2) {
+  if (!m->batch_ok || (m->cfg.max_batch < 2 && m->cfg.kv_type != TQD_KV_F16)) {
     set_error("this model has no batched step (max_batch must be > 1 and the shape supported)");
     return TQD_ERR_UNSUPPORTED_CONFIG;
   }
@@ -1231,7 +1274,7 @@ int32_t tqd_step_bytes(tqd_model* m, int32_t pos, int64_t* bytes_out) {
     set_error("model, bytes_out and pos >= 0 required");
     return TQD_ERR_BAD_ARG;
   }
-  const int64_t kv_row = 4ll * m->dm.kvw * 2 * m->cfg.n_layers;  // K and V, all layers
+  const int64_t kv_row = (m->dm.kv16 ? 2ll : 4ll) * m->dm.kvw * 2 * m->cfg.n_layers;  // K and V, all layers
   *bytes_out = m->weight_bytes + static_cast<int64_t>(row_bytes(m->cfg.weight_type, m->cfg.hidden)) +
                kv_row * (static_cast<int64_t>(pos) + 1) + kv_row;
   return TQD_OK;
