@@ -43,7 +43,7 @@ extern "C" {
 typedef enum tqd_status {
   TQD_OK = 0,
   TQD_ERR_BAD_ARG = 1,             /* NULL pointer, out-of-range id, bad size */
-  TQD_ERR_UNSUPPORTED_CONFIG = 2,  /* config this build cannot run; see tqd_last_error() */
+  TQD_ERR_UNSUPPORTED_CONFIG = 2,  /* a config the library cannot run; see tqd_last_error() */
   TQD_ERR_NO_DEVICE = 3,           /* no CUDA device, or not an sm_103 device */
   TQD_ERR_CUDA = 4,                /* a CUDA runtime call failed (model poisoned) */
   TQD_ERR_OOM = 5,                 /* device allocation failed (nothing leaked) */
