@@ -3,6 +3,7 @@ numpy / scipy as independent decoders and contractions, closed forms,
 invariants of the mathematics, brute force on tiny inputs, and the worked
 cases of inferno.rs "IV.4: One command buffer per token", "The correctness
 ladder"."""
+import dataclasses
 import math
 
 import numpy as np
@@ -382,3 +383,69 @@ def test_step_rejects_bad_positions():
         om.step(1, 1)  # skips position 0
     with pytest.raises(ValueError):
         om.step(synth.TINY.vocab, 0)
+
+
+def _scaled_q8_scales(w: np.ndarray, factor: float) -> np.ndarray:
+    """Q8_0 bytes with every block's f16 scale multiplied by `factor` (a power
+    of two that keeps the scales normal, so the product is exact in f16)."""
+    out = w.copy()
+    blocks = out.reshape(-1, 34)
+    s = blocks[:, :2].copy().view(np.float16).astype(np.float64)
+    t = (s * factor).astype(np.float16)
+    assert np.array_equal(t.astype(np.float64), s * factor)
+    blocks[:, :2] = t.view(np.uint8).reshape(-1, 2)
+    return out
+
+
+def _qk_logits(m, ids):
+    om = oracle.OracleModel(m, 16)
+    _, logits = om.prefill(ids)
+    return logits
+
+
+def test_qk_norm_removes_the_scale_of_q_and_k():
+    """Per-head RMSNorm of q and of k ("Eight kernels", rms_norm_row, applied
+    after the projections): with eps = 0 it is invariant to a positive scale
+    of its input, so multiplying every Q8_0 scale of W_q (then of W_k) by 4
+    leaves the logits unchanged, while the same change to W_v (which is not
+    normed) changes them.  Fails if the oracle drops the q side of the norm."""
+    cfg = dataclasses.replace(synth.TINY, rms_eps=0.0)
+    m = synth.make_model(cfg, 3)
+    ids = synth.token_ids(1000, 5, 6, cfg.vocab)
+    base = _qk_logits(m, ids)
+    scale = float(np.abs(base).max())
+    for name in ("wq", "wk"):
+        layers = [dict(d) for d in m.layers]
+        for d in layers:
+            d[name] = _scaled_q8_scales(d[name], 4.0)
+        got = _qk_logits(dataclasses.replace(m, layers=layers), ids)
+        assert np.max(np.abs(got - base)) <= 1e-12 * scale, name
+    layers = [dict(d) for d in m.layers]
+    for d in layers:
+        d["wv"] = _scaled_q8_scales(d["wv"], 4.0)
+    assert np.max(np.abs(_qk_logits(dataclasses.replace(m, layers=layers), ids) - base)) > 1e-3 * scale
+
+
+def test_qk_norm_gains_act_on_their_own_side():
+    """A constant gain c on q's norm scales every attention score by c, and so
+    does the same gain on k's norm: the two models give the same logits (to
+    rounding), and both differ from c = 1.  Fails if the oracle applied the
+    k-norm gain to q (then the first model scales by 1 and the second by c^2)
+    or skipped the q-side norm."""
+    cfg = synth.TINY
+    m = synth.make_model(cfg, 4)
+    ids = synth.token_ids(1000, 6, 6, cfg.vocab)
+
+    def with_gains(gq, gk):
+        layers = [dict(d) for d in m.layers]
+        for d in layers:
+            d["q_norm"] = np.full(cfg.head_dim, gq, dtype=np.float32)
+            d["k_norm"] = np.full(cfg.head_dim, gk, dtype=np.float32)
+        return _qk_logits(dataclasses.replace(m, layers=layers), ids)
+
+    one = with_gains(1.0, 1.0)
+    on_q = with_gains(4.0, 1.0)
+    on_k = with_gains(1.0, 4.0)
+    scale = float(np.abs(one).max())
+    assert np.max(np.abs(on_q - on_k)) <= 1e-12 * scale
+    assert np.max(np.abs(on_q - one)) > 1e-3 * scale
