@@ -227,16 +227,21 @@ int32_t tqd_generate_batch(tqd_model* model, int32_t n_seq, const int32_t* first
  * temperature <= 0 falls back to the greedy token and top_k = 1 reproduces
  * it).  The draw, in this order: the penalties on the distinct tokens among
  * the sequence's inputs so far (count c): l = l > 0 ? l / repeat : l * repeat,
- * then l -= presence, then l -= frequency * c; z = l / temperature; top_k
- * keeps the top_k largest z (ties to the lower index); top_p keeps, of those
- * in the order (z descending, index ascending), the shortest prefix whose
- * probability reaches top_p of their total; min_p keeps z - z_max >=
- * ln(min_p); the token is drawn from the kept probabilities exp(z - z_max)
- * by inverting their running sum in index order at u = the top 24 bits of
- * splitmix64's output number `position` from `seed`, times 2^-24, where
- * position is the drawn token's position.  Every float step is f32; the
- * probabilities are summed as integers in units of 2^-32 of the most likely
- * token's, so a draw is deterministic. */
+ * then l -= presence, then l -= frequency * c (NaN logits count as -inf);
+ * the tokens are ranked by that penalised l, descending, ties to the lower
+ * index (division by a positive temperature keeps the order, so ranking
+ * before it keeps top_k = 1 the greedy token even where l / temperature
+ * merges two logits); top_k keeps the first top_k of that order; top_p keeps,
+ * of those, the shortest prefix of the order whose probability reaches top_p
+ * of their total; min_p keeps z - z_max >= ln(min_p), z = l / temperature;
+ * the token is drawn from the kept probabilities exp(z - z_max) by inverting
+ * their running sum in index order at u = the top 24 bits of splitmix64's
+ * output number `position` from `seed`, times 2^-24, where position is the
+ * drawn token's position.  Every float step is f32; the probabilities are
+ * summed as integers in units of 2^-32 of the most likely token's, so a draw
+ * is deterministic.  A temperature so small that l_max / temperature
+ * overflows f32 draws the greedy token of the penalised logits (the limit
+ * of the distribution as the temperature goes to 0). */
 typedef struct tqd_sampling {
   float temperature;        /* <= 0: the greedy token */
   int32_t top_k;            /* 0: off; 1: the greedy token of the penalised logits */
@@ -352,6 +357,18 @@ int32_t tqd_op_silu_mul(const float* g, const float* u, int64_t n, float* out, v
 int32_t tqd_op_argmax(const float* x, int64_t n, int32_t* idx_out, void* scratch, void* stream);
 size_t tqd_argmax_scratch_bytes(void);
 
+/* Seeded sampling on caller memory, the draw of tqd_sample (controls and
+ * order as documented at tqd_sampling): logits f32 [vocab] (device); tokens
+ * int32 [n_inputs + 1] (device): tokens[0, n_inputs) are the inputs so far
+ * (the penalties' history) and the drawn token, for position n_inputs, is
+ * written to tokens[n_inputs] (-1 when every logit is NaN).  n_inputs >= 1.
+ * scratch: caller-owned device memory of tqd_sample_scratch_bytes(vocab)
+ * bytes (the logits are copied there, padded for 16-byte loads).  BAD_ARG
+ * for out-of-range controls as tqd_sample. */
+int32_t tqd_op_sample(const float* logits, int32_t vocab, int32_t* tokens, int32_t n_inputs,
+                      const tqd_sampling* sampling, void* scratch, void* stream);
+size_t tqd_sample_scratch_bytes(int32_t vocab);
+
 /* Allocation-free variant of tqd_op_attention (the pages have no counterpart;
  * this is an interface for callers that may not allocate device memory while
  * they run, e.g. a serving loop whose memory budget is fixed at start-up, or a
@@ -363,6 +380,8 @@ size_t tqd_argmax_scratch_bytes(void);
  * allocated by the call.
  *  - The first call on a device looks up that array's device address (with
  *    the device current); make that first call before any stream capture.
+ *    A lookup that fails returns TQD_ERR_CUDA and is tried again by the
+ *    next call; only a successful one is kept.
  *  - Calls whose tqd_attention_scratch_bytes(...) exceeds the array's size
  *    return TQD_ERR_BAD_ARG (see tqd_last_error()).
  *  - Every call on a device shares the array and leaves its contents behind;

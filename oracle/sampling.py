@@ -10,21 +10,29 @@ Everything else is a reading of those names, in this order:
 
 1. penalties, once per distinct token t among the sequence's inputs so far
    (count c_t): a = l_t / r if l_t > 0 else l_t * r; a = a - presence;
-   a = a - frequency * c_t (each an f32 operation, in that order);
-2. temperature: z = l / T in f32 (NaN logits become -inf);
-3. top_k (1 <= k < V): the k largest z, ties to the lower index;
-4. top_p (p < 1): of those, in the order (z descending, index ascending), the
-   shortest prefix whose probability mass reaches p of the kept mass;
-5. min_p (> 0): keep z_i - z_max >= f32(ln min_p), the difference in f32;
+   a = a - frequency * c_t (each an f32 operation, in that order); NaN
+   logits become -inf;
+2. the order: tokens ranked by the penalised logit l descending, index
+   ascending.  Division by T > 0 preserves that order, so ranking before the
+   division keeps top_k = 1 equal to the greedy token even where l / T rounds
+   two adjacent logits to the same f32 value;
+3. top_k (1 <= k < V): the first k tokens of that order;
+4. top_p (p < 1): of those, in that order, the shortest prefix whose
+   probability mass reaches p of the kept mass;
+5. min_p (> 0): keep z_i - z_max >= f32(ln min_p), with z = l / T in f32 and
+   the difference in f32;
 6. draw: u = (splitmix64 draw at the sampled token's position) top 24 bits
    * 2^-24; the token is the first kept one in index order whose running
    mass exceeds u times the kept mass.
 
-Probabilities are exp(z_i - z_max) in double precision.  Where a float
-decides a kept set or a draw, the decision is taken on the same f32 values
-the device uses (steps 1, 2, 3, 5); steps 4 and 6 compare masses, which the
-device carries in fixed point, so ``sample`` also returns how far the
-decisive masses lie from their boundaries.
+Probabilities are exp(z_i - z_max) in double precision, z = l / T in f32.
+When l_max / T overflows f32 to +-inf (a temperature so small that the
+distribution is the limit T -> 0), the draw is the greedy token of the
+penalised logits.
+Where a float decides a kept set or a draw, the decision is taken on the same
+f32 values the device uses (steps 1, 2, 3, 5); steps 4 and 6 compare masses,
+which the device carries in fixed point, so ``sample`` also returns how far
+the decisive masses lie from their boundaries.
 """
 from __future__ import annotations
 
@@ -86,9 +94,16 @@ def kept(logits, history, temperature: float, top_k: int = 0, top_p: float = 1.0
     V = len(logits)
     l = penalised(logits, history, repeat, presence, frequency)
     l = np.where(np.isnan(l), np.float32(-np.inf), l).astype(np.float32)
-    z = (l / np.float32(temperature)).astype(np.float32)
-    order = np.lexsort((np.arange(V), -z.astype(np.float64)))   # z descending, index ascending
-    zmax = z[order[0]]
+    order = np.lexsort((np.arange(V), -l.astype(np.float64)))   # l descending, index ascending
+    with np.errstate(over="ignore"):
+        z = (l / np.float32(temperature)).astype(np.float32)
+        zmax = np.float32(l[order[0]] / np.float32(temperature))
+    if np.isinf(zmax) and np.isfinite(l[order[0]]):                # the T -> 0 limit: greedy on l
+        w = np.zeros(V)
+        w[order[0]] = 1.0
+        keep = np.zeros(V, dtype=bool)
+        keep[order[0]] = True
+        return w, keep, np.inf
     w = np.exp(z.astype(np.float64) - np.float64(zmax))
     keep = np.ones(V, dtype=bool)
     margin = np.inf

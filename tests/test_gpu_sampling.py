@@ -231,3 +231,66 @@ def test_sampling_refusals(tqd):
         dec.sample(tqd.sampling())
     assert ei.value.name == "TQD_ERR_NOT_PREFILLED"
     dec.close()
+
+
+def op_draw(tqd, logits, hist, p, seed):
+    """tqd_op_sample on caller tensors: the token drawn after `hist`."""
+    from token_quantized_decode_gb300 import ops
+    V = len(logits)
+    lg = torch.tensor(np.asarray(logits, dtype=np.float32), device="cuda")
+    toks = torch.tensor(list(hist) + [0], dtype=torch.int32, device="cuda")
+    scratch = torch.empty(ops.tqd_sample_scratch_bytes(V), dtype=torch.uint8, device="cuda")
+    ops.tqd_op_sample(lg, V, toks, len(hist), tqd.sampling(seed=seed, **p), scratch)
+    torch.cuda.synchronize()
+    return int(toks[-1].item())
+
+
+def test_op_sample_matches_the_oracle(tqd):
+    """The operator entry point on planted logits (a peaked distribution, so
+    the draws are mostly unique) against the sampling oracle."""
+    rng = np.random.default_rng(21)
+    V = 1001
+    unique = 0
+    for i, p in enumerate(PARAMS):
+        for seed in range(4):
+            l = (rng.normal(size=V) * 3).astype(np.float32)
+            hist = rng.integers(0, V, size=9)
+            unique += check_draw(op_draw(tqd, l, hist, p, 100 * i + seed), l, hist, len(hist), p,
+                                 100 * i + seed, f"params {i} seed {seed}")
+    assert unique >= 0.8 * len(PARAMS) * 4
+
+
+def test_top_k_one_is_greedy_where_the_temperature_merges_two_logits(tqd):
+    """Two adjacent f32 logits l_lo < l_hi with l_lo / T == l_hi / T in f32,
+    the lower index holding l_lo: top_k = 1 and a tiny top_p still give the
+    greedy token, top_k = 2 keeps both."""
+    T = 3.0
+    t = np.float32(T)
+    lo = np.float32(7.0)
+    while np.float32(lo / t) != np.float32(np.nextafter(lo, np.float32(np.inf)) / t):
+        lo = np.nextafter(lo, np.float32(np.inf))
+    hi = np.nextafter(lo, np.float32(np.inf))
+    rng = np.random.default_rng(22)
+    for i in range(8):
+        l = rng.normal(size=3000).astype(np.float32)
+        a, b = sorted(rng.choice(3000, 2, replace=False))
+        l[a], l[b] = lo, hi
+        for seed in range(3):
+            assert op_draw(tqd, l, [int(a)], dict(temperature=T, top_k=1), seed) == b
+            assert op_draw(tqd, l, [1, 2], dict(temperature=T, top_p=1e-6), seed) == b
+            assert op_draw(tqd, l, [3], dict(temperature=T, top_k=2), seed) in (a, b)
+
+
+def test_an_overflowing_temperature_is_the_greedy_limit(tqd):
+    """l_max / T beyond f32 (T = 1e-38, and negative logits at 1e-39): the
+    greedy token of the penalised logits."""
+    rng = np.random.default_rng(23)
+    for i in range(6):
+        l = (rng.normal(size=2000) * 4).astype(np.float32)
+        hist = rng.integers(0, 2000, size=7)
+        p = dict(temperature=1e-38, top_p=0.9, repeat_penalty=1.3, presence_penalty=0.2)
+        want = S.greedy(S.penalised(l, hist, 1.3, 0.2, 0.0))
+        assert S.sample(l, hist, len(hist), 1e-38, top_p=0.9, repeat=1.3, presence=0.2)[0] == want
+        assert op_draw(tqd, l, hist, p, i) == want
+    l = np.array([-3.0, -1.0, -2.0, -1.0, -5.0], dtype=np.float32)
+    assert op_draw(tqd, l, [0], dict(temperature=1e-39), 1) == 1

@@ -137,3 +137,60 @@ def test_boundaries_inside_ties_follow_the_index_order():
     assert ks(top_p=0.5) == {1, 0}        # 0.4 < 0.5 <= 0.6
     assert ks(top_p=0.7) == {1, 0, 2}     # 0.6 < 0.7 <= 0.8
     assert ks(top_k=3, top_p=0.9) == {1, 0, 2}
+
+
+def colliding_pair(T):
+    """Adjacent f32 values lo < hi (searched upward from 7) with
+    f32(lo / T) == f32(hi / T)."""
+    t = np.float32(T)
+    lo = np.float32(7.0)
+    for _ in range(1000):
+        hi = np.nextafter(lo, np.float32(np.inf))
+        if np.float32(lo / t) == np.float32(hi / t):
+            return lo, hi
+        lo = hi
+    raise AssertionError("no colliding pair")
+
+
+def test_top_k_one_is_greedy_where_the_temperature_merges_two_logits():
+    # l_hi > l_lo but l_hi / T == l_lo / T in f32; the lower index holds l_lo,
+    # so ranking on z with ties to the lower index would keep the wrong token
+    T = 3.0
+    lo, hi = colliding_pair(T)
+    rng = np.random.default_rng(4)
+    for i in range(50):
+        l = rng.normal(size=300).astype(np.float32)
+        a, b = sorted(rng.choice(300, 2, replace=False))
+        l[a], l[b] = lo, hi
+        assert S.greedy(l) == b
+        assert S.sample(l, [], i, T, top_k=1, seed=i)[0] == b
+        _, keep, _ = S.kept(l, [], T, top_k=2)
+        assert set(np.nonzero(keep)[0].tolist()) == {a, b}
+        _, keep, _ = S.kept(l, [], T, top_k=1, top_p=0.3, min_p=0.5)
+        assert np.nonzero(keep)[0].tolist() == [b]
+
+
+def test_the_order_applies_after_the_penalties():
+    # the penalty moves token 2 below token 0; top_k = 1 is then the greedy
+    # token of the penalised logits
+    l = np.array([1.0, 0.5, 1.5], dtype=np.float32)
+    assert S.sample(l, [2], 0, 1.0, top_k=1, repeat=2.0)[0] == 0
+    assert S.sample(l, [2], 0, 1.0, top_k=1)[0] == 2
+
+
+def test_an_overflowing_temperature_is_the_greedy_limit():
+    # l_max / T beyond f32: every draw is the greedy token of the penalised logits
+    rng = np.random.default_rng(6)
+    for i in range(20):
+        l = rng.normal(size=100).astype(np.float32) * 4
+        hist = rng.integers(0, 100, size=5)
+        want = S.greedy(S.penalised(l, hist, 1.3, 0.2, 0.0))
+        for T in (1e-38, 1e-40):
+            assert np.isinf(np.float32(np.max(np.abs(l)) / np.float32(T)))
+            assert S.sample(l, hist, i, T, top_p=0.9, repeat=1.3, presence=0.2, seed=i)[0] == want
+
+
+def test_an_overflowing_temperature_on_negative_logits_is_the_greedy_limit():
+    l = np.array([-3.0, -1.0, -2.0, -1.0], dtype=np.float32)
+    assert S.sample(l, [], 0, 1e-39, seed=1)[0] == 1
+    assert S.sample(l, [], 0, 1e-39, top_k=2, seed=1)[0] == 1

@@ -105,6 +105,8 @@ def lib():
         "tqd_op_silu_mul": (i32, [vp, vp, i64, vp, vp]),
         "tqd_op_argmax": (i32, [vp, i64, vp, vp, vp]),
         "tqd_argmax_scratch_bytes": (sz, []),
+        "tqd_op_sample": (i32, [vp, i32, vp, i32, P(tqd_sampling), vp, vp]),
+        "tqd_sample_scratch_bytes": (sz, [i32]),
         "tqd_op_attention_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "tqd_op_attention_noalloc_max_scratch": (sz, []),
     }
@@ -126,7 +128,7 @@ def exported_symbols():
         "tqd_phase_count", "tqd_step_bytes", "tqd_op_q8_0_repack", "tqd_op_q8_0_matvec",
         "tqd_op_bf16_matvec", "tqd_op_rmsnorm", "tqd_op_rope_table", "tqd_op_rope", "tqd_op_attention",
         "tqd_attention_scratch_bytes", "tqd_op_wait_selftest", "tqd_op_silu_mul", "tqd_op_argmax", "tqd_argmax_scratch_bytes",
-        "tqd_op_attention_noalloc", "tqd_op_attention_noalloc_max_scratch",
+        "tqd_op_sample", "tqd_sample_scratch_bytes", "tqd_op_attention_noalloc", "tqd_op_attention_noalloc_max_scratch",
     ]
 
 

@@ -266,7 +266,7 @@ struct DevSeq {
   float* x_mid;           // [H] residual after the attention block
   DevBarrier* gbar;       // per kv group g: [16 g] QKV rows written, [16 g + 8] attention partials written
   float* opart;           // [n_kv][H] per-group partial O products (persistent schedule)
-  float* sz;              // [V] the sampler's tempered, penalised logits
+  float* sz;              // [V] the sampler's penalised logits
   uint32_t* scnt;         // [V] the sampler's input-token counts (zero between draws)
 };
 

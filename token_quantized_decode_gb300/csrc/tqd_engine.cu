@@ -965,6 +965,12 @@ int32_t generate_impl(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_
 
 }  // namespace
 
+extern "C++" {
+namespace tqd {
+int32_t sampling_args(const tqd_sampling* p, SampleArgs& a, bool* greedy) { return sample_args(p, a, greedy); }
+}  // namespace tqd
+}
+
 int32_t tqd_generate(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_steps, int32_t* ids_out) {
   return generate_impl(m, seq, first_token, n_steps, ids_out, nullptr);
 }

@@ -9,6 +9,8 @@
 
 #include "tqd_device.cuh"
 
+struct tqd_sampling;  // include/tqd.h
+
 namespace tqd {
 
 constexpr int kMatvecThreads = 256;      // 8 warps per matvec block (graph schedule)
@@ -136,6 +138,8 @@ struct SampleArgs {
   unsigned long long seed;
 };
 cudaError_t launch_sample(const DevSeq* seqs, int n, int V, int max_seq, const SampleArgs& a, cudaStream_t st);
+// Validate the caller's sampling controls into a, and say whether they are greedy.
+int32_t sampling_args(const ::tqd_sampling* p, SampleArgs& a, bool* greedy);
 
 // The bounded-wait self-test (tqd_op_wait_selftest): runs it on st and
 // returns the error bits its waits set.

@@ -125,4 +125,45 @@ int32_t tqd_op_argmax(const float* x, int64_t n, int32_t* idx_out, void* scratch
   return status_of(launch_op_argmax(x, n, idx_out, cv, ci, cnt, static_cast<cudaStream_t>(stream)));
 }
 
+size_t tqd_sample_scratch_bytes(int32_t vocab) {
+  if (vocab <= 0) return 0;
+  const size_t v4 = (static_cast<size_t>(vocab) + 3) / 4 * 4;
+  return 256 + 3 * 4 * v4;
+}
+
+int32_t tqd_op_sample(const float* logits, int32_t vocab, int32_t* tokens, int32_t n_inputs,
+                      const tqd_sampling* sampling, void* scratch, void* stream) {
+  if (!logits || !tokens || !scratch || vocab <= 0 || n_inputs < 1 || n_inputs >= 0x7FFFFFFF ||
+      reinterpret_cast<uintptr_t>(scratch) % 16)
+    return TQD_ERR_BAD_ARG;
+  SampleArgs a{};
+  bool greedy = false;
+  int32_t rc = sampling_args(sampling, a, &greedy);
+  if (rc) return rc;
+  if (greedy) a.temperature = 0.f;
+  // scratch: the sequence descriptor and its state, then the padded logits,
+  // the penalised logits and the input counts ([vocab rounded up to 4] each)
+  const size_t v4 = (static_cast<size_t>(vocab) + 3) / 4 * 4;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  DevSeq* dseq = reinterpret_cast<DevSeq*>(base);
+  DevState* dstate = reinterpret_cast<DevState*>(base + 192);
+  float* lg = reinterpret_cast<float*>(base + 256);
+  DevSeq h{};
+  h.state = dstate;
+  h.tokens = tokens;
+  h.logits = lg;
+  h.sz = lg + v4;
+  h.scnt = reinterpret_cast<uint32_t*>(lg + 2 * v4);
+  static_assert(sizeof(DevSeq) <= 192, "descriptor fits the scratch header");
+  DevState st{static_cast<uint32_t>(n_inputs), 0u, 0u, 0u};
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // copies from pageable host memory are staged before cudaMemcpyAsync returns
+  cudaError_t e = cudaMemcpyAsync(dseq, &h, sizeof(h), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dstate, &st, sizeof(st), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(lg, logits, 4ull * vocab, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h.scnt, 0, 4 * v4, s);
+  if (e == cudaSuccess) e = launch_sample(dseq, 1, vocab, n_inputs, a, s);
+  return status_of(e);
+}
+
 }  // extern "C"

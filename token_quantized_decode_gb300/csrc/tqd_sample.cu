@@ -6,19 +6,25 @@
 //   1. penalties on the distinct tokens among the sequence's inputs (counted
 //      in a per-sequence array the block leaves zeroed), each an f32
 //      operation: a = l > 0 ? l / r : l * r; a -= presence; a -= frequency * c;
-//   2. z = l / T in f32 (NaN -> -inf), into a per-sequence array;
-//   3. top_k: the k largest z, ties to the lower index;
-//   4. top_p: of those, in the order (z descending, index ascending), the
-//      shortest prefix whose mass reaches p of their mass;
-//   5. min_p: z - z_max >= ln(min_p) (f32 difference; the log taken on the host);
+//      NaN -> -inf; the penalised logits go to a per-sequence array;
+//   2. the order: penalised logit l descending, index ascending.  Division by
+//      T > 0 keeps that order, and ranking before the division keeps top_k = 1
+//      equal to the greedy token where l / T merges two adjacent logits;
+//   3. top_k: the first k tokens of that order;
+//   4. top_p: of those, in that order, the shortest prefix whose mass reaches
+//      p of their mass;
+//   5. min_p: z - z_max >= ln(min_p), z = l / T in f32 (f32 difference; the
+//      log taken on the host);
 //   6. draw: u = the top 24 bits of splitmix64's output at the drawn token's
 //      position, times 2^-24; the token is the first kept one in index order
 //      whose running mass exceeds u times the kept mass.
 // Masses are exp(z - z_max) in f32, carried as integers in units of 2^-32 of
 // the most likely token's, so every sum is exact and independent of order and
-// the draw is deterministic.  A boundary (steps 3, 4) is found by a histogram
-// of the values over [z_min, z_max], then an exact sort of the boundary bin's
-// tokens (a zoom into the bin when it holds too many), ties in index order.
+// the draw is deterministic.  When l_max / T overflows f32 (the limit T -> 0)
+// the draw is the greedy token of the penalised logits.  A boundary (steps 3,
+// 4) is found by a histogram of the values over [l_min, l_max], then an exact
+// sort of the boundary bin's tokens (a zoom into the bin when it holds too
+// many), ties in index order.
 #include <climits>
 
 #include "tqd_internal.h"
@@ -64,16 +70,24 @@ __device__ __forceinline__ unsigned long long wfix(float z, float zmax) {
   return __float2ull_rz(__fmul_rn(expf(__fsub_rn(z, zmax)), kFix));
 }
 
-// A token v of value z is kept when it passes every stage set so far.
+// The mass of a token with penalised logit l: z = l / T, weight exp(z - z_max).
+struct LWeight {
+  float temp, zmax;
+  __device__ unsigned long long operator()(float l) const { return wfix(__fdiv_rn(l, temp), zmax); }
+};
+
+// A token v of penalised logit l is kept when it passes every stage set so far.
 struct Keep {
   float kz;
-  int ki;      // top_k: z > kz, or z == kz and v <= ki
+  int ki;      // top_k: l > kz, or l == kz and v <= ki
   float pz;
   int pi;      // top_p: the same
+  float temp;
   float zmax;
-  float lnmp;  // min_p: z - zmax >= lnmp (-inf when off)
-  __device__ bool operator()(int v, float z) const {
-    return (z > kz || (z == kz && v <= ki)) && (z > pz || (z == pz && v <= pi)) && __fsub_rn(z, zmax) >= lnmp;
+  float lnmp;  // min_p: l / T - zmax >= lnmp (-inf when off)
+  __device__ bool operator()(int v, float l) const {
+    return (l > kz || (l == kz && v <= ki)) && (l > pz || (l == pz && v <= pi)) &&
+           __fsub_rn(__fdiv_rn(l, temp), zmax) >= lnmp;
   }
 };
 
@@ -450,7 +464,7 @@ __device__ Sel select_top(const float* z, int V, In in, Wt weight, unsigned long
 
 // top_k <= kSCand: every token at or above the top_k boundary's value bin,
 // sorted (z descending, index ascending) into sm.cand[0, n); its first top_k
-// entries are the kept set.  A count histogram over [zmin, zmax] (one atomic
+// entries are the kept set.  A count histogram over [l_min, l_max] (one atomic
 // per distinct bin per warp) finds the bin; -1 when the tokens down to that
 // bin do not fit (or the finite values hold fewer than top_k tokens).
 __device__ int topk_list(const float* z, int V, int k, float hi, float lo_all, SampleSm& sm) {
@@ -600,10 +614,10 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
       const int x = tok[i];
       if (x >= 0 && x < V) atomicAdd(&cnt[x], 1u);
     }
-  // z = penalised l / T, four float4 groups in flight per thread; the counts
+  // the penalised logits, four float4 groups in flight per thread; the counts
   // are read beside the logits and zeroed; the padding gets -inf
   __syncthreads();
-  float zmax = -INFINITY, zmin = INFINITY;
+  float lmax = -INFINITY, lmin = INFINITY;
   {
     const int n4 = (V + 3) >> 2;
     const float4* l4 = reinterpret_cast<const float4*>(lg);
@@ -617,10 +631,9 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
         l = __fsub_rn(l, __fmul_rn(a.frequency, static_cast<float>(c)));
         if (isnan(l)) return -INFINITY;
       }
-      const float r = __fdiv_rn(l, a.temperature);
-      zmax = fmaxf(zmax, r);
-      if (r > -INFINITY) zmin = fminf(zmin, r);
-      return r;
+      lmax = fmaxf(lmax, l);
+      if (l > -INFINITY) lmin = fminf(lmin, l);
+      return l;
     };
     for (int g0 = t; g0 < n4; g0 += 4 * kSThreads) {
       float4 q[4];
@@ -643,22 +656,30 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
       }
     }
   }
-  block_maxmin(zmax, zmin, sm);
-  if (!(zmax > -INFINITY) || !(zmax < INFINITY)) {  // every logit NaN, or z overflowed
+  block_maxmin(lmax, lmin, sm);
+  if (!(lmax > -INFINITY)) {  // every logit NaN
     if (t == 0) {
       atomicOr(&s.state->err, kErrAllNaN);
       tok[S] = -1;
     }
     return;
   }
+  const float zmax = __fdiv_rn(lmax, a.temperature);
+  if (!(zmax > -INFINITY && zmax < INFINITY)) {  // l_max / T overflows: the T -> 0 limit, greedy on l
+    const float lm = lmax;
+    const int v = first_over(z, V, [lm](int, float lv) { return lv == lm ? 1ull : 0ull; }, 0ull, sm);
+    if (t == 0) tok[S] = v;
+    return;
+  }
+  const LWeight wl{a.temperature, zmax};
   const unsigned long long m24 = mix64(a.seed + (static_cast<unsigned long long>(S) + 1ull) * kGolden) >> 40;
-  Keep kp{-INFINITY, INT_MAX, -INFINITY, INT_MAX, zmax, a.ln_min_p};
+  Keep kp{-INFINITY, INT_MAX, -INFINITY, INT_MAX, a.temperature, zmax, a.ln_min_p};
   if (a.top_k >= 1 && a.top_k < V && a.top_k <= kSCand) {
     // the kept tokens fit shared memory: top_p, min_p and the draw on that list
-    const int n = topk_list(z, V, a.top_k, zmax, zmin, sm);
+    const int n = topk_list(z, V, a.top_k, lmax, lmin, sm);
     if (n >= 0) {
       const int K = a.top_k;
-      auto w_desc = [&](int i) { return wfix(key_float(static_cast<uint32_t>(sm.cand[i] >> 32)), zmax); };
+      auto w_desc = [&](int i) { return wl(key_float(static_cast<uint32_t>(sm.cand[i] >> 32))); };
       int nk = K;
       if (a.top_p < 1.f) {
         unsigned long long wk = 0;
@@ -677,8 +698,8 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
         const unsigned long long c = sm.cand[i];
         bool keep = false;
         if (i < nk) {
-          const float zv = key_float(static_cast<uint32_t>(c >> 32));
-          keep = __fsub_rn(zv, zmax) >= a.ln_min_p;
+          const float lv = key_float(static_cast<uint32_t>(c >> 32));
+          keep = __fsub_rn(__fdiv_rn(lv, a.temperature), zmax) >= a.ln_min_p;
         }
         const unsigned long long v = 0xFFFFFFFFull - (c & 0xFFFFFFFFull);
         sm.cand[i] = keep ? ((v << 32) | (c >> 32)) : ~0ull;
@@ -686,7 +707,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
       }
       const int nkept = static_cast<int>(block_sum(kept, sm));
       sort_cand(P, false, sm);
-      auto w_idx = [&](int i) { return wfix(key_float(static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull)), zmax); };
+      auto w_idx = [&](int i) { return wl(key_float(static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull))); };
       unsigned long long W = 0;
       for (int i = t; i < nkept; i += kSThreads) W += w_idx(i);
       W = block_sum(W, sm);
@@ -699,7 +720,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
   if (a.top_k >= 1 && a.top_k < V) {
     const Sel r = select_top(
         z, V, [](int, float) { return true; }, [](int, float) { return 1ull; },
-        static_cast<unsigned long long>(a.top_k), 0.f, zmax, zmin, sm);
+        static_cast<unsigned long long>(a.top_k), 0.f, lmax, lmin, sm);
     kp.kz = r.zb;
     kp.ki = r.ib;
   }
@@ -710,7 +731,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
     const int ki = kp.ki;
     const Sel r = select_top(
         z, V, [kz, ki](int v, float zv) { return zv > kz || (zv == kz && v <= ki); },
-        [zmax](int, float zv) { return wfix(zv, zmax); }, 0ull, a.top_p, zmax, fmaxf(zmin, kz), sm);
+        [wl](int, float lv) { return wl(lv); }, 0ull, a.top_p, lmax, fmaxf(lmin, kz), sm);
     kp.pz = r.zb;
     kp.pi = r.ib;
     W = r.wsel;  // the kept mass, unless min_p removes more
@@ -719,14 +740,14 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
   if (!have_w) {
     W = 0;
     each4(z, V, [&](int v, float zv) {
-      if (kp(v, zv)) W += wfix(zv, zmax);
+      if (kp(v, zv)) W += wl(zv);
     });
     W = block_sum(W, sm);
   }
   // the draw
   const unsigned long long target = (W >> 24) * m24 + (((W & 0xFFFFFFull) * m24) >> 24);  // floor(u W)
   const int v = first_over(
-      z, V, [&](int i, float zv) { return kp(i, zv) ? wfix(zv, zmax) : 0ull; }, target, sm);
+      z, V, [&](int i, float zv) { return kp(i, zv) ? wl(zv) : 0ull; }, target, sm);
   if (t == 0) tok[S] = v < V ? v : V - 1;
 }
 

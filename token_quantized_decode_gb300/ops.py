@@ -83,3 +83,16 @@ def tqd_argmax_scratch_bytes() -> int:
 def tqd_op_argmax(x, n: int, idx_out, scratch, stream=None):
     check(lib().tqd_op_argmax(x.data_ptr(), n, idx_out.data_ptr(), scratch.data_ptr(), _s(stream)),
           "tqd_op_argmax")
+
+
+def tqd_sample_scratch_bytes(vocab: int) -> int:
+    return int(lib().tqd_sample_scratch_bytes(vocab))
+
+
+def tqd_op_sample(logits, vocab: int, tokens, n_inputs: int, params, scratch, stream=None):
+    """The seeded draw of tqd_sample on caller tensors: tokens[:n_inputs] are
+    the inputs so far, the drawn token is written to tokens[n_inputs]."""
+    import ctypes
+    check(lib().tqd_op_sample(logits.data_ptr(), vocab, tokens.data_ptr(), n_inputs, ctypes.byref(params),
+                              scratch.data_ptr(), _s(stream)),
+          "tqd_op_sample")
