@@ -28,9 +28,23 @@ constexpr int kMaxDevices = 64;
 // head.  Shared by all calls on a device; see the contract in tqd.h.
 static __device__ __align__(256) unsigned char g_attention_scratch[kScratchBytes];
 
-std::once_flag g_once[kMaxDevices];
+// The array's device address per device, looked up on first use; a failed
+// lookup (for instance inside a stream capture) is not remembered, so the next
+// call tries again.
+std::mutex g_lookup_mu[kMaxDevices];
 void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+
+cudaError_t scratch_address(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_lookup_mu[dev]);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_attention_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -61,17 +75,17 @@ int32_t tqd_op_attention_noalloc(const float* q, const float* K, const float* V,
     set_last_error("tqd_op_attention_noalloc: no usable current device");
     return e != cudaSuccess ? TQD_ERR_CUDA : TQD_ERR_NO_DEVICE;
   }
-  // Once per device, with that device current: the array's device address
-  // (its name in host code is only a stand-in for the symbol).
-  std::call_once(g_once[dev], [dev]() {
-    g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_attention_scratch);
-  });
-  if (g_scratch_err[dev] != cudaSuccess) {
+  // With this device current, the array's device address (its name in host
+  // code is only a stand-in for the symbol), looked up once it succeeds.
+  void* base = nullptr;
+  e = scratch_address(dev, &base);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // the failed lookup leaves no error behind for later calls
     set_last_error("tqd_op_attention_noalloc: cudaGetSymbolAddress failed");
     return TQD_ERR_CUDA;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* po = static_cast<float*>(g_scratch_ptr[dev]);
+  float* po = static_cast<float*>(base);
   float* pml = po + static_cast<size_t>(n_heads) * n_chunks * head_dim;
   uint32_t* cnt = reinterpret_cast<uint32_t*>(pml + static_cast<size_t>(n_heads) * n_chunks * 2);
   // the arrival counters must start at zero (the partials are overwritten)
