@@ -397,12 +397,12 @@ def run_tqd(args, wl, world, rank, local, pg):
         weights once, one embedding row and (p + 2) K/V positions per sequence."""
         return w_and_row + (B - 1) * emb_row + B * kv_pos * (p + 2)
 
-    def windows(n_steps):
-        out, left = [], n_steps
-        while left > 0:
-            out.append(min(left, D))
-            left -= out[-1]
-        return out
+    def windows(n_steps, at_least=1):
+        """Window lengths summing to n_steps: at least `at_least` windows (when
+        there are that many steps), none longer than the D decode positions."""
+        k = max(at_least, -(-n_steps // D))
+        k = min(k, n_steps)
+        return [n_steps // k + (1 if i < n_steps % k else 0) for i in range(k)]
 
     def run_window(n):
         for b in range(B):
@@ -423,7 +423,7 @@ def run_tqd(args, wl, world, rank, local, pg):
     torch.cuda.synchronize()
     total_bytes = 0
     launches = 0
-    for n in windows(steps_timed):
+    for n in windows(steps_timed, at_least=5):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for b in range(B):
             dec.truncate(P, seq=b)
@@ -444,6 +444,8 @@ def run_tqd(args, wl, world, rank, local, pg):
     clocks = sampler.stop()
     t_ms = sum(s.elapsed_time(e) for s, e, _ in ev)
     steps = sum(n for _, _, n in ev)
+    win_rates = [n * B / (s.elapsed_time(e) / 1000.0) for s, e, n in ev]
+    longest = max(n for _, _, n in ev)
     tokens = steps * B
     t_max = max_over_ranks(pg, t_ms)
     all_tokens = sum_over_ranks(pg, tokens)
@@ -486,7 +488,8 @@ def run_tqd(args, wl, world, rank, local, pg):
         "metric": metric_for(wl), "value": value, "unit": UNIT, "n_gpus": world, "steps": tokens,
         "warmup": args.warmup, "ms_per_step": t_max / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "prompt_len": P, "decode_positions": f"{P}..{P + D - 1}",
+        "config": {"workload": wl.name, "prompt_len": P, "decode_positions": f"{P}..{P + longest - 1}",
+                   "timed_windows": len(ev),
                    "batch": B, "schedule": args.schedule if B == 1 else "batched graph",
                    "weights": ("Q8_0 (34-byte blocks)" if cfg.weight_type == "q8_0" else "bf16") + ", resident",
                    "kv_history": args.kv_source + (f" ({args.prefill})" if args.kv_source == "prefill" else ""),
@@ -502,6 +505,10 @@ def run_tqd(args, wl, world, rank, local, pg):
         "step_roofline_frac": (mean_step_bytes / (hbm * 1e9)) / (t_max / steps / 1000.0),
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4 * B, "d2h_bytes_per_step": (4 + 16) * B,
                 "api": "tqd_decode_step per token" if B == 1 else "tqd_decode_step_batch per step"},
+        "windows": {"n": len(ev), "steps_each": sorted({n for _, _, n in ev}),
+                    "median": float(np.median(win_rates)), "min": float(min(win_rates)),
+                    "max": float(max(win_rates)), "unit": UNIT,
+                    "note": "each window restarts at the prompt's end; value is all timed tokens over the summed window times"},
         "gpu_launches": launches,
         "clocks": clocks,
     }
@@ -526,11 +533,18 @@ def main():
     line = run_tqd(args, wl, world, rank, local, pg)
     if rank == 0:
         if not args.no_cpu_baseline:
+            import oracle
             tps, n, cores, el = oracle_sample(wl, args.cpu_seconds)
             line["cpu_baseline"] = {
                 "value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
                 "sample": (f"{n} oracle decode steps ({el:.1f} s) at positions {wl.prompt_len}.. after a seeded "
                            f"stand-in KV history of {wl.prompt_len} rows")}
+            oracle.set_threads(1)
+            tps1, n1, _, el1 = oracle_sample(wl, min(args.cpu_seconds, 4.0))
+            oracle.set_threads(cores)
+            line["cpu_baseline"]["one_core"] = {
+                "value": tps1, "unit": UNIT, "cores": 1,
+                "sample": f"{n1} oracle decode steps ({el1:.1f} s) on one thread, same positions"}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

@@ -93,6 +93,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// An L2 policy that marks lines as the first to evict: for the weight and K/V
+// streams, read once per step, so that they do not push the small data every
+// step re-reads (norm gains, RoPE rows, activations) out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Order this thread's generic-proxy global accesses with later async-proxy
 // (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -207,6 +226,7 @@ struct DevLayer {
   const uint8_t* wo_g;    // persistent schedule: wo's columns split by kv group, [n_kv][H][G hd]
   const uint8_t* wgu;
   const uint8_t* wd;
+  const uint8_t* wd_c;    // persistent schedule: wd by column blocks (see DevModel::dcol_bytes)
   const float* attn_norm;
   const float* q_norm;
   const float* k_norm;
@@ -237,6 +257,13 @@ struct DevModel {
   size_t row_bytes_qw;    // ... with qw columns
   size_t row_bytes_i;     // ... with I columns
   size_t row_bytes_gh;    // ... with (n_heads / n_kv_heads) * head_dim columns
+  // The down projection by columns (persistent schedule), so that a block that
+  // owns SwiGLU outputs h[j0, j1) reads exactly the columns that multiply them.
+  // Q8_0: per 32-column block c, the H f16 scales of that block's rows (padded
+  // to 16 bytes), then 32 runs of H int8 quants, run j the quants of column
+  // 32c + j for rows 0..H-1; dcol_bytes is the size of one such block.  bf16:
+  // per column j, its H values; dcol_bytes = 2H.
+  size_t dcol_bytes;
   const DevLayer* layers;
   const uint8_t* lm_head;
   const uint8_t* embed;
@@ -268,6 +295,7 @@ struct DevSeq {
   float* opart;           // [n_kv][H] per-group partial O products (persistent schedule)
   float* sz;              // [V] the sampler's penalised logits
   uint32_t* scnt;         // [V] the sampler's input-token counts (zero between draws)
+  float* xacc;            // [2][8][H] the persistent schedule's down-projection sums (two sets of eight copies)
 };
 
 }  // namespace tqd

@@ -432,7 +432,10 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const bool persist = cfg->schedule == TQD_SCHED_PERSISTENT;
   const int gh = (nq / nkv) * hd;
   const size_t rbg = row_bytes(wt, gh);
-  struct LayerOff { size_t wqkv, wo, wog, wgu, wd, an, qn, kn, fn; };
+  // and the down projection by column blocks (DevModel::dcol_bytes)
+  const size_t dcol = wt == TQD_WEIGHT_Q8_0 ? align_up(2ull * H, 16) + 32ull * H : 2ull * H;
+  const size_t dcol_total = wt == TQD_WEIGHT_Q8_0 ? dcol * (I / 32) : dcol * I;
+  struct LayerOff { size_t wqkv, wo, wog, wgu, wd, wdc, an, qn, kn, fn; };
   std::vector<LayerOff> lo(L);
   for (int l = 0; l < L; ++l) {
     lo[l].wqkv = take(rbh * (qw + 2 * kvw));
@@ -440,6 +443,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     lo[l].wog = persist ? take(rbg * H * nkv) : 0;
     lo[l].wgu = take(rbh * 2 * I);
     lo[l].wd = take(rbi * H);
+    lo[l].wdc = persist ? take(dcol_total) : 0;
     lo[l].an = take(4 * H);
     lo[l].qn = take(4 * hd);
     lo[l].kn = take(4 * hd);
@@ -462,7 +466,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     return TQD_ERR_UNSUPPORTED_CONFIG;
   }
   struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar, gbar,
-                  opart, sz, scnt; };
+                  opart, sz, scnt, xacc; };
   std::vector<SeqOff> so(cfg->max_batch);
   const size_t kv_bytes = (kv16 ? 2 : 4) * static_cast<size_t>(L) * S * kvw;
   for (int b = 0; b < cfg->max_batch; ++b) {
@@ -487,6 +491,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].opart = take(4ull * nkv * H);
     so[b].sz = take(4 * align_up(static_cast<size_t>(V), 4));
     so[b].scnt = take(4 * align_up(static_cast<size_t>(V), 4));
+    so[b].xacc = persist ? take(4ull * 2 * 8 * H) : 0;
   }
   const size_t o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);  // the descriptors, for kernels over sequences
   // batched-step buffers (several sequences per step, or a prompt's tiles),
@@ -606,6 +611,40 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
         return fail(e, "upload the grouped O projection");
       }
       dl[l].wo_g = base + lo[l].wog;
+      // wd by column blocks: the block a CTA streams holds exactly the columns
+      // that multiply the SwiGLU outputs it computed
+      std::vector<uint8_t> cols(dcol_total);
+      const uint8_t* src = static_cast<const uint8_t*>(W.w_down);
+      const size_t hrb_d = host_row_bytes(wt, I);
+      if (wt == TQD_WEIGHT_Q8_0) {
+        for (int c = 0; c < I / 32; ++c) {
+          uint8_t* blk = cols.data() + dcol * c;
+          uint8_t* q = blk + align_up(2ull * H, 16);
+          for (int r = 0; r < H; ++r) {
+            const uint8_t* b34 = src + hrb_d * r + 34ull * c;
+            blk[2 * r] = b34[0];
+            blk[2 * r + 1] = b34[1];
+            for (int j = 0; j < 32; ++j) q[static_cast<size_t>(j) * H + r] = b34[2 + j];
+          }
+        }
+      } else {
+        uint16_t* dst16 = reinterpret_cast<uint16_t*>(cols.data());
+        for (int r = 0; r < H; ++r) {
+          const uint8_t* row = src + hrb_d * r;
+          for (int j = 0; j < I; ++j) {
+            uint16_t v;
+            memcpy(&v, row + 2ull * j, 2);
+            dst16[static_cast<size_t>(j) * H + r] = v;
+          }
+        }
+      }
+      e = cudaMemcpyAsync(base + lo[l].wdc, cols.data(), dcol_total, cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // the host copy is freed below
+      if (e != cudaSuccess) {
+        if (tmp) cudaFree(tmp);
+        return fail(e, "upload the down projection by columns");
+      }
+      dl[l].wd_c = base + lo[l].wdc;
     }
     dl[l].wqkv = base + lo[l].wqkv;
     dl[l].wo = base + lo[l].wo;
@@ -645,6 +684,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   dm.eps = cfg->rms_eps;
   dm.attn_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
   dm.row_bytes_h = rbh; dm.row_bytes_qw = rbq; dm.row_bytes_i = rbi; dm.row_bytes_gh = rbg;
+  dm.dcol_bytes = dcol;
   dm.layers = reinterpret_cast<const DevLayer*>(base + o_layers);
   dm.lm_head = base + o_lm;
   dm.embed = base + o_embed;
@@ -676,6 +716,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.opart = reinterpret_cast<float*>(base + so[b].opart);
     d.sz = reinterpret_cast<float*>(base + so[b].sz);
     d.scnt = reinterpret_cast<uint32_t*>(base + so[b].scnt);
+    d.xacc = persist ? reinterpret_cast<float*>(base + so[b].xacc) : nullptr;
   }
   m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
   {

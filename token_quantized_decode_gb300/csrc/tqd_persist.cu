@@ -256,7 +256,7 @@ struct Plan {
   int qr0[3], qr1[3];  // QKV matrix rows: the group's q, k and v rows this block owns
   int chunk;         // attention chunk of item (grp, chunk), or -1
   int o0, o1;        // rows of the group's O column slice
-  int g0, g1, d0, d1, v0, v1;
+  int g0, g1, v0, v1;  // gate/up rows (pairs: SwiGLU outputs g0/2 .. g1/2), lm_head rows
 };
 
 __device__ __forceinline__ Plan make_plan(const DevModel& m, int b, int nb) {
@@ -306,7 +306,6 @@ __device__ __forceinline__ Plan make_plan(const DevModel& m, int b, int nb) {
   }
   p.chunk = (p.grp >= 0 && p.j < m.n_chunks) ? p.j : -1;
   block_rows(2 * m.I, 2, b, nb, p.g0, p.g1);
-  block_rows(m.H, 1, b, nb, p.d0, p.d1);
   block_rows(m.V, 1, b, nb, p.v0, p.v1);
   return p;
 }
@@ -316,6 +315,7 @@ struct Producer {
   Ring r;
   uint32_t* err;
   bool ok;
+  uint64_t policy;  // L2 evict-first: every byte streamed here is read once per step
 
   __device__ bool acquire() {
     const uint32_t slot = r.n % kSlots, use = r.n / kSlots;
@@ -330,7 +330,7 @@ struct Producer {
       const uint32_t bytes = static_cast<uint32_t>(n * rb);
       uint64_t* fb = r.full + r.n % kSlots;
       mbar_arrive_expect_tx(fb, bytes);
-      bulk_g2s(slot_ptr(r), W + static_cast<size_t>(a) * rb, bytes, fb);
+      bulk_g2s_hint(slot_ptr(r), W + static_cast<size_t>(a) * rb, bytes, fb, policy);
       ++r.n;
     }
   }
@@ -343,9 +343,41 @@ struct Producer {
       uint64_t* fb = r.full + r.n % kSlots;
       uint8_t* dst = slot_ptr(r);
       mbar_arrive_expect_tx(fb, 2u * bytes);
-      bulk_g2s(dst, kc + static_cast<size_t>(a) * hd, bytes, fb);
-      bulk_g2s(dst + static_cast<size_t>(rpp) * hd * 4u, vc + static_cast<size_t>(a) * hd, bytes, fb);
+      bulk_g2s_hint(dst, kc + static_cast<size_t>(a) * hd, bytes, fb, policy);
+      bulk_g2s_hint(dst + static_cast<size_t>(rpp) * hd * 4u, vc + static_cast<size_t>(a) * hd, bytes, fb, policy);
       ++r.n;
+    }
+  }
+  // Columns [j0, j1) of the down projection in its column-block layout
+  // (DevModel::dcol_bytes).  Q8_0: one piece per 32-column block touched, the
+  // block's scales then the quant runs of those columns; bf16: whole columns,
+  // as many as a slot holds.
+  __device__ void dcols(const uint8_t* Wc, const DevModel& m, int j0, int j1) {
+    if (m.wtype == kFmtQ8) {
+      const uint32_t sb = a16(2u * m.H);
+      for (int c = j0 / 32; c * 32 < j1 && ok; ++c) {
+        const int ja = max(j0, 32 * c), jb = min(j1, 32 * c + 32);
+        if (!acquire()) return;
+        const uint8_t* blk = Wc + static_cast<size_t>(c) * m.dcol_bytes;
+        const uint32_t qb = static_cast<uint32_t>(jb - ja) * m.H;
+        uint64_t* fb = r.full + r.n % kSlots;
+        uint8_t* dst = slot_ptr(r);
+        mbar_arrive_expect_tx(fb, sb + qb);
+        bulk_g2s_hint(dst, blk, sb, fb, policy);
+        bulk_g2s_hint(dst + sb, blk + sb + static_cast<size_t>(ja - 32 * c) * m.H, qb, fb, policy);
+        ++r.n;
+      }
+    } else {
+      const int cpp = static_cast<int>(kSlotBytes / (2u * m.H));
+      for (int a = j0; a < j1 && ok; a += cpp) {
+        const int n = min(cpp, j1 - a);
+        if (!acquire()) return;
+        const uint32_t bytes = static_cast<uint32_t>(n) * 2u * m.H;
+        uint64_t* fb = r.full + r.n % kSlots;
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_g2s_hint(slot_ptr(r), Wc + static_cast<size_t>(a) * m.dcol_bytes, bytes, fb, policy);
+        ++r.n;
+      }
     }
   }
   // Wait until every issued copy has landed (used when stopping early).
@@ -361,7 +393,7 @@ struct Producer {
 
 __device__ void run_producer(const DevModel& m, const DevSeq& s, int n_steps, int full_from,
                              uint32_t pos0, Ring ring) {
-  Producer P{ring, &s.state->err, true};
+  Producer P{ring, &s.state->err, true, l2_evict_first_policy()};
   const Plan pl = make_plan(m, blockIdx.x, gridDim.x);
   for (int step = 0; step < n_steps && P.ok; ++step) {
     const int pos = static_cast<int>(pos0) + step;
@@ -378,7 +410,7 @@ __device__ void run_producer(const DevModel& m, const DevSeq& s, int n_steps, in
       if (pl.grp >= 0)
         P.rows(L.wo_g + static_cast<size_t>(pl.grp) * m.H * m.row_bytes_gh, m.row_bytes_gh, pl.o0, pl.o1);
       P.rows(L.wgu, m.row_bytes_h, pl.g0, pl.g1);
-      P.rows(L.wd, m.row_bytes_i, pl.d0, pl.d1);
+      P.dcols(L.wd_c, m, pl.g0 / 2, pl.g1 / 2);
     }
     if (step >= full_from) P.rows(m.lm_head, m.row_bytes_h, pl.v0, pl.v1);
   }
@@ -443,44 +475,12 @@ __device__ __forceinline__ float to_xin_norm(Cons& C, const float* src, int K, c
   return rsqrtf(t / static_cast<float>(K) + C.m.eps);
 }
 
-// RMSNorm input read straight from global memory (written by other blocks
-// before the last grid barrier): each thread loads its elements into
-// registers and writes the plain copy (residual source) and the padded
-// product with the gain in one pass; returns the folded 1/rms factor as
-// to_xin_norm does.  The barrier wait that precedes it ended with a consumer
-// sync, so earlier readers of xraw and xin are done.
-__device__ __forceinline__ float load_norm(Cons& C, const float* src, int K, const Gain& g) {
-  float* red = C.red + 16 * C.rsel;
-  C.rsel ^= 1u;
-  float v[kMaxGain];
-#pragma unroll
-  for (int j = 0; j < kMaxGain; ++j) {
-    const int i = threadIdx.x + kCT * j;
-    v[j] = i < K ? __ldcg(src + i) : 0.f;
-  }
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxGain; ++j) {
-    const int i = threadIdx.x + kCT * j;
-    if (i < K) {
-      ss = fmaf(v[j], v[j], ss);
-      C.xraw[i] = v[j];
-      C.xin[xpad(C.fmt, i)] = v[j] * g.v[j];
-    }
-  }
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  csync();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < kCW; ++w) t += red[w];
-  return rsqrtf(t / static_cast<float>(K) + C.m.eps);
-}
-
-// As load_norm for x after the attention block: the layer's input x (still
-// in xraw, where this thread staged its own elements) plus the nparts partial
-// O products (one per kv group, [nparts][K] in global memory), added in group
-// order; xraw becomes x after the attention block.
+// RMSNorm of a sum read from global memory (written by other blocks before
+// the last grid barrier), folded into the following matvec as to_xin_norm
+// does: the plain vector in xraw (the layer's input x, or x after the
+// attention block) plus nparts partial sums ([nparts][K] in global memory:
+// the per-group O products, or the eight copies of the down projection's
+// sums), added in part order; xraw becomes the sum.
 __device__ __forceinline__ float load_norm_sum(Cons& C, const float* parts, int nparts, int K, const Gain& g) {
   float* red = C.red + 16 * C.rsel;
   C.rsel ^= 1u;
@@ -520,17 +520,6 @@ __device__ __forceinline__ float load_norm_sum(Cons& C, const float* parts, int 
 #pragma unroll
   for (int w = 0; w < kCW; ++w) t += red[w];
   return rsqrtf(t / static_cast<float>(K) + C.m.eps);
-}
-
-// Stage n floats of global memory straight into the padded matvec layout
-// (16-byte pieces stay contiguous inside a chunk).
-__device__ __forceinline__ void stage_xin(Cons& C, const float* src, int n) {
-  for (int i = threadIdx.x; i < n / 4; i += kCT)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(C.xin + xpad(C.fmt, 4 * i))),
-                 "l"(src + 4 * i)
-                 : "memory");
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-  csync();
 }
 
 struct MvOut {
@@ -745,6 +734,85 @@ __device__ void mv_phase(Cons& C, size_t rb, int K, int r0, int r1, MvOut& o) {
   }
 }
 
+__device__ __forceinline__ void red_add_v4(float* p, float4 v) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
+// The down projection restricted to this block's columns [j0, j1) times its
+// SwiGLU outputs hs[j - j0] (shared memory): a partial sum for each of the H
+// rows, added into `out` (one of the eight copies of the current set) with
+// vector atomic adds.  The columns arrive through the ring in the layout of
+// DevModel::dcol_bytes; thread t owns rows 4t..4t+3 (H <= 4 consumer threads
+// per row group).  Per Q8_0 block c: sum_j q[r][j] h_j over its columns, then
+// times the f16 scale of (r, c) ("Eight kernels", q8_matvec, split by
+// columns: the partial sums of the blocks add up to the row's dot product).
+template <int FMT>
+__device__ void down_cols(Cons& C, int j0, int j1, const float* hs, float* out) {
+  const int H = C.m.H, t = threadIdx.x, lane = t & 31;
+  const bool has = 4 * t < H;
+  float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (FMT == kFmtQ8) {
+    const uint32_t sb = a16(2u * H);
+    for (int c = j0 / 32; c * 32 < j1; ++c) {
+      const int ja = max(j0, 32 * c), jb = min(j1, 32 * c + 32);
+      mwait(C.r.full + C.r.n % kSlots, (C.r.n / kSlots) & 1u, C.err);
+      const uint8_t* slot = slot_ptr(C.r);
+      if (has) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint8_t* q = slot + sb + 4 * t;
+        for (int j = ja; j < jb; ++j) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(q + static_cast<size_t>(j - ja) * H);
+          const float hv = hs[j - j0];
+          float f0, f1, f2, f3;
+          i8x4_to_f32(w, f0, f1, f2, f3);
+          acc.x = fmaf(f0, hv, acc.x);
+          acc.y = fmaf(f1, hv, acc.y);
+          acc.z = fmaf(f2, hv, acc.z);
+          acc.w = fmaf(f3, hv, acc.w);
+        }
+        const uint2 sc = *reinterpret_cast<const uint2*>(slot + 8 * t);  // scales of rows 4t..4t+3
+        tot.x = fmaf(acc.x, __half2float(__ushort_as_half(static_cast<unsigned short>(sc.x & 0xFFFFu))), tot.x);
+        tot.y = fmaf(acc.y, __half2float(__ushort_as_half(static_cast<unsigned short>(sc.x >> 16))), tot.y);
+        tot.z = fmaf(acc.z, __half2float(__ushort_as_half(static_cast<unsigned short>(sc.y & 0xFFFFu))), tot.z);
+        tot.w = fmaf(acc.w, __half2float(__ushort_as_half(static_cast<unsigned short>(sc.y >> 16))), tot.w);
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(C.r.empty + C.r.n % kSlots)) : "memory");
+      ++C.r.n;
+    }
+  } else {
+    const int cpp = static_cast<int>(kSlotBytes / (2u * H));
+    for (int a = j0; a < j1; a += cpp) {
+      const int n = min(cpp, j1 - a);
+      mwait(C.r.full + C.r.n % kSlots, (C.r.n / kSlots) & 1u, C.err);
+      const uint8_t* slot = slot_ptr(C.r);
+      if (has) {
+        for (int k = 0; k < n; ++k) {
+          const uint2 w = *reinterpret_cast<const uint2*>(slot + static_cast<size_t>(k) * 2u * H + 8 * t);
+          const float hv = hs[a + k - j0];
+          tot.x = fmaf(bf16_lo(w.x), hv, tot.x);
+          tot.y = fmaf(bf16_hi(w.x), hv, tot.y);
+          tot.z = fmaf(bf16_lo(w.y), hv, tot.z);
+          tot.w = fmaf(bf16_hi(w.y), hv, tot.w);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(C.r.empty + C.r.n % kSlots)) : "memory");
+      ++C.r.n;
+    }
+  }
+  if (has && j0 < j1) red_add_v4(out + 4 * t, tot);
+}
+
+// Zero this block's share of n floats (plain stores).
+__device__ __forceinline__ void zero_share(float* p, int n, int b, int nb) {
+  const int e0 = static_cast<int>(static_cast<long long>(n) * b / nb);
+  const int e1 = static_cast<int>(static_cast<long long>(n) * (b + 1) / nb);
+  for (int i = e0 + threadIdx.x; i < e1; i += kCT) p[i] = 0.f;
+}
+
 // Constants of the attention phase a lane needs (QK-norm gains and the RoPE
 // (cos, sin) pairs of the current position), loaded before the barrier wait.
 struct AttnPre {
@@ -907,24 +975,32 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
     }
   }
   csync();
+  // per head, once (one warp each): the chunk's max M over the warps, their
+  // weights f_w = exp(m_w - M) and the chunk's sum; written over qs, which
+  // every warp finished reading before its rows
+  float* fw = qs;  // [G][kCW] weights, then [G][2] (M, sum)
+  if (warp < G) {
+    const float mw = lane < kCW ? wst[(lane * G + warp) * stride + HD] : -INFINITY;
+    const float M = warp_max(mw);
+    const float f = (lane < kCW && mw != -INFINITY) ? expf(mw - M) : 0.f;
+    const float Ls = warp_sum(lane < kCW ? f * wst[(lane * G + warp) * stride + HD + 1] : 0.f);
+    if (lane < kCW) fw[warp * kCW + lane] = f;
+    if (lane == 0) {
+      fw[G * kCW + 2 * warp] = M;
+      fw[G * kCW + 2 * warp + 1] = Ls;
+    }
+  }
+  csync();
   for (int idx = threadIdx.x; idx < G * HD; idx += kCT) {
     const int hh = idx / HD, d = idx - hh * HD;
-    float M = -INFINITY;
-    for (int w = 0; w < kCW; ++w) M = fmaxf(M, wst[(w * G + hh) * stride + HD]);
-    float O = 0.f, Lsum = 0.f;
-    if (M != -INFINITY) {
-      for (int w = 0; w < kCW; ++w) {
-        const float* ws = wst + (w * G + hh) * stride;
-        const float f = expf(ws[HD] - M);
-        O = fmaf(f, ws[d], O);
-        Lsum = fmaf(f, ws[HD + 1], Lsum);
-      }
-    }
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) O = fmaf(fw[hh * kCW + w], wst[(w * G + hh) * stride + d], O);
     const int h = g * G + hh;
     s.part_o[(static_cast<size_t>(h) * m.n_chunks + c) * HD + d] = O;
     if (d == 0) {
-      s.part_ml[(static_cast<size_t>(h) * m.n_chunks + c) * 2] = M;
-      s.part_ml[(static_cast<size_t>(h) * m.n_chunks + c) * 2 + 1] = Lsum;
+      s.part_ml[(static_cast<size_t>(h) * m.n_chunks + c) * 2] = fw[G * kCW + 2 * hh];
+      s.part_ml[(static_cast<size_t>(h) * m.n_chunks + c) * 2 + 1] = fw[G * kCW + 2 * hh + 1];
     }
   }
 }
@@ -939,11 +1015,35 @@ __device__ void group_combine(Cons& C, int g, int HD, int G) {
   const int NC = m.n_chunks;
   float* po = C.scr;                      // [G][NC][HD]
   float* pml = po + G * NC * HD;          // [G][NC][2]
+  // every partial is requested before any is stored (one L2 round trip):
+  // the partials are at most 24 KB (the engine caps the chunk count), so at
+  // most kCombineLoads float4 per thread
+  const int n4 = G * NC * HD / 4, nml = G * NC * 2;
   const float4* src_o = reinterpret_cast<const float4*>(s.part_o + static_cast<size_t>(g) * G * NC * HD);
-  for (int i = threadIdx.x; i < G * NC * HD / 4; i += kCT)
-    reinterpret_cast<float4*>(po)[i] = __ldcg(src_o + i);
   const float* src_ml = s.part_ml + static_cast<size_t>(g) * G * NC * 2;
-  for (int i = threadIdx.x; i < G * NC * 2; i += kCT) pml[i] = __ldcg(src_ml + i);
+  constexpr int kCombineLoads = 4;
+  float4 r[kCombineLoads];
+#pragma unroll
+  for (int k = 0; k < kCombineLoads; ++k) {
+    const int i = threadIdx.x + k * kCT;
+    r[k] = i < n4 ? __ldcg(src_o + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float ml[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = threadIdx.x + k * kCT;
+    ml[k] = i < nml ? __ldcg(src_ml + i) : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < kCombineLoads; ++k) {
+    const int i = threadIdx.x + k * kCT;
+    if (i < n4) reinterpret_cast<float4*>(po)[i] = r[k];
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = threadIdx.x + k * kCT;
+    if (i < nml) pml[i] = ml[k];
+  }
   csync();
   // chunk weights exp(m_c - M) / L of every head, once: one warp per head
   float* wts = pml + G * NC * 2;          // [G][NC]
@@ -1003,6 +1103,15 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
   DevBarrier* ga = pl.grp >= 0 ? s.gbar + 16 * pl.grp : nullptr;  // the group's QKV rows are written
   DevBarrier* gb = pl.grp >= 0 ? ga + 8 : nullptr;                 // the group's attention partials are written
   unsigned long long gepoch = pl.grp >= 0 ? ga->epoch : 0ull;      // group barriers completed before this launch
+  // FFN phases of this launch: phase k adds its down-projection partial sums
+  // into set k & 1 of xacc (eight copies, one per block & 7, to spread the
+  // atomic adds) and clears this block's share of the other set, which the
+  // next FFN phase sums into after at least two more grid barriers; readers
+  // of set k (the next layer's input, or the lm_head's) finish before the
+  // grid barrier that starts FFN phase k + 1.  Set 0 is cleared here.
+  const int H = m.H;
+  int kph = 0;
+  zero_share(s.xacc, 8 * H, b, nb);
   for (int step = 0; step < n_steps; ++step) {
     const uint32_t pos = pos0 + step;
     if (pos >= static_cast<uint32_t>(m.max_seq)) {
@@ -1036,7 +1145,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
         o.scale = to_xin_norm(C, C.xraw, m.H, gain);
       } else {
         if (!wait()) return;
-        o.scale = load_norm(C, s.x, m.H, gain);
+        o.scale = load_norm_sum(C, s.xacc + ((kph - 1) & 1) * 8 * H, 8, H, gain);
       }
       o.epi = kEpiStore;
       o.y = s.qkv;
@@ -1065,21 +1174,18 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
         mv_phase<FMT>(C, m.row_bytes_gh, G * m.hd, pl.o0, pl.o1, o);
       }
       arrive();
-      // ---- residual + RMSNorm + gate/up + SwiGLU ----
+      // ---- residual + RMSNorm + gate/up + SwiGLU, then the down projection
+      //      over this block's SwiGLU outputs, summed into xacc ----
       if (!wait()) return;
-      o.scale = load_norm_sum(C, s.opart, m.nkv, m.H, gain);
+      o.scale = load_norm_sum(C, s.opart, m.nkv, H, gain);
       o.epi = kEpiSwiGLU;
-      o.y = s.h;
-      mv_phase<FMT>(C, m.row_bytes_h, m.H, pl.g0, pl.g1, o);
-      arrive();
-      // ---- down projection + residual ----
-      if (!wait()) return;
-      stage_xin(C, s.h, m.I);
-      o.scale = 1.f;
-      o.epi = kEpiResid;
-      o.y = s.x;
-      o.res = C.xraw;
-      mv_phase<FMT>(C, m.row_bytes_i, m.I, pl.d0, pl.d1, o);
+      const int j0 = pl.g0 / 2, j1 = pl.g1 / 2;
+      o.y = C.scr - j0;  // h[j] of this block's rows, in shared memory at scr[j - j0]
+      mv_phase<FMT>(C, m.row_bytes_h, H, pl.g0, pl.g1, o);
+      csync();
+      down_cols<FMT>(C, j0, j1, C.scr, s.xacc + (kph & 1) * 8 * H + (b & 7) * H);
+      zero_share(s.xacc + ((kph + 1) & 1) * 8 * H, 8 * H, b, nb);
+      ++kph;
       arrive();
     }
     if (step >= full_from) {
@@ -1088,7 +1194,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       load_gain(gain, m.out_norm, m.H);
       if (!wait()) return;
       MvOut o{};
-      o.scale = load_norm(C, s.x, m.H, gain);
+      o.scale = load_norm_sum(C, s.xacc + ((kph - 1) & 1) * 8 * H, 8, H, gain);
       o.epi = kEpiArgmax;
       o.y = s.logits;
       o.bv = -INFINITY;
@@ -1198,7 +1304,11 @@ size_t persistent_smem_bytes(const DevModel& m) { return playout(m).total; }
 
 bool persistent_supported(const DevModel& m) {
   const int G = m.nq / m.nkv;
-  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && m.H <= kMaxGain * kCT && m.nkv <= kMaxParts;
+  // the down projection's column pieces: 16-byte aligned runs that fit a slot
+  const bool dcol_ok = m.wtype == kFmtQ8 ? (m.H % 16 == 0 && a16(2u * m.H) + 32u * m.H <= kSlotBytes)
+                                         : (m.H % 8 == 0 && 2u * m.H <= kSlotBytes);
+  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && m.H <= kMaxGain * kCT && m.nkv <= kMaxParts &&
+         dcol_ok && m.I % 32 == 0;
 }
 
 int persistent_blocks_per_sm(const DevModel& m) {
