@@ -330,15 +330,25 @@ def time_sampling(dec, wl, stream, firsts, greedy_ms):
 
 
 def time_kv16(args, wl, model, stream, hbm, kind):
-    """The same batched decode windows on a model whose KV cache holds f16
-    elements (TQD_KV_F16: rows rounded to binary16 as they are appended),
-    after the same prompts prefilled in tiles: tokens/s and the step's
-    algorithmic bytes with two-byte K/V elements."""
+    """The same decode windows on a model whose KV cache holds f16 elements
+    (TQD_KV_F16: rows rounded to binary16 as they are appended), after the
+    same prompts prefilled in tiles (or the same history uploaded):
+    tokens/s and the step's algorithmic bytes with two-byte K/V elements.
+    Batch 1 runs the persistent schedule."""
     import torch
     import token_quantized_decode_gb300 as tqd
     cfg, P, D, B = wl.model, wl.prompt_len, wl.decode_steps, wl.batch
-    dec = tqd.Decoder(model, P + D, B, stream=stream, kv_type=tqd.TQD_KV_F16)
-    firsts = [dec.prefill_batch(synth.prompt(wl, seq=b), seq=b) for b in range(B)]
+    schedule = tqd.TQD_SCHED_PERSISTENT if B == 1 else tqd.TQD_SCHED_GRAPH
+    dec = tqd.Decoder(model, P + D, B, schedule, stream=stream, kv_type=tqd.TQD_KV_F16)
+    if args.kv_source == "upload":
+        firsts = []
+        for b in range(B):
+            k, v = synth.kv_fill(cfg, 7, b, P, -1.0, 1.0)
+            dec.kv_upload(k, v, seq=b)
+            del k, v
+            firsts.append(int(synth.prompt(wl, seq=b)[-1]))
+    else:
+        firsts = [dec.prefill_batch(synth.prompt(wl, seq=b), seq=b) for b in range(B)]
     kv_pos = 2 * cfg.kv_width * 2 * cfg.n_layers
     w_and_row = dec.step_bytes(0) - 2 * kv_pos
     emb_row = cfg.hidden * 17 // 16 if cfg.weight_type == "q8_0" else 2 * cfg.hidden
@@ -349,19 +359,23 @@ def time_kv16(args, wl, model, stream, hbm, kind):
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        dec.generate_batch(np.array(firsts), D)
+        if B == 1:
+            dec.generate(firsts[0], D)
+        else:
+            dec.generate_batch(np.array(firsts), D)
         e.record(stream)
         torch.cuda.synchronize()
         return s.elapsed_time(e)
 
     window()
-    ms = float(np.median([window() for _ in range(3)]))
+    ms = float(np.median([window() for _ in range(5)]))
     nbytes = sum(w_and_row + (B - 1) * emb_row + B * kv_pos * (p + 2) for p in range(P, P + D)) / D
     dec.close()
     return {"value": D * B / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms / D,
             "step_roofline_frac": nbytes / (hbm * 1e9) / (ms / D / 1000.0), "bytes_per_step": nbytes,
             "peak_kind": f"{kind} copy bandwidth",
-            "api": "tqd_generate_batch on a TQD_KV_F16 model (prompts prefilled in tiles)"}
+            "api": ("tqd_generate" if B == 1 else "tqd_generate_batch") + " on a TQD_KV_F16 model (history "
+                   + ("uploaded" if args.kv_source == "upload" else "prefilled in tiles") + ")"}
 
 
 def run_tqd(args, wl, world, rank, local, pg):
@@ -375,7 +389,7 @@ def run_tqd(args, wl, world, rank, local, pg):
     P, D, B = wl.prompt_len, wl.decode_steps, wl.batch
     schedule = tqd.TQD_SCHED_PERSISTENT if args.schedule == "persistent" else tqd.TQD_SCHED_GRAPH
     dec = tqd.Decoder(model, P + D, B, schedule, stream=stream)
-    if B == 1:
+    if B == 1 and P < 4096:
         del model
     firsts = []
     for b in range(B):
@@ -516,7 +530,7 @@ def run_tqd(args, wl, world, rank, local, pg):
     if prefill_line:
         line["prefill"] = prefill_line
     dec.close()
-    if B > 1:
+    if B > 1 or P >= 4096:  # the workloads where the K/V bytes rival the weights
         line["kv_f16"] = time_kv16(args, wl, model, stream, hbm, kind)
     return line
 

@@ -68,10 +68,10 @@ enum { TQD_SCHED_GRAPH = 0, TQD_SCHED_PERSISTENT = 1 };
  * TQD_KV_F16: every K and V element rounded to the nearest IEEE binary16
  * (ties to even) when it is appended or uploaded, halving the attention's
  * bytes (the packed-F16 KV representation "Metal LLM decode" names as the
- * batched prefill+decode arm's next step).  An f16 cache runs in the batched
- * step, the prefill tiles and the sampler; the batch-1 schedules read an f32
- * cache, so tqd_prefill, tqd_decode_step, tqd_generate and
- * tqd_generate_sampled refuse it with UNSUPPORTED_CONFIG. */
+ * batched prefill+decode arm's next step).  Every entry point runs either
+ * type: both batch-1 schedules, the batched step and the prefill tiles read
+ * and append f16 rows when the cache is f16, the step's own row included
+ * (rounded before it is used). */
 enum { TQD_KV_F32 = 0, TQD_KV_F16 = 1 };
 
 /* Model hyper-parameters ("One command buffer per token", section "The seam":
@@ -125,6 +125,28 @@ typedef struct tqd_host_weights {
 } tqd_host_weights;
 
 typedef struct tqd_model tqd_model;
+
+/* Create a model whose weights are the seeded synthetic ones the tests and
+ * the benchmark use (north star: "load synthetic model"; "Metal LLM decode",
+ * section "Functions": one call stands up the session): every matrix
+ * N(0, 0.02), quantized to Q8_0 (scale = max|w| / 127 as f16, quants
+ * rint(w / scale) clamped to +-127) or rounded to bf16, every norm gain
+ * 1 + N(0, 0.1) in f32, the lm_head tied to the embedding.  Draws come from
+ * counter-based splitmix64 streams, one per tensor: the lm_head 0, then per
+ * layer attn_norm, wq, wk, wv, wo, q_norm, k_norm, ffn_norm, w_gate, w_up,
+ * w_down, then the final norm; a normal draw is the Irwin-Hall sum of twelve
+ * 16-bit uniforms.  The bytes equal those of the repository's Python
+ * generator (synth.make_model(cfg, seed)).  Host memory for one copy of the
+ * weights is held during the call.  Errors as tqd_create. */
+int32_t tqd_create_synthetic(const tqd_config* cfg, uint64_t seed, void* stream, tqd_model** out);
+
+/* Copy a model's weights back to host memory in the upload format of
+ * tqd_host_weights (34-byte Q8_0 blocks or bf16, f32 gains): every pointer
+ * of *out and of out->layers[0 .. n_layers) names caller memory of the
+ * tensor's size (q_norm, k_norm only when qk_norm; embed may be NULL, and is
+ * skipped when the model's embedding is tied).  Synchronous; off the decode
+ * path.  Errors: BAD_ARG (a NULL destination), CUDA, POISONED. */
+int32_t tqd_export_weights(tqd_model* model, const tqd_host_weights* out);
 
 /* Name of a status code ("TQD_OK", ...); "TQD_UNKNOWN_STATUS" for others.
  * Needs no device.  ("Metal LLM decode", section "Status codes and the
@@ -277,9 +299,10 @@ int32_t tqd_generate_batch_sampled(tqd_model* model, int32_t n_seq, const int32_
 int32_t tqd_read_logits(tqd_model* model, int32_t seq, float* host_out);
 
 /* Number of device phases one decode step runs (kernel launches for
- * TQD_SCHED_GRAPH, barrier-separated phases for TQD_SCHED_PERSISTENT, counting
- * the grid and the KV-group barriers) —
- * the analogue of the per-token dispatch budget of "Metal LLM decode". */
+ * TQD_SCHED_GRAPH: 5 per layer plus 2; for TQD_SCHED_PERSISTENT the dependent
+ * phases of one step: per layer the projections, the attention chunks, the O
+ * projection and the fused feed-forward, then the lm_head: 4 per layer plus
+ * 1) — the analogue of the per-token dispatch budget of "Metal LLM decode". */
 int32_t tqd_phase_count(tqd_model* model, int32_t* out);
 
 /* Algorithmic HBM bytes of one decode step at position pos (weights read

@@ -72,6 +72,8 @@ def test_bad_configs_are_refused_before_any_device_work(L):
 
 def test_null_arguments_are_refused(L):
     assert L.tqd_create(None, None, None, None) == _lib.TQD_ERR_BAD_ARG
+    assert L.tqd_create_synthetic(None, 0, None, None) == _lib.TQD_ERR_BAD_ARG
+    assert L.tqd_export_weights(None, None) == _lib.TQD_ERR_BAD_ARG
     assert L.tqd_decode_step(None, 0, 0, 0, None) == _lib.TQD_ERR_BAD_ARG
     assert L.tqd_generate(None, 0, 0, 1, None) == _lib.TQD_ERR_BAD_ARG
     assert L.tqd_phase_count(None, None) == _lib.TQD_ERR_BAD_ARG
@@ -87,6 +89,9 @@ def test_no_device_is_a_status_not_a_crash(L):
     m = synth.make_model(synth.TINY, 0)
     with pytest.raises(tqd.TQDError) as ei:
         tqd.Decoder(m, 16)
+    assert ei.value.name == "TQD_ERR_NO_DEVICE"
+    with pytest.raises(tqd.TQDError) as ei:
+        tqd.Decoder.synthetic(synth.TINY, 0, 16)
     assert ei.value.name == "TQD_ERR_NO_DEVICE"
 
 

@@ -160,7 +160,7 @@ def test_refusals_and_state(tqd):
     assert dec.phase_count == 5 * wl.model.n_layers + 2
     dec.close()
     dp = tqd.Decoder(model, 8, 1, tqd.TQD_SCHED_PERSISTENT)
-    assert dp.phase_count == 5 * wl.model.n_layers + 1
+    assert dp.phase_count == 4 * wl.model.n_layers + 1
     dp.close()
 
 
@@ -206,12 +206,12 @@ def qwen3_reference():
     wl = synth.WORKLOADS["qwen3_0.6b"]
     model = synth.make_model(wl.model, wl.model_seed)
     ids = synth.prompt(wl)
-    return wl, model, ids, reference_run(model, ids, wl.prompt_len + 3, 3)
+    return wl, model, ids, reference_run(model, ids, wl.prompt_len + 8, 8)
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)
 def test_qwen3_shape_full_size(tqd, qwen3_reference, schedule):
-    """Qwen3-0.6B shape, 511-token prompt prefilled on the GPU, then three
+    """Qwen3-0.6B shape, 511-token prompt prefilled on the GPU, then eight
     teacher-forced decode steps, in the launch configuration the benchmark
     times."""
     wl, model, ids, ref = qwen3_reference
@@ -223,7 +223,7 @@ def test_qwen3_shape_full_size(tqd, qwen3_reference, schedule):
 def test_qwen3_shape_prefill_tiles_full_size(tqd, qwen3_reference):
     """The same 511-token prompt prefilled in tiles of 16 (31 full tiles and
     one of 15) on the one-sequence persistent model the benchmark times, then
-    the three teacher-forced decode steps over the cache the tiles wrote."""
+    the eight teacher-forced decode steps over the cache the tiles wrote."""
     wl, model, ids, ref = qwen3_reference
     dec = tqd.Decoder(model, wl.prompt_len + wl.decode_steps, 1, tqd.TQD_SCHED_PERSISTENT)
     replay(dec, ids, ref, tiles=True)
@@ -234,7 +234,7 @@ def test_smollm2_shape_bf16_full_size(tqd):
     wl = synth.WORKLOADS["smollm2_360m"]
     model = synth.make_model(wl.model, wl.model_seed)
     ids = synth.prompt(wl)
-    ref = reference_run(model, ids, wl.prompt_len + 2, 2)
+    ref = reference_run(model, ids, wl.prompt_len + 4, 4)
     for schedule in SCHEDULES:
         dec = tqd.Decoder(model, wl.prompt_len + wl.decode_steps, 1, sched(tqd, schedule))
         replay(dec, ids, ref)
@@ -249,9 +249,9 @@ def test_qwen3_long_context_from_uploaded_kv(tqd):
     model = synth.make_model(cfg, wl.model_seed)
     k, v = synth.kv_fill(cfg, 7, 0, wl.prompt_len, -1.0, 1.0)
     for schedule in SCHEDULES:
-        om = oracle.OracleModel(model, wl.prompt_len + 4)
+        om = oracle.OracleModel(model, wl.prompt_len + 5)
         om.kv_load(k, v)
         dec = tqd.Decoder(model, wl.prompt_len + 64, 1, sched(tqd, schedule))
         dec.kv_upload(k, v)
-        teacher_forced(tqd, dec, om, wl.prompt_len, 12345, 2)
+        teacher_forced(tqd, dec, om, wl.prompt_len, 12345, 4)
         dec.close()

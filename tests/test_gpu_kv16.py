@@ -1,7 +1,7 @@
 """An f16 KV cache (TQD_KV_F16: every cached K and V element rounded to the
-nearest binary16 as it is appended or uploaded) in the batched step and the
-prefill tiles, against the oracle with the same rounding step, at the whole
-step's tolerance (the device rounds its f32 rows, the oracle its f64 rows, so
+nearest binary16 as it is appended or uploaded) in the batched step, the
+prefill tiles and both batch-1 schedules, against the oracle with the same
+rounding step, at the whole step's tolerance (the device rounds its f32 rows, the oracle its f64 rows, so
 an element can land one f16 step apart)."""
 import numpy as np
 import pytest
@@ -97,20 +97,75 @@ def test_kv16_uploaded_history(tqd):
     dec.close()
 
 
-def test_kv16_refusals(tqd):
-    model = synth.make_model(synth.TINY, 0)
-    dec = tqd.Decoder(model, 16, 2, kv_type=tqd.TQD_KV_F16)
-    for call in (lambda: dec.prefill([1, 2, 3]), lambda: dec.decode_step(1, 0), lambda: dec.generate(1, 2),
-                 lambda: dec.generate_sampled(1, 2, tqd.sampling(seed=1))):
-        with pytest.raises(tqd.TQDError) as ei:
-            call()
-        assert ei.value.name == "TQD_ERR_UNSUPPORTED_CONFIG"
-    assert dec.next_pos() == 0
-    dec.close()
-    wide = synth.ModelConfig(1, 256, 8, 1, 64, 512, 4096, True, "q8_0", 1e6)  # 8 q heads per kv head
+def test_kv16_shape_outside_the_batched_kernels(tqd):
+    """8 q heads per kv head: the batched kernels refuse the shape, the graph
+    schedule runs it on an f16 cache (against the oracle's)."""
+    wide = synth.ModelConfig(1, 256, 8, 1, 64, 512, 4096, True, "q8_0", 1e6)
+    model = synth.make_model(wide, 0)
+    dec = tqd.Decoder(model, 16, 1, tqd.TQD_SCHED_GRAPH, kv_type=tqd.TQD_KV_F16)
     with pytest.raises(tqd.TQDError) as ei:
-        tqd.Decoder(synth.make_model(wide, 0), 8, 1, kv_type=tqd.TQD_KV_F16)
+        dec.prefill_batch([1, 2, 3])
     assert ei.value.name == "TQD_ERR_UNSUPPORTED_CONFIG"
+    om = oracle.OracleModel(model, 16, kv_f16=True)
+    tok, lg = om.prefill([1, 2, 3])
+    got = dec.prefill([1, 2, 3])
+    check_step(dec.logits(), got, lg, tok, "prefill")
+    dec.close()
+
+
+@pytest.mark.parametrize("schedule", ["graph", "persistent"])
+def test_kv16_batch1_schedules(tqd, schedule):
+    """The batch-1 schedules on an f16 cache: a stepwise prefill of 19
+    positions, four teacher-forced steps, then a chained generate whose
+    steps are replayed one by one on the oracle's f16 cache."""
+    cfg = synth.TINY
+    model = synth.make_model(cfg, 24)
+    ids = synth.token_ids(1000, 71, 19, cfg.vocab)
+    sched = tqd.TQD_SCHED_GRAPH if schedule == "graph" else tqd.TQD_SCHED_PERSISTENT
+    om = oracle.OracleModel(model, 40, kv_f16=True)
+    tok, lg = om.prefill(ids)
+    dec = tqd.Decoder(model, 40, 1, sched, kv_type=tqd.TQD_KV_F16)
+    got = dec.prefill(ids)
+    check_step(dec.logits(), got, lg, tok, "prefill")
+    p = len(ids)
+    for i in range(4):
+        ref_tok, ref_lg = om.step(tok, p)
+        got = dec.decode_step(tok, p)
+        check_step(dec.logits(), got, ref_lg, ref_tok, f"step {i}")
+        tok, p = ref_tok, p + 1
+    ids_gen = dec.generate(tok, 6)
+    for i in range(6):  # the oracle follows the device's own chain
+        ref_tok, ref_lg = om.step(tok, p + i)
+        top2 = np.sort(ref_lg)[-2:]
+        if top2[1] - top2[0] > 1e-2:
+            assert int(ids_gen[i]) == ref_tok, f"generated step {i}"
+        tok = int(ids_gen[i])
+    dec.close()
+
+
+@pytest.mark.parametrize("schedule", ["graph", "persistent"])
+def test_kv16_qwen3_long_history_batch1(tqd, schedule):
+    """Qwen3-0.6B shape with a 4096-position history uploaded into an f16
+    cache (rounded on the way, as the oracle rounds its copy), then three
+    teacher-forced steps at positions 4096..4098 on a batch-1 schedule."""
+    wl = synth.WORKLOADS["qwen3_0.6b_long"]
+    cfg = wl.model
+    model = synth.make_model(cfg, wl.model_seed)
+    P = 4096
+    k, v = synth.kv_fill(cfg, 7, 0, P)
+    sched = tqd.TQD_SCHED_GRAPH if schedule == "graph" else tqd.TQD_SCHED_PERSISTENT
+    dec = tqd.Decoder(model, P + 4, 1, sched, kv_type=tqd.TQD_KV_F16)
+    dec.kv_upload(k, v)
+    om = oracle.OracleModel(model, P + 4, kv_f16=True)
+    om.kv_load(k, v)
+    del k, v
+    tok = int(synth.prompt(wl)[-1])
+    for i in range(3):
+        ref_tok, ref_lg = om.step(tok, P + i)
+        got = dec.decode_step(tok, P + i)
+        check_step(dec.logits(), got, ref_lg, ref_tok, f"step {i}")
+        tok = ref_tok
+    dec.close()
 
 
 def test_kv16_qwen3_shape_sixteen_sequences(tqd):

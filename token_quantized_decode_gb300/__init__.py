@@ -103,6 +103,41 @@ def tqd_create(config: tqd_config, weights: HostWeights, stream=None) -> int:
     return h.value
 
 
+def tqd_create_synthetic(config: tqd_config, seed: int, stream=None) -> int:
+    h = ctypes.c_void_p()
+    check(lib().tqd_create_synthetic(ctypes.byref(config), ctypes.c_uint64(seed), _stream(stream), ctypes.byref(h)),
+          "tqd_create_synthetic")
+    return h.value
+
+
+def tqd_export_weights(handle, model_cfg) -> dict:
+    """The model's weights in the upload format: {"layers": [dict name ->
+    array], "lm_head": ..., "out_norm": ...} (host arrays allocated here)."""
+    H, hd, I, V = model_cfg.hidden, model_cfg.head_dim, model_cfg.intermediate, model_cfg.vocab
+    qw, kvw = model_cfg.n_heads * hd, model_cfg.n_kv_heads * hd
+
+    def mat(rows, cols):
+        if model_cfg.weight_type == "q8_0":
+            return np.zeros((rows, cols // 32 * 34), dtype=np.uint8)
+        return np.zeros((rows, cols), dtype=np.uint16)
+
+    shapes = {"wq": (qw, H), "wk": (kvw, H), "wv": (kvw, H), "wo": (H, qw), "w_gate": (I, H), "w_up": (I, H),
+              "w_down": (H, I)}
+    layers = []
+    for _ in range(model_cfg.n_layers):
+        d = {n: mat(*shp) for n, shp in shapes.items()}
+        d["attn_norm"] = np.zeros(H, dtype=np.float32)
+        d["ffn_norm"] = np.zeros(H, dtype=np.float32)
+        if model_cfg.qk_norm:
+            d["q_norm"] = np.zeros(hd, dtype=np.float32)
+            d["k_norm"] = np.zeros(hd, dtype=np.float32)
+        layers.append(d)
+    out = {"layers": layers, "lm_head": mat(V, H), "out_norm": np.zeros(H, dtype=np.float32)}
+    hw = HostWeights(layers, out["lm_head"], out["out_norm"])
+    check(lib().tqd_export_weights(handle, ctypes.byref(hw.struct)), "tqd_export_weights")
+    return out
+
+
 def tqd_destroy(handle) -> None:
     if handle:
         lib().tqd_destroy(handle)
@@ -232,6 +267,21 @@ class Decoder:
         self._weights = make_host_weights(model)
         self.handle = tqd_create(self.config, self._weights, stream)
         self._weights = None  # uploaded; host copies no longer needed by the library
+
+    @classmethod
+    def synthetic(cls, model_cfg, seed: int, max_seq: int, max_batch: int = 1, schedule: int = TQD_SCHED_GRAPH,
+                  stream=None, kv_type: int = TQD_KV_F32):
+        """A decoder over the seeded synthetic weights, generated inside the
+        library (tqd_create_synthetic) rather than uploaded from host arrays."""
+        self = cls.__new__(cls)
+        self.cfg = model_cfg
+        self.config = make_config(model_cfg, max_seq, max_batch, schedule, kv_type)
+        self._weights = None
+        self.handle = tqd_create_synthetic(self.config, seed, stream)
+        return self
+
+    def export_weights(self) -> dict:
+        return tqd_export_weights(self.handle, self.cfg)
 
     def close(self):
         if getattr(self, "handle", None):

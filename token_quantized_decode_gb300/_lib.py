@@ -76,6 +76,8 @@ def lib():
         "tqd_status_name": (ctypes.c_char_p, [i32]),
         "tqd_last_error": (ctypes.c_char_p, []),
         "tqd_create": (i32, [P(tqd_config), P(tqd_host_weights), vp, P(vp)]),
+        "tqd_create_synthetic": (i32, [P(tqd_config), ctypes.c_uint64, vp, P(vp)]),
+        "tqd_export_weights": (i32, [vp, P(tqd_host_weights)]),
         "tqd_destroy": (None, [vp]),
         "tqd_reset": (i32, [vp, i32]),
         "tqd_truncate": (i32, [vp, i32, i32]),
@@ -121,7 +123,7 @@ def lib():
 def exported_symbols():
     """Names the C ABI declares, in header order."""
     return [
-        "tqd_status_name", "tqd_last_error", "tqd_create", "tqd_destroy", "tqd_reset", "tqd_truncate", "tqd_next_pos",
+        "tqd_create_synthetic", "tqd_export_weights", "tqd_status_name", "tqd_last_error", "tqd_create", "tqd_destroy", "tqd_reset", "tqd_truncate", "tqd_next_pos",
         "tqd_prefill", "tqd_prefill_batch", "tqd_kv_upload", "tqd_decode_step", "tqd_generate", "tqd_decode_step_batch",
         "tqd_generate_batch", "tqd_sample", "tqd_generate_sampled", "tqd_generate_batch_sampled",
         "tqd_read_logits",

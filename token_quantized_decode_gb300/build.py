@@ -18,8 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtqd.so")
+SYNTH_SRC = os.path.join(ROOT, "synth", "tqd_synth.c")
 
-SOURCES = ["tqd_kernels.cu", "tqd_persist.cu", "tqd_engine.cu", "tqd_ops.cu", "tqd_noalloc.cu", "tqd_batch.cu",
+SOURCES = ["tqd_kernels.cu", "tqd_persist.cu", "tqd_persist_bf16.cu", "tqd_engine.cu", "tqd_ops.cu", "tqd_noalloc.cu", "tqd_batch.cu",
            "tqd_sample.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -36,7 +37,7 @@ def _deps_mtime() -> float:
     for d in (CSRC, INCLUDE):
         for f in os.listdir(d):
             t = max(t, os.path.getmtime(os.path.join(d, f)))
-    return max(t, os.path.getmtime(__file__))
+    return max(t, os.path.getmtime(__file__), os.path.getmtime(SYNTH_SRC))
 
 
 def build(force: bool = False, verbose: bool = False, extra: list | None = None) -> str:
@@ -55,13 +56,25 @@ def build(force: bool = False, verbose: bool = False, extra: list | None = None)
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    def compile_synth():
+        # the seeded input generator, linked in for tqd_create_synthetic (the
+        # same source and flags as the Python synth module's own build)
+        obj = os.path.join(BUILD, "tqd_synth.o")
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-c",
+               SYNTH_SRC, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"gcc failed for tqd_synth.c:\n{r.stdout}\n{r.stderr}")
+        return obj, r.stderr
+
+    with ThreadPoolExecutor(len(SOURCES) + 1) as ex:
+        futs = [ex.submit(compile_one, src) for src in SOURCES] + [ex.submit(compile_synth)]
+        results = [f.result() for f in futs]
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"]
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart", "-lgomp"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

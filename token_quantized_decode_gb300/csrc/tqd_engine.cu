@@ -460,13 +460,8 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   shape.H = H; shape.nq = nq; shape.nkv = nkv; shape.hd = hd; shape.I = I; shape.qw = qw;
   const bool batched = batch_supported(shape) && (V + 127) / 128 <= kMaxArgmaxBlocks;
   const bool kv16 = cfg->kv_type == TQD_KV_F16;
-  if (kv16 && !batched) {
-    set_error("an f16 KV cache runs in the batched kernels, which do not support this shape");
-    tqd_destroy(m);
-    return TQD_ERR_UNSUPPORTED_CONFIG;
-  }
   struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar, gbar,
-                  opart, sz, scnt, xacc; };
+                  opart, sz, scnt, xacc, qkvt; };
   std::vector<SeqOff> so(cfg->max_batch);
   const size_t kv_bytes = (kv16 ? 2 : 4) * static_cast<size_t>(L) * S * kvw;
   for (int b = 0; b < cfg->max_batch; ++b) {
@@ -492,6 +487,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].sz = take(4 * align_up(static_cast<size_t>(V), 4));
     so[b].scnt = take(4 * align_up(static_cast<size_t>(V), 4));
     so[b].xacc = persist ? take(4ull * 2 * 8 * H) : 0;
+    so[b].qkvt = persist ? take(8ull * (qw + 2 * kvw)) : 0;
   }
   const size_t o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);  // the descriptors, for kernels over sequences
   // batched-step buffers (several sequences per step, or a prompt's tiles),
@@ -717,6 +713,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.sz = reinterpret_cast<float*>(base + so[b].sz);
     d.scnt = reinterpret_cast<uint32_t*>(base + so[b].scnt);
     d.xacc = persist ? reinterpret_cast<float*>(base + so[b].xacc) : nullptr;
+    d.qkv_tag = persist ? reinterpret_cast<uint64_t*>(base + so[b].qkvt) : nullptr;
   }
   m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
   {
@@ -802,22 +799,9 @@ int32_t tqd_next_pos(tqd_model* m, int32_t seq, int32_t* pos_out) {
   return TQD_OK;
 }
 
-namespace {
-
-// The batch-1 schedules (persistent kernel, per-phase graph) read an f32 cache.
-int32_t refuse_kv16(tqd_model* m, const char* what) {
-  if (m->cfg.kv_type != TQD_KV_F16) return TQD_OK;
-  set_error("%s runs the batch-1 schedules, which read an f32 KV cache; this model's cache is f16 "
-            "(tqd_prefill_batch, tqd_decode_step_batch and tqd_generate_batch[_sampled] run it)", what);
-  return TQD_ERR_UNSUPPORTED_CONFIG;
-}
-
-}  // namespace
-
 int32_t tqd_prefill(tqd_model* m, int32_t seq, const int32_t* ids, int32_t n, int32_t* next_out) {
   int32_t rc = check_model(m, seq);
   if (rc) return rc;
-  if ((rc = refuse_kv16(m, "tqd_prefill"))) return rc;
   if (!ids || !next_out || n <= 0) {
     set_error("prefill needs ids, next_out and n > 0");
     return TQD_ERR_BAD_ARG;
@@ -906,7 +890,6 @@ int32_t tqd_kv_upload(tqd_model* m, int32_t seq, int32_t n_pos, const float* k, 
 int32_t tqd_decode_step(tqd_model* m, int32_t seq, int32_t token, int32_t pos, int32_t* next_out) {
   int32_t rc = check_model(m, seq);
   if (rc) return rc;
-  if ((rc = refuse_kv16(m, "tqd_decode_step"))) return rc;
   if (!next_out || token < 0 || token >= m->cfg.vocab) {
     set_error("decode_step needs next_out and a token in [0, vocab)");
     return TQD_ERR_BAD_ARG;
@@ -972,7 +955,6 @@ int32_t generate_impl(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_
                       const SampleArgs* sa) {
   int32_t rc = check_model(m, seq);
   if (rc) return rc;
-  if ((rc = refuse_kv16(m, "tqd_generate"))) return rc;
   if (!ids_out || n_steps <= 0 || first_token < 0 || first_token >= m->cfg.vocab) {
     set_error("generate needs ids_out, n_steps > 0 and a first token in [0, vocab)");
     return TQD_ERR_BAD_ARG;
@@ -1312,7 +1294,7 @@ int32_t tqd_phase_count(tqd_model* m, int32_t* out) {
     return TQD_ERR_BAD_ARG;
   }
   const int L = m->cfg.n_layers;
-  *out = m->cfg.schedule == TQD_SCHED_GRAPH ? 5 * L + 2 : 5 * L + 1;
+  *out = m->cfg.schedule == TQD_SCHED_GRAPH ? 5 * L + 2 : 4 * L + 1;
   return TQD_OK;
 }
 
@@ -1324,6 +1306,150 @@ int32_t tqd_step_bytes(tqd_model* m, int32_t pos, int64_t* bytes_out) {
   const int64_t kv_row = (m->dm.kv16 ? 2ll : 4ll) * m->dm.kvw * 2 * m->cfg.n_layers;  // K and V, all layers
   *bytes_out = m->weight_bytes + static_cast<int64_t>(row_bytes(m->cfg.weight_type, m->cfg.hidden)) +
                kv_row * (static_cast<int64_t>(pos) + 1) + kv_row;
+  return TQD_OK;
+}
+
+// ---------------------------------------------------------------- synthetic models
+// The seeded generator of the synthetic inputs (synth/tqd_synth.c, linked
+// into the library): input construction only, the same bytes the tests and
+// the benchmark build in Python.
+uint64_t tqs_stream(uint64_t seed, uint64_t tensor);
+void tqs_normal_f32(uint64_t seed, uint64_t tensor, int64_t n, double mean, double sigma, float* out);
+int tqs_q8_0_matrix(uint64_t seed, uint64_t tensor, int64_t rows, int64_t cols, double sigma, uint8_t* out);
+int tqs_bf16_matrix(uint64_t seed, uint64_t tensor, int64_t rows, int64_t cols, double sigma, uint16_t* out);
+
+int32_t tqd_create_synthetic(const tqd_config* cfg, uint64_t seed, void* stream, tqd_model** out) {
+  if (!cfg || !out) {
+    set_error("cfg and out must be non-NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  *out = nullptr;
+  if (int32_t rc = validate_config(cfg)) return rc;
+  const int L = cfg->n_layers, H = cfg->hidden, hd = cfg->head_dim, I = cfg->intermediate, V = cfg->vocab;
+  const int qw = cfg->n_heads * hd, kvw = cfg->n_kv_heads * hd, wt = cfg->weight_type;
+  // tensor streams: the lm_head (tied embedding) 0, then per layer in this
+  // order, then the final norm
+  enum { kAttnNorm, kWq, kWk, kWv, kWo, kQNorm, kKNorm, kFfnNorm, kGate, kUp, kDown, kPerLayer };
+  auto tensor = [&](int l, int which) { return static_cast<uint64_t>(1 + kPerLayer * l + which); };
+  std::vector<std::vector<uint8_t>> mats;
+  std::vector<std::vector<float>> gains;
+  mats.reserve(7 * L + 1);
+  gains.reserve(4 * L + 1);
+  auto matrix = [&](uint64_t t, int rows, int cols) -> const void* {
+    mats.emplace_back(host_row_bytes(wt, cols) * rows);
+    uint8_t* p = mats.back().data();
+    const int rc = wt == TQD_WEIGHT_Q8_0 ? tqs_q8_0_matrix(seed, t, rows, cols, 0.02, p)
+                                         : tqs_bf16_matrix(seed, t, rows, cols, 0.02, reinterpret_cast<uint16_t*>(p));
+    return rc == 0 ? p : nullptr;
+  };
+  auto gain = [&](uint64_t t, int n) -> const float* {
+    gains.emplace_back(n);
+    tqs_normal_f32(seed, t, n, 1.0, 0.1, gains.back().data());
+    return gains.back().data();
+  };
+  std::vector<tqd_layer_weights> lw(L);
+  bool ok = true;
+  const void* lm = matrix(0, V, H);
+  ok = ok && lm;
+  for (int l = 0; l < L && ok; ++l) {
+    tqd_layer_weights& w = lw[l];
+    w.attn_norm = gain(tensor(l, kAttnNorm), H);
+    w.wq = matrix(tensor(l, kWq), qw, H);
+    w.wk = matrix(tensor(l, kWk), kvw, H);
+    w.wv = matrix(tensor(l, kWv), kvw, H);
+    w.wo = matrix(tensor(l, kWo), H, qw);
+    w.q_norm = cfg->qk_norm ? gain(tensor(l, kQNorm), hd) : nullptr;
+    w.k_norm = cfg->qk_norm ? gain(tensor(l, kKNorm), hd) : nullptr;
+    w.ffn_norm = gain(tensor(l, kFfnNorm), H);
+    w.w_gate = matrix(tensor(l, kGate), I, H);
+    w.w_up = matrix(tensor(l, kUp), I, H);
+    w.w_down = matrix(tensor(l, kDown), H, I);
+    ok = w.wq && w.wk && w.wv && w.wo && w.w_gate && w.w_up && w.w_down;
+  }
+  if (!ok) {
+    set_error("the synthetic generator refused a shape (Q8_0 needs columns %% 32 == 0)");
+    return TQD_ERR_BAD_ARG;
+  }
+  tqd_host_weights hw{};
+  hw.layers = lw.data();
+  hw.out_norm = gain(static_cast<uint64_t>(1 + kPerLayer * L), H);
+  hw.lm_head = lm;
+  hw.embed = nullptr;  // tied
+  return tqd_create(cfg, &hw, stream, out);
+}
+
+int32_t tqd_export_weights(tqd_model* m, const tqd_host_weights* out) {
+  if (!m || !out || !out->layers || !out->out_norm || !out->lm_head) {
+    set_error("model, out, out->layers, out->out_norm and out->lm_head must be non-NULL");
+    return TQD_ERR_BAD_ARG;
+  }
+  if (m->poisoned) {
+    set_error("model is poisoned by an earlier device error");
+    return TQD_ERR_POISONED;
+  }
+  const tqd_config& c = m->cfg;
+  const int L = c.n_layers, H = c.hidden, hd = c.head_dim, I = c.intermediate, V = c.vocab;
+  const int qw = c.n_heads * hd, kvw = c.n_kv_heads * hd, wt = c.weight_type;
+  for (int l = 0; l < L; ++l) {
+    const tqd_layer_weights& w = out->layers[l];
+    if (!w.attn_norm || !w.wq || !w.wk || !w.wv || !w.wo || !w.ffn_norm || !w.w_gate || !w.w_up || !w.w_down ||
+        (c.qk_norm && (!w.q_norm || !w.k_norm))) {
+      set_error("layer %d: every destination pointer must be non-NULL (q_norm, k_norm only with qk_norm)", l);
+      return TQD_ERR_BAD_ARG;
+    }
+  }
+  std::vector<uint8_t> buf;
+  // `rows` device rows of `cols` columns starting at row r0, every `step`-th
+  // row, into host rows in the upload format
+  auto get = [&](const uint8_t* dev, int r0, int step, int rows, int cols, void* dst) -> cudaError_t {
+    const size_t rb = row_bytes(wt, cols), hrb = host_row_bytes(wt, cols);
+    buf.resize(rb * rows);
+    cudaError_t e = cudaMemcpy2DAsync(buf.data(), rb, dev + rb * r0, rb * step, rb, rows, cudaMemcpyDeviceToHost,
+                                      m->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+    if (e != cudaSuccess) return e;
+    uint8_t* o = static_cast<uint8_t*>(dst);
+    for (int r = 0; r < rows; ++r) {
+      const uint8_t* src = buf.data() + rb * r;
+      uint8_t* d = o + hrb * r;
+      if (wt == TQD_WEIGHT_Q8_0) {
+        for (int b = 0; b < cols / 32; ++b) {  // row layout: quants, then the blocks' f16 scales
+          d[34 * b] = src[cols + 2 * b];
+          d[34 * b + 1] = src[cols + 2 * b + 1];
+          memcpy(d + 34 * b + 2, src + 32 * b, 32);
+        }
+      } else {
+        memcpy(d, src, hrb);
+      }
+    }
+    return cudaSuccess;
+  };
+  auto getf = [&](const float* dev, int n, const float* dst) -> cudaError_t {
+    cudaError_t e = cudaMemcpyAsync(const_cast<float*>(dst), dev, 4ull * n, cudaMemcpyDeviceToHost, m->stream);
+    return e == cudaSuccess ? cudaStreamSynchronize(m->stream) : e;
+  };
+  cudaError_t e = cudaSuccess;
+  for (int l = 0; l < L && e == cudaSuccess; ++l) {
+    const DevLayer& d = m->host_layers[l];
+    const tqd_layer_weights& w = out->layers[l];
+    void* wq = const_cast<void*>(w.wq);
+    if ((e = get(d.wqkv, 0, 1, qw, H, wq)) != cudaSuccess ||
+        (e = get(d.wqkv, qw, 1, kvw, H, const_cast<void*>(w.wk))) != cudaSuccess ||
+        (e = get(d.wqkv, qw + kvw, 1, kvw, H, const_cast<void*>(w.wv))) != cudaSuccess ||
+        (e = get(d.wo, 0, 1, H, qw, const_cast<void*>(w.wo))) != cudaSuccess ||
+        (e = get(d.wgu, 0, 2, I, H, const_cast<void*>(w.w_gate))) != cudaSuccess ||
+        (e = get(d.wgu, 1, 2, I, H, const_cast<void*>(w.w_up))) != cudaSuccess ||
+        (e = get(d.wd, 0, 1, H, I, const_cast<void*>(w.w_down))) != cudaSuccess ||
+        (e = getf(d.attn_norm, H, w.attn_norm)) != cudaSuccess || (e = getf(d.ffn_norm, H, w.ffn_norm)) != cudaSuccess)
+      break;
+    if (c.qk_norm && ((e = getf(d.q_norm, hd, w.q_norm)) != cudaSuccess || (e = getf(d.k_norm, hd, w.k_norm)) != cudaSuccess))
+      break;
+  }
+  if (e == cudaSuccess) e = get(m->dm.lm_head, 0, 1, V, H, const_cast<void*>(out->lm_head));
+  if (e == cudaSuccess && out->embed && m->dm.embed != m->dm.lm_head)
+    e = get(m->dm.embed, 0, 1, V, H, const_cast<void*>(out->embed));
+  if (e == cudaSuccess) e = getf(m->dm.out_norm, H, out->out_norm);
+  if (e != cudaSuccess) return fail_cuda(m, e, "export weights");
   return TQD_OK;
 }
 

@@ -186,6 +186,11 @@ __device__ __forceinline__ AttnJob layer_attn_job(const DevModel& m, const DevSe
   a.vc = s.vcache + static_cast<size_t>(layer) * m.max_seq * m.kvw;
   a.head_stride = static_cast<size_t>(m.max_seq) * m.hd;
   a.row_stride = static_cast<size_t>(m.hd);
+  a.kv16 = m.kv16;
+  if (m.kv16) {  // element offsets of an f16 cache: the layer starts half as many bytes in
+    a.kc = reinterpret_cast<float*>(reinterpret_cast<__half*>(s.kcache) + static_cast<size_t>(layer) * m.max_seq * m.kvw);
+    a.vc = reinterpret_cast<float*>(reinterpret_cast<__half*>(s.vcache) + static_cast<size_t>(layer) * m.max_seq * m.kvw);
+  }
   a.S = static_cast<int>(pos) + 1;
   a.nq = m.nq;
   a.nkv = m.nkv;

@@ -275,8 +275,9 @@ struct AttnJob {
   const float* k_norm;
   const float2* rope;    // (cos, sin) row of the current position, or nullptr
   float* kc;             // keys of this layer (post-RoPE): row t of kv head g at
-  float* vc;             //   kc + g * head_stride + t * row_stride
+  float* vc;             //   kc + g * head_stride + t * row_stride (in elements)
   size_t head_stride, row_stride;
+  int kv16;              // the cache holds f16 elements (kc, vc point at halves)
   int S, nq, nkv, n_chunks;
   float eps, scale;
   float* part_o;         // [nq][n_chunks][HD]
@@ -351,12 +352,23 @@ __device__ void attention_item(const AttnJob& a, int g, int c, float* smem, uint
       vv[j] = ld_cg(a.v_new + g * HD + lane + 32 * j);
     }
     head_norm_rope<HD>(kv, a.k_norm, a.rope, a.eps);
-    float* krow = a.kc + g * a.head_stride + static_cast<size_t>(pos) * a.row_stride;
-    float* vrow = a.vc + g * a.head_stride + static_cast<size_t>(pos) * a.row_stride;
+    const size_t off = g * a.head_stride + static_cast<size_t>(pos) * a.row_stride;
+    if (a.kv16) {  // rounded to binary16 as the row enters the cache; the scan reads it back
+      __half* krow = reinterpret_cast<__half*>(a.kc) + off;
+      __half* vrow = reinterpret_cast<__half*>(a.vc) + off;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      krow[lane + 32 * j] = kv[j];
-      vrow[lane + 32 * j] = vv[j];
+      for (int j = 0; j < NJ; ++j) {
+        krow[lane + 32 * j] = __float2half_rn(kv[j]);
+        vrow[lane + 32 * j] = __float2half_rn(vv[j]);
+      }
+    } else {
+      float* krow = a.kc + off;
+      float* vrow = a.vc + off;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        krow[lane + 32 * j] = kv[j];
+        vrow[lane + 32 * j] = vv[j];
+      }
     }
   }
   __syncthreads();
@@ -377,10 +389,21 @@ __device__ void attention_item(const AttnJob& a, int g, int c, float* smem, uint
     for (int d = 0; d < DPL; ++d) qv[hh][d] = qs[hh * HD + lane * DPL + d];
 
   for (int t = t0 + warp; t < t1; t += nw) {
-    const float* krow = a.kc + g * a.head_stride + static_cast<size_t>(t) * a.row_stride + lane * DPL;
-    const float* vrow = a.vc + g * a.head_stride + static_cast<size_t>(t) * a.row_stride + lane * DPL;
+    const size_t off = g * a.head_stride + static_cast<size_t>(t) * a.row_stride + lane * DPL;
+    const float* krow = a.kc + off;
+    const float* vrow = a.vc + off;
     float kf[DPL], vf[DPL];
-    if constexpr (DPL == 4) {
+    if (a.kv16) {
+      const __half* kh = reinterpret_cast<const __half*>(a.kc) + off;
+      const __half* vh = reinterpret_cast<const __half*>(a.vc) + off;
+#pragma unroll
+      for (int e = 0; e < DPL; e += 2) {
+        const float2 k2 = __half22float2(__ldcg(reinterpret_cast<const __half2*>(kh + e)));
+        const float2 v2 = __half22float2(__ldcg(reinterpret_cast<const __half2*>(vh + e)));
+        kf[e] = k2.x; kf[e + 1] = k2.y;
+        vf[e] = v2.x; vf[e + 1] = v2.y;
+      }
+    } else if constexpr (DPL == 4) {
       const float4 k4 = ld_cg4(reinterpret_cast<const float4*>(krow));
       const float4 v4 = ld_cg4(reinterpret_cast<const float4*>(vrow));
       kf[0] = k4.x; kf[1] = k4.y; kf[2] = k4.z; kf[3] = k4.w;
