@@ -72,9 +72,10 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def measured_traffic(tokens_per_launch: float):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since the capture."""
+def measured_traffic(bytes_per_launch: float):
+    """DRAM bytes per launch: the committed ncu capture's ratio of DRAM traffic
+    to algorithmic bytes times this launch's algorithmic bytes, or None when
+    the kernel sources changed since the capture."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "k_persist_qwen3-0.6b_traffic.txt")
     try:
@@ -88,7 +89,7 @@ def measured_traffic(tokens_per_launch: float):
             h.update(open(os.path.join(ROOT, "token_quantized_decode_gb300", "csrc", f), "rb").read())
         if h.hexdigest() != kv["sources_sha256"]:
             return None
-        return float(kv["dram_bytes_per_token"]) * tokens_per_launch
+        return float(kv["traffic_over_algorithmic"]) * bytes_per_launch
     except Exception:
         return None
 
@@ -511,7 +512,7 @@ def run_tqd(args, wl, world, rank, local, pg):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm,
-                     "traffic": (measured_traffic(steps / len(ev))
+                     "traffic": (measured_traffic(per_launch_bytes)
                                  if persistent_b1 and wl.name.startswith("qwen3-0.6b-shape-q8_0-prompt511")
                                  else None),
                      "kernel": kernel, "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
