@@ -23,7 +23,7 @@ enum : uint32_t {
 
 // weight formats and matvec epilogues
 enum { kFmtQ8 = 0, kFmtBF16 = 1 };
-enum { kEpiStore = 0, kEpiResid = 1, kEpiSwiGLU = 2, kEpiArgmax = 3, kEpiTagged = 4 };
+enum { kEpiStore = 0, kEpiResid = 1, kEpiSwiGLU = 2, kEpiArgmax = 3, kEpiTagged = 4, kEpiAtomicAdd = 5 };
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -292,10 +292,10 @@ struct DevSeq {
   DevBarrier* bar;        // grid barrier of the persistent schedule
   float* x_mid;           // [H] residual after the attention block
   DevBarrier* gbar;       // per kv group g: [16 g] QKV rows written, [16 g + 8] attention partials written
-  float* opart;           // [n_kv][H] per-group partial O products (persistent schedule)
+  float* opart;           // [2][H] the persistent schedule's O products, summed over groups (two sets)
   float* sz;              // [V] the sampler's penalised logits
   uint32_t* scnt;         // [V] the sampler's input-token counts (zero between draws)
-  float* xacc;            // [2][8][H] the persistent schedule's down-projection sums (two sets of eight copies)
+  float* xacc;            // [2][4][H] the persistent schedule's down-projection sums (two sets of four copies)
   uint64_t* qkv_tag;      // [qw + 2 kvw] the persistent schedule's projections as (tag << 32 | f32 bits) words
 };
 

@@ -483,10 +483,10 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].acount = take(4);
     so[b].bar = take(sizeof(DevBarrier));
     so[b].gbar = take(sizeof(DevBarrier) * 16 * nkv);  // two per group, 128 bytes apart
-    so[b].opart = take(4ull * nkv * H);
+    so[b].opart = take(4ull * 2 * H);  // the persistent schedule's O products, two sets
     so[b].sz = take(4 * align_up(static_cast<size_t>(V), 4));
     so[b].scnt = take(4 * align_up(static_cast<size_t>(V), 4));
-    so[b].xacc = persist ? take(4ull * 2 * 8 * H) : 0;
+    so[b].xacc = persist ? take(4ull * 2 * 4 * H) : 0;
     so[b].qkvt = persist ? take(8ull * (qw + 2 * kvw)) : 0;
   }
   const size_t o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);  // the descriptors, for kernels over sequences

@@ -24,7 +24,7 @@ bool persistent_supported(const DevModel& m) {
   // the down projection's column pieces: 16-byte aligned runs that fit a slot
   const bool dcol_ok = m.wtype == kFmtQ8 ? (m.H % 16 == 0 && a16(2u * m.H) + 32u * m.H <= kSlotBytes)
                                          : (m.H % 8 == 0 && 2u * m.H <= kSlotBytes);
-  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && m.H <= kMaxGain * kCT && m.nkv <= kMaxParts &&
+  return G >= 1 && G <= 4 && (m.hd == 64 || m.hd == 128) && m.H <= kMaxGain * kCT &&
          dcol_ok && m.I % 32 == 0;
 }
 

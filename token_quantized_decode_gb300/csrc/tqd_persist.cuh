@@ -32,7 +32,9 @@ constexpr int kSlots = 4;
 constexpr int kPartFloats = 320;        // per-task partial sums of one ring piece
 constexpr int kRedFloats = 64 + 2 * kPartFloats;
 constexpr int kMaxGain = 4;             // norm gains held per thread (H <= 4 * kCT)
-constexpr int kMaxParts = 8;            // kv groups whose partial O products are summed (n_kv_heads <= 8)
+constexpr int kMaxParts = 4;            // partial sums load_norm_sum adds (the down projection's copies)
+constexpr int kAccCopies = 4;           // copies of the down projection's accumulator (copy b % 4: at most 38
+                                        // blocks add into an address; fewer copies to read back)
 // Error bits that end every block's waits; the others (a bad token id, every
 // logit NaN, capacity) are reported to the host without stopping the launch.
 constexpr uint32_t kFatal = kErrGridBarrier | kErrMbarrier;
@@ -557,6 +559,8 @@ __device__ __forceinline__ unsigned long long ld_tagged(const uint64_t* p) {
 __device__ __forceinline__ void epi_row(MvOut& o, int row, float v) {
   if (o.epi == kEpiTagged) {
     st_tagged(o.ytag + row, o.tag, v);
+  } else if (o.epi == kEpiAtomicAdd) {
+    atomicAdd(o.y + row, v);
   } else if (o.epi == kEpiResid) {
     o.y[row] = o.res[row] + v;
   } else {
@@ -1040,7 +1044,41 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
     mwait(C.r.full + C.r.n % kSlots, (C.r.n / kSlots) & 1u, C.err);
     const uint8_t* Ks = slot_ptr(C.r);
     const uint8_t* Vs = Ks + static_cast<size_t>(rpp) * HD * esz;
-    for (int t = warp; t < n; t += kCW) {
+    int t = warp;
+    for (; t + kCW < n; t += 2 * kCW) {  // two rows at a time: both scores before one softmax update
+      float kf[DPL], vf[DPL], kg[DPL], vg[DPL];
+      load_row(Ks + static_cast<size_t>(t) * HD * esz, Vs + static_cast<size_t>(t) * HD * esz, kv16, kf, vf);
+      load_row(Ks + static_cast<size_t>(t + kCW) * HD * esz, Vs + static_cast<size_t>(t + kCW) * HD * esz, kv16, kg, vg);
+      float d1[G], d2[G];
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        d1[hh] = 0.f;
+        d2[hh] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+          d1[hh] = fmaf(qv[hh][e], kf[e], d1[hh]);
+          d2[hh] = fmaf(qv[hh][e], kg[e], d2[hh]);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          d1[hh] += __shfl_xor_sync(0xFFFFFFFFu, d1[hh], o);
+          d2[hh] += __shfl_xor_sync(0xFFFFFFFFu, d2[hh], o);
+        }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float s1 = d1[hh] * m.attn_scale, s2 = d2[hh] * m.attn_scale;
+        const float mn = fmaxf(mm[hh], fmaxf(s1, s2));
+        const float corr = expf(mm[hh] - mn), p1 = expf(s1 - mn), p2 = expf(s2 - mn);
+        mm[hh] = mn;
+        ll[hh] = fmaf(ll[hh], corr, p1 + p2);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) oo[hh][e] = fmaf(oo[hh][e], corr, fmaf(p1, vf[e], p2 * vg[e]));
+      }
+    }
+    if (t < n) {
       float kf[DPL], vf[DPL];
       load_row(Ks + static_cast<size_t>(t) * HD * esz, Vs + static_cast<size_t>(t) * HD * esz, kv16, kf, vf);
       row_update(kf, vf);
@@ -1181,7 +1219,13 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
     ++epoch;
   };
   auto wait = [&]() { return gb_wait(bar, epoch * static_cast<unsigned long long>(nb), C.err); };
-  const Plan pl = make_plan(m, b, nb);
+  // the plan in shared memory: indexed by a loop variable, a local copy would
+  // live in local memory, which misses the small L1 left beside the
+  // shared-memory carve-out on every layer
+  __shared__ Plan s_pl;
+  if (threadIdx.x == 0) s_pl = make_plan(m, b, nb);
+  csync();
+  const Plan& pl = s_pl;
   const int v0 = pl.v0, v1 = pl.v1;
   // each counter on its own 128-byte line: groups do not contend
   DevBarrier* ga = pl.grp >= 0 ? s.gbar + 16 * pl.grp : nullptr;  // its epoch: the group's layers so far (kept across launches)
@@ -1196,7 +1240,13 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
   const int H = m.H;
   const int rpp_h = rows_per_piece(m.row_bytes_h), rpp_gh = rows_per_piece(m.row_bytes_gh);  // rows per ring piece
   int kph = 0;
-  zero_share(s.xacc, 8 * H, b, nb);
+  zero_share(s.xacc, kAccCopies * H, b, nb);
+  zero_share(s.opart, H, b, nb);
+  // the O products of the first layer are added into opart set 0 by blocks of
+  // every group before any later grid barrier: the clearing must be visible
+  // first (one extra grid barrier per launch)
+  arrive();
+  if (!wait()) return;
   for (int step = 0; step < n_steps; ++step) {
     const uint32_t pos = pos0 + step;
     if (pos >= static_cast<uint32_t>(m.max_seq)) {
@@ -1230,7 +1280,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
         o.scale = to_xin_norm(C, C.xraw, m.H, gain);
       } else {
         if (!wait()) return;
-        o.scale = load_norm_sum(C, s.xacc + ((kph - 1) & 1) * 8 * H, 8, H, gain);
+        o.scale = load_norm_sum(C, s.xacc + ((kph - 1) & 1) * kAccCopies * H, kAccCopies, H, gain);
       }
       // the group's Q, K and V rows as tagged words: the attention blocks of
       // the group poll exactly the rows they need, with no barrier between
@@ -1255,22 +1305,23 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
         if (!gb_wait(gb, tgt, C.err)) return;
         group_combine(C, pl.grp, m.hd, G);
         o.scale = 1.f;
-        o.epi = kEpiStore;
-        o.y = s.opart + static_cast<size_t>(pl.grp) * m.H;
+        o.epi = kEpiAtomicAdd;  // the groups' products of a row meet in one sum
+        o.y = s.opart + static_cast<size_t>(kph & 1) * m.H;
         mv_phase<FMT>(C, m.row_bytes_gh, rpp_gh, G * m.hd, pl.o0, pl.o1, o);
       }
       arrive();
       // ---- residual + RMSNorm + gate/up + SwiGLU, then the down projection
       //      over this block's SwiGLU outputs, summed into xacc ----
       if (!wait()) return;
-      o.scale = load_norm_sum(C, s.opart, m.nkv, H, gain);
+      o.scale = load_norm_sum(C, s.opart + static_cast<size_t>(kph & 1) * m.H, 1, H, gain);
+      zero_share(s.opart + static_cast<size_t>((kph + 1) & 1) * m.H, H, b, nb);
       o.epi = kEpiSwiGLU;
       const int j0 = pl.g0 / 2, j1 = pl.g1 / 2;
       o.y = C.scr - j0;  // h[j] of this block's rows, in shared memory at scr[j - j0]
       mv_phase<FMT>(C, m.row_bytes_h, rpp_h, H, pl.g0, pl.g1, o);
       csync();
-      down_cols<FMT>(C, j0, j1, C.scr, s.xacc + (kph & 1) * 8 * H + (b & 7) * H);
-      zero_share(s.xacc + ((kph + 1) & 1) * 8 * H, 8 * H, b, nb);
+      down_cols<FMT>(C, j0, j1, C.scr, s.xacc + (kph & 1) * kAccCopies * H + (b % kAccCopies) * H);
+      zero_share(s.xacc + ((kph + 1) & 1) * kAccCopies * H, kAccCopies * H, b, nb);
       ++kph;
       arrive();
     }
@@ -1280,7 +1331,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       load_gain(gain, m.out_norm, m.H);
       if (!wait()) return;
       MvOut o{};
-      o.scale = load_norm_sum(C, s.xacc + ((kph - 1) & 1) * 8 * H, 8, H, gain);
+      o.scale = load_norm_sum(C, s.xacc + ((kph - 1) & 1) * kAccCopies * H, kAccCopies, H, gain);
       o.epi = kEpiArgmax;
       o.y = s.logits;
       o.bv = -INFINITY;
