@@ -451,7 +451,7 @@ def run_tqd(args, wl, world, rank, local, pg):
         ev.append((s, e, n))
         total_bytes += sum(step_bytes(p) for p in range(P, P + n))
         if B > 1:
-            launches += n * (1 + 5 * cfg.n_layers + 1)
+            launches += n * -(-B // 16) * (1 + 5 * cfg.n_layers + 1)  # one graph per group of 16 sequences
         else:
             launches += 1 if schedule == tqd.TQD_SCHED_PERSISTENT else n * dec.phase_count
     torch.cuda.synchronize()

@@ -226,15 +226,17 @@ int32_t tqd_decode_step(tqd_model* model, int32_t seq, int32_t token, int32_t po
 int32_t tqd_generate(tqd_model* model, int32_t seq, int32_t first_token, int32_t n_steps,
                      int32_t* ids_out);
 
-/* One greedy step for sequences 0 .. n_seq-1 together (n_seq <= 16 and
- * <= max_batch): sequence b feeds tokens[b] at pos[b] (its next position).
- * The projections run as tensor-core contractions over the batch (tcgen05,
- * f32-accurate: exact int8 weight operands, activations split into bf16 or f16
- * parts), attention per sequence.  next_out[b]
- * receives sequence b's argmax.  Errors: as tqd_decode_step, plus
+/* One greedy step for sequences 0 .. n_seq-1 together (n_seq <= max_batch,
+ * at most 64): sequence b feeds tokens[b] at pos[b] (its next position; the
+ * positions may all differ).  The projections run as tensor-core contractions
+ * over the batch (tcgen05, f32-accurate: exact int8 weight operands,
+ * activations split into bf16 or f16 parts), attention per sequence.  Up to 16
+ * sequences share one sweep of the weights; a larger batch runs as
+ * consecutive groups of 16 (sequences 0-15, 16-31, ...), one sweep each.
+ * next_out[b] receives sequence b's argmax.  Errors: as tqd_decode_step, plus
  * UNSUPPORTED_CONFIG when the model has no batched step (max_batch == 1).
  * ("Metal LLM decode", the batched prefill+decode arm: sequences share one
- * sweep of the weights per step.) */
+ * sweep of the weights per step, up to BATCH_DECODE_MAX_SEQS = 32.) */
 int32_t tqd_decode_step_batch(tqd_model* model, int32_t n_seq, const int32_t* tokens,
                               const int32_t* pos, int32_t* next_out);
 

@@ -190,6 +190,7 @@ WORKLOADS = {
     "smollm2_360m": Workload("smollm2-360m-shape-bf16-prompt256-decode128", SMOLLM2_360M, 256, 128),
     "qwen3_0.6b_long": Workload("qwen3-0.6b-shape-q8_0-kv4096-decode64", QWEN3_06B, 4096, 64),
     "qwen3_0.6b_batch16": Workload("qwen3-0.6b-shape-q8_0-16x1024-decode64", QWEN3_06B, 1024, 64, batch=16),
+    "qwen3_0.6b_batch32": Workload("qwen3-0.6b-shape-q8_0-32x1024-decode64", QWEN3_06B, 1024, 64, batch=32),
 }
 
 

@@ -212,3 +212,56 @@ def test_batch_qwen3_shape_sixteen_sequences(tqd):
             ref_tok, ref_lg = om.step(inputs[i][b], P + i)
             check_step(logits[i][b], outs[i][b], ref_lg, ref_tok, f"step {i} seq {b}")
         del om
+
+
+def test_batch_beyond_sixteen_sequences(tqd):
+    """32 sequences at ragged positions (prompts of 3..34 positions prefilled
+    in tiles), then three teacher-forced batched steps of all 32 (two groups
+    of 16, each one sweep of the weights) and two of the first 20 (a group of
+    16 and one of 4): every sequence against the oracle at every step; then a
+    chained generate of the 32 replayed against the oracle."""
+    cfg = synth.TINY
+    model = synth.make_model(cfg, 31)
+    n, max_seq = 32, 48
+    dec = tqd.Decoder(model, max_seq, n)
+    oms, toks, pos = [], [], []
+    for b in range(n):
+        P = 3 + b
+        ids = synth.token_ids(1000, 200 + b, P, cfg.vocab)
+        om = oracle.OracleModel(model, max_seq)
+        tok, lg = om.prefill(ids)
+        got = dec.prefill_batch(ids, seq=b)
+        check_step(dec.logits(seq=b), got, lg, tok, f"prefill seq {b}")
+        oms.append(om)
+        toks.append(tok)
+        pos.append(P)
+    for width, steps in ((32, 3), (20, 2)):
+        for i in range(steps):
+            refs = [oms[b].step(toks[b], pos[b]) for b in range(width)]
+            got = dec.decode_step_batch(np.array(toks[:width]), np.array(pos[:width]))
+            for b in range(width):
+                check_step(dec.logits(seq=b), int(got[b]), refs[b][1], refs[b][0], f"{width}-wide step {i} seq {b}")
+                toks[b] = refs[b][0]
+                pos[b] += 1
+    dec.close()
+    # chained: 32 sequences, four device-chained steps, the oracle following
+    # each sequence's own chain
+    dec = tqd.Decoder(model, max_seq, n)
+    firsts, oms = [], []
+    for b in range(n):
+        ids = synth.token_ids(1000, 300 + b, 5 + b % 7, cfg.vocab)
+        firsts.append(dec.prefill_batch(ids, seq=b))
+        om = oracle.OracleModel(model, max_seq)
+        om.prefill(ids)
+        oms.append((om, len(ids)))
+    got = dec.generate_batch(np.array(firsts), 4)
+    for b in range(n):
+        om, P = oms[b]
+        tok = firsts[b]
+        for i in range(4):
+            ref_tok, ref_lg = om.step(tok, P + i)
+            top2 = np.sort(ref_lg)[-2:]
+            if top2[1] - top2[0] > 1e-2:
+                assert int(got[i, b]) == ref_tok, f"chained step {i} seq {b}"
+            tok = int(got[i, b])
+    dec.close()

@@ -1672,12 +1672,12 @@ __global__ void k_prefill_tile_end(const DevSeq* slots, int n) {
 }  // namespace
 
 cudaError_t launch_batch_tokens_in(const DevSeq* seqs, int n, const int32_t* tok, cudaStream_t st) {
-  k_batch_tokens_in<<<1, kTcN, 0, st>>>(seqs, n, tok);
+  k_batch_tokens_in<<<1, 64, 0, st>>>(seqs, n, tok);  // n <= 64 (tqd_config.max_batch)
   return cudaGetLastError();
 }
 
 cudaError_t launch_batch_tokens_out(const DevSeq* seqs, int n, int32_t* out, cudaStream_t st) {
-  k_batch_tokens_out<<<1, kTcN, 0, st>>>(seqs, n, out);
+  k_batch_tokens_out<<<1, 64, 0, st>>>(seqs, n, out);
   return cudaGetLastError();
 }
 

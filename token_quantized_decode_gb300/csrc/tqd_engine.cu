@@ -62,7 +62,7 @@ struct tqd_model {
   DevModel dm{};
   std::vector<SeqSlot> seqs;
   std::vector<DevLayer> host_layers;  // host copy of dm.layers (launch arguments)
-  int32_t* h_tokens = nullptr;  // pinned staging [max(max_seq + 1, 128)]
+  int32_t* h_tokens = nullptr;  // pinned staging [max(max_seq + 1, 256)]
   DevState* h_state = nullptr;  // pinned
   bool poisoned = false;
   bool pdl = true;
@@ -78,8 +78,9 @@ struct tqd_model {
   float* bss = nullptr;
   uint8_t* blm = nullptr;  // the lm_head in the batched step's tile-pass order
   int32_t* bio = nullptr;  // a batched step's tokens in [16], argmax out and error words [2 x 16]
-  int batch_nch = 1;
-  cudaGraphExec_t bgraph[17] = {};
+  // batches beyond batch_max() sequences run as consecutive groups of at most
+  // batch_max(): one graph per (group, group size)
+  cudaGraphExec_t bgraph[kBatchGroups][17] = {};
   // prefill tiles: batch_max() slot descriptors and the sequence's own (the
   // device copy and its host image), the slots' state words, and one graph per
   // (tile size, whether the tile ends the prompt)
@@ -346,7 +347,8 @@ void tqd_destroy(tqd_model* m) {
     if (s.g_full) cudaGraphExecDestroy(s.g_full);
     if (s.g_layers) cudaGraphExecDestroy(s.g_layers);
   }
-  for (cudaGraphExec_t& g : m->bgraph)
+  for (auto& row : m->bgraph)
+    for (cudaGraphExec_t& g : row)
     if (g) cudaGraphExecDestroy(g);
   for (auto& row : m->pgraph)
     for (cudaGraphExec_t& g : row)
@@ -504,7 +506,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     o_bcount = take(4);
     o_bss = take(4ull * 2 * batch_ss_slots(H) * bmax);
     o_blm = take(batch_head_bytes(V, H, fmt));
-    o_bio = take(4ull * 3 * bmax);
+    o_bio = take(4ull * 3 * 64);  // tokens in [64], argmaxes and error words out [2 x 64]
     o_pslots = take(sizeof(DevSeq) * (bmax + 1));
     o_pstates = take(sizeof(DevState) * bmax);
   }
@@ -517,7 +519,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     tqd_destroy(m);
     return TQD_ERR_OOM;
   }
-  if (cudaMallocHost(&m->h_tokens, 4 * std::max<size_t>(static_cast<size_t>(S) + 1, 128)) != cudaSuccess ||
+  if (cudaMallocHost(&m->h_tokens, 4 * std::max<size_t>(static_cast<size_t>(S) + 1, 256)) != cudaSuccess ||
       cudaMallocHost(&m->h_state, sizeof(DevState)) != cudaSuccess) {
     cudaGetLastError();
     set_error("pinned host allocation failed");
@@ -1041,28 +1043,32 @@ int32_t check_batch(tqd_model* m, int32_t n_seq) {
     set_error("this model has no batched step (max_batch must be > 1 and the shape supported)");
     return TQD_ERR_UNSUPPORTED_CONFIG;
   }
-  if (n_seq < 1 || n_seq > batch_max() || n_seq > m->cfg.max_batch) {
-    set_error("n_seq %d outside [1, %d]", n_seq, std::min(batch_max(), m->cfg.max_batch));
+  if (n_seq < 1 || n_seq > m->cfg.max_batch) {
+    set_error("n_seq %d outside [1, %d]", n_seq, m->cfg.max_batch);
     return TQD_ERR_BAD_ARG;
   }
   return TQD_OK;
 }
 
-// Enqueue `steps` batched steps of sequences 0..n-1 (graph captured once per n).
+// Enqueue `steps` batched steps of sequences 0..n-1: consecutive groups of at
+// most batch_max() sequences, each one sweep of the weights (one graph per
+// group and size, captured on first use).
 int32_t run_batch(tqd_model* m, int n, int steps) {
-  cudaGraphExec_t& g = m->bgraph[n];
-  if (!g) {
+  const int bm = batch_max(), groups = (n + bm - 1) / bm;
+  for (int gi = 0; gi < groups; ++gi) {
+    const int ng = std::min(bm, n - gi * bm);
+    cudaGraphExec_t& g = m->bgraph[gi][ng];
+    if (g) continue;
     // split-K chunks: as many as keep every (sequence, kv head, chunk) block
     // in one wave at two blocks per SM (a partial last wave would run alone)
-    int nch = 2 * m->num_sms / (n * m->dm.nkv);
+    int nch = 2 * m->num_sms / (ng * m->dm.nkv);
     if (nch > m->dm.n_chunks) nch = m->dm.n_chunks;
     if (nch < 1) nch = 1;
-    m->batch_nch = nch;
     cudaGraph_t graph = nullptr;
     CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
-    cudaError_t e = enqueue_batch_step(m->dm, m->host_layers.data(), m->blm, m->dseqs, n, nch, m->bx, m->bqkv,
-                                       m->bpo, m->bpml, m->bh, m->bss, m->bcount, &m->seqs[0].d.state->err,
-                                       m->stream, false, 0);
+    cudaError_t e = enqueue_batch_step(m->dm, m->host_layers.data(), m->blm, m->dseqs + gi * bm, ng, nch, m->bx,
+                                       m->bqkv, m->bpo, m->bpml, m->bh, m->bss, m->bcount,
+                                       &m->seqs[gi * bm].d.state->err, m->stream, false, 0);
     cudaError_t e2 = cudaStreamEndCapture(m->stream, &graph);
     if (e != cudaSuccess) {
       if (graph) cudaGraphDestroy(graph);
@@ -1073,7 +1079,9 @@ int32_t run_batch(tqd_model* m, int n, int steps) {
     cudaGraphDestroy(graph);
     if (e != cudaSuccess) return fail_cuda(m, e, "instantiate batched graph");
   }
-  for (int i = 0; i < steps; ++i) CK(cudaGraphLaunch(g, m->stream), "batched graph launch");
+  for (int i = 0; i < steps; ++i)
+    for (int gi = 0; gi < groups; ++gi)
+      CK(cudaGraphLaunch(m->bgraph[gi][std::min(bm, n - gi * bm)], m->stream), "batched graph launch");
   return TQD_OK;
 }
 
@@ -1149,8 +1157,8 @@ int32_t tqd_decode_step_batch(tqd_model* m, int32_t n_seq, const int32_t* tokens
   CK(cudaMemcpyAsync(m->bio, m->h_tokens, 4ull * n_seq, cudaMemcpyHostToDevice, m->stream), "write tokens");
   CK(launch_batch_tokens_in(m->dseqs, n_seq, m->bio, m->stream), "place tokens");
   if ((rc = run_batch(m, n_seq, 1))) return rc;
-  CK(launch_batch_tokens_out(m->dseqs, n_seq, m->bio + batch_max(), m->stream), "gather tokens");
-  CK(cudaMemcpyAsync(m->h_tokens + 64, m->bio + batch_max(), 8ull * n_seq, cudaMemcpyDeviceToHost, m->stream),
+  CK(launch_batch_tokens_out(m->dseqs, n_seq, m->bio + 64, m->stream), "gather tokens");
+  CK(cudaMemcpyAsync(m->h_tokens + 64, m->bio + 64, 8ull * n_seq, cudaMemcpyDeviceToHost, m->stream),
      "read next tokens");
   CK(cudaStreamSynchronize(m->stream), "synchronize");
   for (int b = 0; b < n_seq; ++b)

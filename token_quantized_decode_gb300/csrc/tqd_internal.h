@@ -137,6 +137,8 @@ struct SampleArgs {
   int penalize;        // any penalty differs from neutral
   unsigned long long seed;
 };
+// Groups of batch_max() sequences a batched step can run (tqd_config.max_batch <= 64).
+constexpr int kBatchGroups = 4;
 cudaError_t launch_sample(const DevSeq* seqs, int n, int V, int max_seq, const SampleArgs& a, cudaStream_t st);
 // Validate the caller's sampling controls into a, and say whether they are greedy.
 int32_t sampling_args(const ::tqd_sampling* p, SampleArgs& a, bool* greedy);
