@@ -155,6 +155,15 @@ __device__ __forceinline__ bool gb_wait(DevBarrier* b, unsigned long long target
   return !csync_or(fail);
 }
 
+__device__ __forceinline__ float silu_mul_fast(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// floor(a / b) for 0 <= a < 2^21 and b >= 1: (a + 1/2) / b is at least 1/(2b)
+// away from an integer, far more than the error of an approximate reciprocal
+// and one rounded product.
+__device__ __forceinline__ int small_div(int a, int b) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(static_cast<float>(b)));
+  return __float2int_rz((static_cast<float>(a) + 0.5f) * r);
+}
 // ---------------------------------------------------------------- f32x2
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;
@@ -261,6 +270,7 @@ struct Plan {
   int chunk;         // attention chunk of item (grp, chunk), or -1
   int o0, o1;        // rows of the group's O column slice
   int g0, g1, v0, v1;  // gate/up rows (pairs: SwiGLU outputs g0/2 .. g1/2), lm_head rows
+  int zo0, zo1, zx0, zx1;  // this block's shares of the O products (H) and of the accumulator copies
 };
 
 __device__ __forceinline__ Plan make_plan(const DevModel& m, int b, int nb) {
@@ -311,6 +321,8 @@ __device__ __forceinline__ Plan make_plan(const DevModel& m, int b, int nb) {
   p.chunk = (p.grp >= 0 && p.j < m.n_chunks) ? p.j : -1;
   block_rows(2 * m.I, 2, b, nb, p.g0, p.g1);
   block_rows(m.V, 1, b, nb, p.v0, p.v1);
+  block_rows(m.H, 1, b, nb, p.zo0, p.zo1);
+  block_rows(kAccCopies * m.H, 1, b, nb, p.zx0, p.zx1);
   return p;
 }
 
@@ -440,6 +452,7 @@ struct Cons {
   uint32_t psel;   // alternating partial-sum buffers of mv_phase
   uint32_t* err;
   int fmt;
+  float inv_h;     // 1 / H (every norm of the consumers is over H values)
   __device__ Cons(const DevModel& m_, const DevSeq& s_) : m(m_), s(s_) {}
 };
 
@@ -482,15 +495,15 @@ __device__ __forceinline__ float to_xin_norm(Cons& C, const float* src, int K, c
   float t = 0.f;
 #pragma unroll
   for (int w = 0; w < kCW; ++w) t += red[w];
-  return rsqrtf(t / static_cast<float>(K) + C.m.eps);
+  return rsqrtf(fmaf(t, C.inv_h, C.m.eps));
 }
 
 // RMSNorm of a sum read from global memory (written by other blocks before
 // the last grid barrier), folded into the following matvec as to_xin_norm
 // does: the plain vector in xraw (the layer's input x, or x after the
 // attention block) plus nparts partial sums ([nparts][K] in global memory:
-// the per-group O products, or the eight copies of the down projection's
-// sums), added in part order; xraw becomes the sum.
+// the per-group O products, or the copies of the down projection's sums),
+// added in part order; xraw becomes the sum.
 __device__ __forceinline__ float load_norm_sum(Cons& C, const float* parts, int nparts, int K, const Gain& g) {
   float* red = C.red + 16 * C.rsel;
   C.rsel ^= 1u;
@@ -529,7 +542,7 @@ __device__ __forceinline__ float load_norm_sum(Cons& C, const float* parts, int 
   float t = 0.f;
 #pragma unroll
   for (int w = 0; w < kCW; ++w) t += red[w];
-  return rsqrtf(t / static_cast<float>(K) + C.m.eps);
+  return rsqrtf(fmaf(t, C.inv_h, C.m.eps));
 }
 
 struct MvOut {
@@ -650,7 +663,7 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
   for (int a = r0; a < r1; a += rpp) {
     const int n = min(rpp, r1 - a);
     const int pairs = (n + 1) >> 1;
-    int nseg = pairs >= kCW ? 1 : kCW / pairs;
+    int nseg = pairs >= kCW ? 1 : small_div(kCW, pairs);
     if (nseg < 1) nseg = 1;
     if (nseg > iters) nseg = iters;
     const int tasks = pairs * nseg;
@@ -697,7 +710,7 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
           acc_a *= o.scale;
           acc_b *= o.scale;
           if (o.epi == kEpiSwiGLU) {
-            o.y[(a + ra) >> 1] = silu_mul(acc_a, acc_b);
+            o.y[(a + ra) >> 1] = silu_mul_fast(acc_a, acc_b);
           } else {
             epi_row(o, a + ra, acc_a);
             if (has_b) epi_row(o, a + rbw, acc_b);
@@ -710,13 +723,13 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
       continue;
     }
     for (int t = warp; t < tasks; t += kCW) {
-      const int p = t / nseg, sg = t - p * nseg;
+      const int p = nseg == 1 ? t : small_div(t, nseg), sg = t - p * nseg;
       const int ra = 2 * p, rbw = 2 * p + 1;
       const bool has_b = rbw < n;
       float acc_a = 0.f, acc_b = 0.f;
       dot_rows<FMT>(C.xin, slot + static_cast<size_t>(ra) * rb,
                     slot + static_cast<size_t>(has_b ? rbw : ra) * rb, K, nchunks,
-                    nseg == 1 ? 0 : iters * sg / nseg, nseg == 1 ? iters : iters * (sg + 1) / nseg, acc_a, acc_b);
+                    nseg == 1 ? 0 : small_div(iters * sg, nseg), nseg == 1 ? iters : small_div(iters * (sg + 1), nseg), acc_a, acc_b);
       acc_a = warp_sum(acc_a);
       acc_b = warp_sum(acc_b);
       if (lane == 0) {
@@ -724,7 +737,7 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
           acc_a *= o.scale;
           acc_b *= o.scale;
           if (o.epi == kEpiSwiGLU) {
-            o.y[(a + ra) >> 1] = silu_mul(acc_a, acc_b);
+            o.y[(a + ra) >> 1] = silu_mul_fast(acc_a, acc_b);
           } else {
             epi_row(o, a + ra, acc_a);
             if (has_b) epi_row(o, a + rbw, acc_b);
@@ -748,7 +761,7 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
           g += part[2 * (p * nseg + sg)];
           u += part[2 * (p * nseg + sg) + 1];
         }
-        o.y[(a >> 1) + p] = silu_mul(g * o.scale, u * o.scale);
+        o.y[(a >> 1) + p] = silu_mul_fast(g * o.scale, u * o.scale);
       }
     } else {
       for (int i = threadIdx.x; i < n; i += kCT) {
@@ -769,7 +782,7 @@ __device__ __forceinline__ void red_add_v4(float* p, float4 v) {
 
 // The down projection restricted to this block's columns [j0, j1) times its
 // SwiGLU outputs hs[j - j0] (shared memory): a partial sum for each of the H
-// rows, added into `out` (one of the eight copies of the current set) with
+// rows, added into `out` (one of the copies of the current set) with
 // vector atomic adds.  The columns arrive through the ring in the layout of
 // DevModel::dcol_bytes; thread t owns rows 4t..4t+3 (H <= 4 consumer threads
 // per row group).  Per Q8_0 block c: sum_j q[r][j] h_j over its columns, then
@@ -833,10 +846,8 @@ __device__ void down_cols(Cons& C, int j0, int j1, const float* hs, float* out) 
   if (has && j0 < j1) red_add_v4(out + 4 * t, tot);
 }
 
-// Zero this block's share of n floats (plain stores).
-__device__ __forceinline__ void zero_share(float* p, int n, int b, int nb) {
-  const int e0 = static_cast<int>(static_cast<long long>(n) * b / nb);
-  const int e1 = static_cast<int>(static_cast<long long>(n) * (b + 1) / nb);
+// Zero this block's share [e0, e1) of an array (plain stores).
+__device__ __forceinline__ void zero_share(float* p, int e0, int e1) {
   for (int i = e0 + threadIdx.x; i < e1; i += kCT) p[i] = 0.f;
 }
 
@@ -925,7 +936,7 @@ __device__ __forceinline__ void norm_rope_regs(float (&v)[HD / 32], const float*
 // chunk of the group to finish combines all chunks ("Eight kernels",
 // attention_decode, as a split-K flash decode).
 template <int HD, int G>
-__device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnPre& pre) {
+__device__ void attn_item(Cons& C, int layer, int g, int c, int pos, int t0, int t1, const AttnPre& pre) {
   constexpr int NJ = HD / 32, DPL = HD / 32;
   const DevModel& m = C.m;
   const DevSeq& s = C.s;
@@ -934,9 +945,6 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
   float* knew = qs + G * HD;       // [HD]
   float* vnew = knew + HD;         // [HD]
   float* wst = vnew + HD;          // [kCW][G][HD + 2], then the group's partials
-  const int S = pos + 1;
-  int t0, t1;
-  chunk_range(S, m.n_chunks, c, t0, t1);
   const bool has_new = t0 <= pos && pos < t1;
   const int tc = min(t1, pos);     // cached rows end
   if (warp < G) {
@@ -1023,13 +1031,13 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
       for (int e = 0; e < DPL; ++e) d = fmaf(qv[hh][e], kf[e], d);
       const float sc = warp_sum(d) * m.attn_scale;
       if (sc > mm[hh]) {
-        const float corr = expf(mm[hh] - sc);
+        const float corr = __expf(mm[hh] - sc);
         mm[hh] = sc;
         ll[hh] = ll[hh] * corr + 1.f;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) oo[hh][e] = fmaf(oo[hh][e], corr, vf[e]);
       } else {
-        const float p = expf(sc - mm[hh]);
+        const float p = __expf(sc - mm[hh]);
         ll[hh] += p;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) oo[hh][e] = fmaf(p, vf[e], oo[hh][e]);
@@ -1071,7 +1079,7 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
       for (int hh = 0; hh < G; ++hh) {
         const float s1 = d1[hh] * m.attn_scale, s2 = d2[hh] * m.attn_scale;
         const float mn = fmaxf(mm[hh], fmaxf(s1, s2));
-        const float corr = expf(mm[hh] - mn), p1 = expf(s1 - mn), p2 = expf(s2 - mn);
+        const float corr = __expf(mm[hh] - mn), p1 = __expf(s1 - mn), p2 = __expf(s2 - mn);
         mm[hh] = mn;
         ll[hh] = fmaf(ll[hh], corr, p1 + p2);
 #pragma unroll
@@ -1112,7 +1120,7 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
   if (warp < G) {
     const float mw = lane < kCW ? wst[(lane * G + warp) * stride + HD] : -INFINITY;
     const float M = warp_max(mw);
-    const float f = (lane < kCW && mw != -INFINITY) ? expf(mw - M) : 0.f;
+    const float f = (lane < kCW && mw != -INFINITY) ? __expf(mw - M) : 0.f;
     const float Ls = warp_sum(lane < kCW ? f * wst[(lane * G + warp) * stride + HD + 1] : 0.f);
     if (lane < kCW) fw[warp * kCW + lane] = f;
     if (lane == 0) {
@@ -1139,7 +1147,8 @@ __device__ void attn_item(Cons& C, int layer, int g, int c, int pos, const AttnP
 // attention_decode, as a split-K flash decode) into the matvec input (the
 // padded layout) of the group's O column slice: xin holds o of the group's
 // heads, G * head_dim values.
-__device__ void group_combine(Cons& C, int g, int HD, int G) {
+template <int HD>
+__device__ void group_combine(Cons& C, int g, int G) {
   const DevModel& m = C.m;
   const DevSeq& s = C.s;
   const int NC = m.n_chunks;
@@ -1185,7 +1194,7 @@ __device__ void group_combine(Cons& C, int g, int HD, int G) {
     float den = 0.f;
     for (int cc = lane; cc < NC; cc += 32) {
       const float mc = pml[(warp * NC + cc) * 2];
-      const float f = mc == -INFINITY ? 0.f : expf(mc - M);
+      const float f = mc == -INFINITY ? 0.f : __expf(mc - M);
       wts[warp * NC + cc] = f;
       den = fmaf(f, pml[(warp * NC + cc) * 2 + 1], den);
     }
@@ -1232,16 +1241,16 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
   DevBarrier* gb = pl.grp >= 0 ? ga + 8 : nullptr;                 // the group's attention partials are written
   unsigned long long gepoch = pl.grp >= 0 ? ga->epoch : 0ull;      // the group's layers before this launch
   // FFN phases of this launch: phase k adds its down-projection partial sums
-  // into set k & 1 of xacc (eight copies, one per block & 7, to spread the
-  // atomic adds) and clears this block's share of the other set, which the
+  // into set k & 1 of xacc (kAccCopies copies, block b adding into copy
+  // b % kAccCopies, to spread the atomic adds) and clears this block's share of the other set, which the
   // next FFN phase sums into after at least two more grid barriers; readers
   // of set k (the next layer's input, or the lm_head's) finish before the
   // grid barrier that starts FFN phase k + 1.  Set 0 is cleared here.
   const int H = m.H;
   const int rpp_h = rows_per_piece(m.row_bytes_h), rpp_gh = rows_per_piece(m.row_bytes_gh);  // rows per ring piece
   int kph = 0;
-  zero_share(s.xacc, kAccCopies * H, b, nb);
-  zero_share(s.opart, H, b, nb);
+  zero_share(s.xacc, pl.zx0, pl.zx1);
+  zero_share(s.opart, pl.zo0, pl.zo1);
   // the O products of the first layer are added into opart set 0 by blocks of
   // every group before any later grid barrier: the clearing must be visible
   // first (one extra grid barrier per launch)
@@ -1255,6 +1264,8 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
     }
     if (step > 0 && !wait()) return;  // the previous step's token is written
     int tok = __ldcg(s.tokens + pos);
+    int ct0 = 0, ct1 = 0;  // this block's attention chunk of the step's pos + 1 rows
+    if (pl.chunk >= 0) chunk_range(static_cast<int>(pos) + 1, m.n_chunks, pl.chunk, ct0, ct1);
     if (tok < 0 || tok >= m.V) {
       if (threadIdx.x == 0) atomicOr(C.err, kErrBadToken);
       tok = 0;
@@ -1297,13 +1308,13 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
           AttnPre pre;
           load_attn_pre(pre, m, L, static_cast<int>(pos));
           pre.tag = static_cast<uint32_t>(gepoch + 1);
-          attn_item<HD, GQ>(C, l, pl.grp, pl.chunk, pos, pre);
+          attn_item<HD, GQ>(C, l, pl.grp, pl.chunk, pos, ct0, ct1, pre);
         }
         gb_arrive(gb);
         ++gepoch;
         // ---- combine the group's chunks + its O column slice ----
         if (!gb_wait(gb, tgt, C.err)) return;
-        group_combine(C, pl.grp, m.hd, G);
+        group_combine<HD>(C, pl.grp, G);
         o.scale = 1.f;
         o.epi = kEpiAtomicAdd;  // the groups' products of a row meet in one sum
         o.y = s.opart + static_cast<size_t>(kph & 1) * m.H;
@@ -1314,14 +1325,14 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       //      over this block's SwiGLU outputs, summed into xacc ----
       if (!wait()) return;
       o.scale = load_norm_sum(C, s.opart + static_cast<size_t>(kph & 1) * m.H, 1, H, gain);
-      zero_share(s.opart + static_cast<size_t>((kph + 1) & 1) * m.H, H, b, nb);
+      zero_share(s.opart + static_cast<size_t>((kph + 1) & 1) * m.H, pl.zo0, pl.zo1);
       o.epi = kEpiSwiGLU;
       const int j0 = pl.g0 / 2, j1 = pl.g1 / 2;
       o.y = C.scr - j0;  // h[j] of this block's rows, in shared memory at scr[j - j0]
       mv_phase<FMT>(C, m.row_bytes_h, rpp_h, H, pl.g0, pl.g1, o);
       csync();
       down_cols<FMT>(C, j0, j1, C.scr, s.xacc + (kph & 1) * kAccCopies * H + (b % kAccCopies) * H);
-      zero_share(s.xacc + ((kph + 1) & 1) * kAccCopies * H, kAccCopies * H, b, nb);
+      zero_share(s.xacc + ((kph + 1) & 1) * kAccCopies * H, pl.zx0, pl.zx1);
       ++kph;
       arrive();
     }
@@ -1427,6 +1438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   C.psel = 0;
   C.err = &s.state->err;
   C.fmt = FMT;
+  C.inv_h = 1.0f / static_cast<float>(m.H);
   run_consumers<FMT, HD, GQ>(C, n_steps, full_from, pos0);
 }
 
