@@ -50,8 +50,8 @@ __host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
 
 // Elements per 16-byte weight chunk, and the padded shared-memory stride of
 // one chunk's x values (chunk c of lane c % 32: conflict-free 128-bit reads).
-__host__ __device__ inline int epc_of(int fmt) { return fmt == kFmtQ8 ? 16 : 8; }
-__host__ __device__ inline int xstride_of(int fmt) { return fmt == kFmtQ8 ? 20 : 12; }
+__host__ __device__ constexpr int epc_of(int fmt) { return fmt == kFmtQ8 ? 16 : 8; }
+__host__ __device__ constexpr int xstride_of(int fmt) { return fmt == kFmtQ8 ? 20 : 12; }
 
 __host__ __device__ inline PLayout playout(const DevModel& m) {
   PLayout L;
@@ -546,7 +546,6 @@ __device__ __forceinline__ float load_norm_sum(Cons& C, const float* parts, int 
 }
 
 struct MvOut {
-  int epi;
   float* y;           // kEpiStore / kEpiArgmax: y[r]; kEpiSwiGLU: y[r/2]; kEpiResid: y[r]
   const float* res;   // kEpiResid: residual source (shared memory), indexed by r
   float scale;        // multiplies every dot product (1, or 1/rms of a folded RMSNorm)
@@ -568,17 +567,18 @@ __device__ __forceinline__ unsigned long long ld_tagged(const uint64_t* p) {
   return w;
 }
 
-// Apply the epilogue to row `row` with dot product v (already scaled).
+// Apply epilogue EPI to row `row` with dot product v (already scaled).
+template <int EPI>
 __device__ __forceinline__ void epi_row(MvOut& o, int row, float v) {
-  if (o.epi == kEpiTagged) {
+  if constexpr (EPI == kEpiTagged) {
     st_tagged(o.ytag + row, o.tag, v);
-  } else if (o.epi == kEpiAtomicAdd) {
+  } else if constexpr (EPI == kEpiAtomicAdd) {
     atomicAdd(o.y + row, v);
-  } else if (o.epi == kEpiResid) {
+  } else if constexpr (EPI == kEpiResid) {
     o.y[row] = o.res[row] + v;
   } else {
     o.y[row] = v;
-    if (o.epi == kEpiArgmax) argmax_merge(o.bv, o.bi, v, row);
+    if constexpr (EPI == kEpiArgmax) argmax_merge(o.bv, o.bi, v, row);
   }
 }
 
@@ -649,12 +649,16 @@ __device__ __forceinline__ void dot_rows(const float* xin, const uint8_t* wa, co
   acc_b += b2;
 }
 
-// One phase of matvec rows [r0, r1) streamed through the ring.  Work in a
-// piece is split into tasks of (row pair, K segment).  When every task owns
-// whole rows (one segment), its warp applies the epilogue itself and moves
-// on to the next piece; otherwise task partial sums go through shared memory
-// and one thread per row applies the epilogue after a consumer sync.
-template <int FMT>
+// One phase of matvec rows [r0, r1) streamed through the ring, with epilogue
+// EPI.  Work in a piece is split into tasks of (row pair, K segment).  When
+// every task owns whole rows (one segment), its warp applies the epilogue
+// itself and moves on to the next piece; otherwise task partial sums go
+// through shared memory and one thread per row applies the epilogue after a
+// consumer sync.  SHORT (rows of at most 16 chunks, K known at compile time at
+// the call site) gives each half-warp its own row pair; the general path
+// handles any K, short rows included.  One instance holds one path and one
+// epilogue only, which keeps the per-layer code small.
+template <int FMT, int EPI, bool SHORT>
 __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvOut& o) {
   constexpr int EPC = FMT == kFmtQ8 ? 16 : 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -674,7 +678,7 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
     // every warp waits for the piece before releasing it, so no warp can run
     // ahead and release a later use of the same slot early
     mwait(fb, (C.r.n / kSlots) & 1u, C.err);
-    if (nchunks <= 16) {
+    if constexpr (SHORT) {
       // short rows (one 16-byte chunk per lane or fewer): each half-warp takes
       // its own row pair; both halves run every round so the shuffles stay
       // warp-uniform, an idle half repeats the last pair and skips the epilogue
@@ -709,11 +713,11 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
         if (t0 + half < pairs && l16 == 0) {
           acc_a *= o.scale;
           acc_b *= o.scale;
-          if (o.epi == kEpiSwiGLU) {
+          if constexpr (EPI == kEpiSwiGLU) {
             o.y[(a + ra) >> 1] = silu_mul_fast(acc_a, acc_b);
           } else {
-            epi_row(o, a + ra, acc_a);
-            if (has_b) epi_row(o, a + rbw, acc_b);
+            epi_row<EPI>(o, a + ra, acc_a);
+            if (has_b) epi_row<EPI>(o, a + rbw, acc_b);
           }
         }
       }
@@ -736,11 +740,11 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
         if (nseg == 1) {
           acc_a *= o.scale;
           acc_b *= o.scale;
-          if (o.epi == kEpiSwiGLU) {
+          if constexpr (EPI == kEpiSwiGLU) {
             o.y[(a + ra) >> 1] = silu_mul_fast(acc_a, acc_b);
           } else {
-            epi_row(o, a + ra, acc_a);
-            if (has_b) epi_row(o, a + rbw, acc_b);
+            epi_row<EPI>(o, a + ra, acc_a);
+            if (has_b) epi_row<EPI>(o, a + rbw, acc_b);
           }
         } else {
           part[2 * t] = acc_a;
@@ -754,7 +758,7 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
     if (nseg == 1) continue;
     csync();
     // split-K epilogue: one thread per row (SwiGLU: one per pair)
-    if (o.epi == kEpiSwiGLU) {
+    if constexpr (EPI == kEpiSwiGLU) {
       for (int p = threadIdx.x; p < pairs; p += kCT) {
         float g = 0.f, u = 0.f;
         for (int sg = 0; sg < nseg; ++sg) {
@@ -768,7 +772,7 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
         const int p = i >> 1, w = i & 1;
         float v = 0.f;
         for (int sg = 0; sg < nseg; ++sg) v += part[2 * (p * nseg + sg) + w];
-        epi_row(o, a + i, v * o.scale);
+        epi_row<EPI>(o, a + i, v * o.scale);
       }
     }
   }
@@ -1295,11 +1299,10 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       }
       // the group's Q, K and V rows as tagged words: the attention blocks of
       // the group poll exactly the rows they need, with no barrier between
-      o.epi = kEpiTagged;
       o.ytag = s.qkv_tag;
       o.tag = static_cast<uint32_t>(gepoch + 1);
       for (int i = 0; i < 3; ++i)
-        if (pl.qr0[i] < pl.qr1[i]) mv_phase<FMT>(C, m.row_bytes_h, rpp_h, m.H, pl.qr0[i], pl.qr1[i], o);
+        if (pl.qr0[i] < pl.qr1[i]) mv_phase<FMT, kEpiTagged, false>(C, m.row_bytes_h, rpp_h, m.H, pl.qr0[i], pl.qr1[i], o);
       load_gain(gain, L.ffn_norm, m.H);  // for the gate/up phase
       if (pl.grp >= 0) {
         const unsigned long long tgt = (gepoch + 1) * static_cast<unsigned long long>(pl.bpg);
@@ -1316,9 +1319,9 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
         if (!gb_wait(gb, tgt, C.err)) return;
         group_combine<HD>(C, pl.grp, G);
         o.scale = 1.f;
-        o.epi = kEpiAtomicAdd;  // the groups' products of a row meet in one sum
+        // kEpiAtomicAdd: the groups' products of a row meet in one sum
         o.y = s.opart + static_cast<size_t>(kph & 1) * m.H;
-        mv_phase<FMT>(C, m.row_bytes_gh, rpp_gh, G * m.hd, pl.o0, pl.o1, o);
+        mv_phase<FMT, kEpiAtomicAdd, (GQ * HD) / epc_of(FMT) <= 16>(C, m.row_bytes_gh, rpp_gh, G * m.hd, pl.o0, pl.o1, o);
       }
       arrive();
       // ---- residual + RMSNorm + gate/up + SwiGLU, then the down projection
@@ -1326,10 +1329,9 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       if (!wait()) return;
       o.scale = load_norm_sum(C, s.opart + static_cast<size_t>(kph & 1) * m.H, 1, H, gain);
       zero_share(s.opart + static_cast<size_t>((kph + 1) & 1) * m.H, pl.zo0, pl.zo1);
-      o.epi = kEpiSwiGLU;
       const int j0 = pl.g0 / 2, j1 = pl.g1 / 2;
       o.y = C.scr - j0;  // h[j] of this block's rows, in shared memory at scr[j - j0]
-      mv_phase<FMT>(C, m.row_bytes_h, rpp_h, H, pl.g0, pl.g1, o);
+      mv_phase<FMT, kEpiSwiGLU, false>(C, m.row_bytes_h, rpp_h, H, pl.g0, pl.g1, o);
       csync();
       down_cols<FMT>(C, j0, j1, C.scr, s.xacc + (kph & 1) * kAccCopies * H + (b % kAccCopies) * H);
       zero_share(s.xacc + ((kph + 1) & 1) * kAccCopies * H, pl.zx0, pl.zx1);
@@ -1343,11 +1345,10 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       if (!wait()) return;
       MvOut o{};
       o.scale = load_norm_sum(C, s.xacc + ((kph - 1) & 1) * kAccCopies * H, kAccCopies, H, gain);
-      o.epi = kEpiArgmax;
       o.y = s.logits;
       o.bv = -INFINITY;
       o.bi = INT_MAX;
-      mv_phase<FMT>(C, m.row_bytes_h, rpp_h, m.H, v0, v1, o);
+      mv_phase<FMT, kEpiArgmax, false>(C, m.row_bytes_h, rpp_h, m.H, v0, v1, o);
       // block candidate -> global candidates -> the last block picks the winner
       warp_argmax(o.bv, o.bi);
       float* redv = C.red + 32;                         // clear of the norm partials
