@@ -518,8 +518,11 @@ def run_tqd(args, wl, world, rank, local, pg):
                      "kernel": kernel, "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
                      "peak_kind": f"{kind} copy bandwidth"},
         "step_roofline_frac": (mean_step_bytes / (hbm * 1e9)) / (t_max / steps / 1000.0),
-        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4 * B, "d2h_bytes_per_step": (4 + 16) * B,
-                "api": "tqd_decode_step per token" if B == 1 else "tqd_decode_step_batch per step"},
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4 * B,
+                "d2h_bytes_per_step": 16 if persistent_b1 else (4 + 16) * B,
+                "api": "tqd_decode_step per token" if B == 1 else "tqd_decode_step_batch per step",
+                "copies": ("the token as a launch argument; the next token inside the 16-byte state record read back"
+                           if persistent_b1 else "the tokens up, the next tokens and the state records back")},
         "windows": {"n": len(ev), "steps_each": sorted({n for _, _, n in ev}),
                     "median": float(np.median(win_rates)), "min": float(min(win_rates)),
                     "max": float(max(win_rates)), "unit": UNIT,

@@ -212,8 +212,11 @@ int32_t tqd_kv_upload(tqd_model* model, int32_t seq, int32_t n_pos, const float*
 
 /* One greedy decode step: feed `token` at position `pos`, which must equal
  * the sequence's next position, append its K/V row, and write the argmax of
- * the logits (ties to the lowest index, NaN never wins) to *next_out.  Four
- * bytes cross back to the host.  Errors: BAD_ARG, POS_MISMATCH, CAPACITY,
+ * the logits (ties to the lowest index, NaN never wins) to *next_out.  With
+ * the persistent schedule the token travels as a launch argument and the next
+ * token comes back inside the sequence's 16-byte state record (one launch and
+ * one readback per call); the graph schedule copies the token up (4 bytes)
+ * and reads the state back.  Errors: BAD_ARG, POS_MISMATCH, CAPACITY,
  * NUMERIC (all logits NaN).  ("One command buffer per token", section "One
  * command buffer": decode_step.) */
 int32_t tqd_decode_step(tqd_model* model, int32_t seq, int32_t token, int32_t pos,

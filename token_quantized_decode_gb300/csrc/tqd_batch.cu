@@ -1173,6 +1173,7 @@ __global__ void __launch_bounds__(kHdThreads, 1) k_head16(MmArgs a) {
         next = -1;
       }
       if (pos + 1 <= static_cast<uint32_t>(a.max_seq)) s.tokens[pos + 1] = next;
+      s.state->last = next;
       s.state->pos = pos + 1;
       s.state->steps += 1;
     }

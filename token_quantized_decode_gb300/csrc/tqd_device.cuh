@@ -237,7 +237,7 @@ struct DevState {  // per sequence, in device memory
   uint32_t pos;    // next position (= KV rows filled)
   uint32_t err;    // kErr* bits
   uint32_t steps;  // steps completed (diagnostic)
-  uint32_t pad;
+  int32_t last;    // the token the last greedy step wrote at its next position (-1: every logit NaN)
 };
 
 // Barrier of the persistent schedule (the whole grid, or the blocks of one kv
@@ -297,6 +297,8 @@ struct DevSeq {
   uint32_t* scnt;         // [V] the sampler's input-token counts (zero between draws)
   float* xacc;            // [2][4][H] the persistent schedule's down-projection sums (two sets of four copies)
   uint64_t* qkv_tag;      // [qw + 2 kvw] the persistent schedule's projections as (tag << 32 | f32 bits) words
+  int32_t tok_in;         // persistent schedule: the first step's input token when >= 0 (the kernel
+                          // stores it at tokens[pos]); -1: the token is already at tokens[pos]
 };
 
 }  // namespace tqd

@@ -716,6 +716,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.scnt = reinterpret_cast<uint32_t*>(base + so[b].scnt);
     d.xacc = persist ? reinterpret_cast<float*>(base + so[b].xacc) : nullptr;
     d.qkv_tag = persist ? reinterpret_cast<uint64_t*>(base + so[b].qkvt) : nullptr;
+    d.tok_in = -1;
   }
   m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
   {
@@ -905,16 +906,22 @@ int32_t tqd_decode_step(tqd_model* m, int32_t seq, int32_t token, int32_t pos, i
     set_error("position %d is beyond max_seq %d", pos, m->cfg.max_seq);
     return TQD_ERR_CAPACITY;
   }
-  m->h_tokens[0] = token;
-  CK(cudaMemcpyAsync(s.d.tokens + pos, m->h_tokens, 4, cudaMemcpyHostToDevice, m->stream),
-     "write token");
-  if ((rc = run_steps(m, s, 1, 0))) return rc;
-  CK(cudaMemcpyAsync(m->h_tokens + 1, s.d.tokens + pos + 1, 4, cudaMemcpyDeviceToHost, m->stream),
-     "read next token");
+  if (m->cfg.schedule == TQD_SCHED_PERSISTENT) {
+    // the token goes in as a launch argument and the next one comes back in
+    // the state record finish() reads: one launch and one readback per token
+    DevSeq d = s.d;
+    d.tok_in = token;
+    CK(launch_persistent(m->dm, d, 1, 0, m->blocks_persist, m->stream), "persistent launch");
+  } else {
+    m->h_tokens[0] = token;
+    CK(cudaMemcpyAsync(s.d.tokens + pos, m->h_tokens, 4, cudaMemcpyHostToDevice, m->stream),
+       "write token");
+    if ((rc = run_steps(m, s, 1, 0))) return rc;
+  }
   if ((rc = finish(m, s))) return rc;
   s.next_pos = pos + 1;
   s.logits_pos = s.next_pos;
-  *next_out = m->h_tokens[1];
+  *next_out = m->h_state->last;
   return TQD_OK;
 }
 

@@ -29,6 +29,7 @@ __device__ __forceinline__ void finish_step(const DevSeq& s, uint32_t pos, int w
     next = -1;
   }
   if (pos + 1 <= static_cast<uint32_t>(max_seq)) s.tokens[pos + 1] = next;
+  s.state->last = next;
   s.state->pos = pos + 1;
   s.state->steps += 1;
 }

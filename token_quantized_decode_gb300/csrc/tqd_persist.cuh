@@ -1267,7 +1267,8 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       break;
     }
     if (step > 0 && !wait()) return;  // the previous step's token is written
-    int tok = __ldcg(s.tokens + pos);
+    int tok = (step == 0 && s.tok_in >= 0) ? s.tok_in : __ldcg(s.tokens + pos);
+    if (step == 0 && s.tok_in >= 0 && b == 0 && threadIdx.x == 0) s.tokens[pos] = s.tok_in;  // the history
     int ct0 = 0, ct1 = 0;  // this block's attention chunk of the step's pos + 1 rows
     if (pl.chunk >= 0) chunk_range(static_cast<int>(pos) + 1, m.n_chunks, pl.chunk, ct0, ct1);
     if (tok < 0 || tok >= m.V) {
@@ -1393,6 +1394,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
             next = -1;
           }
           if (pos + 1 <= static_cast<uint32_t>(m.max_seq)) s.tokens[pos + 1] = next;
+          s.state->last = next;
           s.state->pos = pos + 1;
           s.state->steps += 1;
           *s.amax_count = 0u;
