@@ -650,11 +650,10 @@ __device__ __forceinline__ void dot_rows(const float* xin, const uint8_t* wa, co
 }
 
 // One phase of matvec rows [r0, r1) streamed through the ring, with epilogue
-// EPI.  Work in a piece is split into tasks of (row pair, K segment).  When
-// every task owns whole rows (one segment), its warp applies the epilogue
-// itself and moves on to the next piece; otherwise task partial sums go
-// through shared memory and one thread per row applies the epilogue after a
-// consumer sync.  SHORT (rows of at most 16 chunks, K known at compile time at
+// EPI.  The row pairs of a piece go whole to the warps, kCW at a time (each
+// warp applies the epilogue of its own pairs); the pairs left over are split
+// into (pair, K segment) tasks whose partial sums go through shared memory,
+// and one thread per row applies their epilogue after a consumer sync.  SHORT (rows of at most 16 chunks, K known at compile time at
 // the call site) gives each half-warp its own row pair; the general path
 // handles any K, short rows included.  One instance holds one path and one
 // epilogue only, which keeps the per-layer code small.
@@ -667,10 +666,16 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
   for (int a = r0; a < r1; a += rpp) {
     const int n = min(rpp, r1 - a);
     const int pairs = (n + 1) >> 1;
-    int nseg = pairs >= kCW ? 1 : small_div(kCW, pairs);
-    if (nseg < 1) nseg = 1;
+    // whole pairs kCW at a time; the pairs left over are split over K
+    int full = pairs / kCW * kCW, rem = pairs - full;
+    int nseg = rem > 0 ? small_div(kCW, rem) : 1;
     if (nseg > iters) nseg = iters;
-    const int tasks = pairs * nseg;
+    if (nseg <= 1) {
+      nseg = 1;
+      full = pairs;
+      rem = 0;
+    }
+    const int tasks = rem * nseg;  // split tasks
     uint64_t* fb = C.r.full + C.r.n % kSlots;
     const uint8_t* slot = slot_ptr(C.r);
     float* part = C.red + 64 + kPartFloats * C.psel;  // [tasks][2] when nseg > 1
@@ -726,53 +731,61 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
       ++C.r.n;
       continue;
     }
-    for (int t = warp; t < tasks; t += kCW) {
-      const int p = nseg == 1 ? t : small_div(t, nseg), sg = t - p * nseg;
+    for (int p = warp; p < full; p += kCW) {  // whole pairs: the warp applies the epilogue
       const int ra = 2 * p, rbw = 2 * p + 1;
       const bool has_b = rbw < n;
       float acc_a = 0.f, acc_b = 0.f;
       dot_rows<FMT>(C.xin, slot + static_cast<size_t>(ra) * rb,
-                    slot + static_cast<size_t>(has_b ? rbw : ra) * rb, K, nchunks,
-                    nseg == 1 ? 0 : small_div(iters * sg, nseg), nseg == 1 ? iters : small_div(iters * (sg + 1), nseg), acc_a, acc_b);
+                    slot + static_cast<size_t>(has_b ? rbw : ra) * rb, K, nchunks, 0, iters, acc_a, acc_b);
       acc_a = warp_sum(acc_a);
       acc_b = warp_sum(acc_b);
       if (lane == 0) {
-        if (nseg == 1) {
-          acc_a *= o.scale;
-          acc_b *= o.scale;
-          if constexpr (EPI == kEpiSwiGLU) {
-            o.y[(a + ra) >> 1] = silu_mul_fast(acc_a, acc_b);
-          } else {
-            epi_row<EPI>(o, a + ra, acc_a);
-            if (has_b) epi_row<EPI>(o, a + rbw, acc_b);
-          }
+        acc_a *= o.scale;
+        acc_b *= o.scale;
+        if constexpr (EPI == kEpiSwiGLU) {
+          o.y[(a + ra) >> 1] = silu_mul_fast(acc_a, acc_b);
         } else {
-          part[2 * t] = acc_a;
-          part[2 * t + 1] = acc_b;
+          epi_row<EPI>(o, a + ra, acc_a);
+          if (has_b) epi_row<EPI>(o, a + rbw, acc_b);
         }
+      }
+    }
+    for (int t = warp; t < tasks; t += kCW) {  // (left-over pair, K segment): partial sums
+      const int q = small_div(t, nseg), sg = t - q * nseg;
+      const int ra = 2 * (full + q), rbw = ra + 1;
+      const bool has_b = rbw < n;
+      float acc_a = 0.f, acc_b = 0.f;
+      dot_rows<FMT>(C.xin, slot + static_cast<size_t>(ra) * rb,
+                    slot + static_cast<size_t>(has_b ? rbw : ra) * rb, K, nchunks,
+                    small_div(iters * sg, nseg), small_div(iters * (sg + 1), nseg), acc_a, acc_b);
+      acc_a = warp_sum(acc_a);
+      acc_b = warp_sum(acc_b);
+      if (lane == 0) {
+        part[2 * t] = acc_a;
+        part[2 * t + 1] = acc_b;
       }
     }
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(C.r.empty + C.r.n % kSlots)) : "memory");
     ++C.r.n;
-    if (nseg == 1) continue;
+    if (tasks == 0) continue;
     csync();
-    // split-K epilogue: one thread per row (SwiGLU: one per pair)
+    // split-K epilogue of the left-over pairs: one thread per row (SwiGLU: one per pair)
     if constexpr (EPI == kEpiSwiGLU) {
-      for (int p = threadIdx.x; p < pairs; p += kCT) {
+      for (int q = threadIdx.x; q < rem; q += kCT) {
         float g = 0.f, u = 0.f;
         for (int sg = 0; sg < nseg; ++sg) {
-          g += part[2 * (p * nseg + sg)];
-          u += part[2 * (p * nseg + sg) + 1];
+          g += part[2 * (q * nseg + sg)];
+          u += part[2 * (q * nseg + sg) + 1];
         }
-        o.y[(a >> 1) + p] = silu_mul_fast(g * o.scale, u * o.scale);
+        o.y[((a >> 1) + full) + q] = silu_mul_fast(g * o.scale, u * o.scale);
       }
     } else {
-      for (int i = threadIdx.x; i < n; i += kCT) {
-        const int p = i >> 1, w = i & 1;
+      for (int i = threadIdx.x; i < n - 2 * full; i += kCT) {
+        const int q = i >> 1, w = i & 1;
         float v = 0.f;
-        for (int sg = 0; sg < nseg; ++sg) v += part[2 * (p * nseg + sg) + w];
-        epi_row<EPI>(o, a + i, v * o.scale);
+        for (int sg = 0; sg < nseg; ++sg) v += part[2 * (q * nseg + sg) + w];
+        epi_row<EPI>(o, a + 2 * full + i, v * o.scale);
       }
     }
   }
