@@ -327,7 +327,8 @@ def time_sampling(dec, wl, stream, firsts, greedy_ms):
     return {"value": D * B / (ms / 1000.0), "unit": UNIT, "controls": SAMPLING, "ms_per_step": ms / D,
             "added_ms_per_step": ms / D - greedy_ms,
             "api": "tqd_generate_sampled" if B == 1 else "tqd_generate_batch_sampled",
-            "note": "one sampling block per sequence after each step; steps launched one by one"}
+            "note": ("after each step, one block per 1024-entry vocabulary slice and sequence keeps the "
+                     "slice's top_k, then one block per sequence merges them and draws; steps launched one by one")}
 
 
 def time_kv16(args, wl, model, stream, hbm, kind):

@@ -294,3 +294,38 @@ def test_an_overflowing_temperature_is_the_greedy_limit(tqd):
         assert op_draw(tqd, l, hist, p, i) == want
     l = np.array([-3.0, -1.0, -2.0, -1.0, -5.0], dtype=np.float32)
     assert op_draw(tqd, l, [0], dict(temperature=1e-39), 1) == 1
+
+
+def test_two_pass_draw_edges(tqd):
+    """Draws with 1 <= top_k <= 64 take two passes (each 1024-token slice keeps
+    its own first top_k, one block merges them).  Planted lm_head rows put the
+    whole first top_k in one slice (the merge's threshold is then far below the
+    boundary) or make every logit equal (the order is the index order across
+    all slices; the penalised history tokens then move down the order);
+    top_k = 64 is the last two-pass value and 65 the first one-pass value.
+    The history avoids the planted rows (the lm_head is also the embedding), so
+    planting leaves the hidden state alone.  Vocabulary 20011: twenty slices,
+    the last one partial."""
+    cfg = dataclasses.replace(synth.TINY, vocab=20011)
+    base_model = synth.make_model(cfg, 21)
+    ids = np.array([11, 250, 19000, 11, 5, 250, 11], dtype=np.int32)
+    dec = tqd.Decoder(base_model, 16, 1)
+    dec.prefill(ids)
+    r = int(np.argmax(dec.logits()))
+    dec.close()
+    cases = [dict(temperature=1.0, top_k=40), dict(temperature=0.7, top_k=64, top_p=0.5),
+             dict(temperature=1.0, top_k=65), dict(temperature=1.2, top_k=40, repeat_penalty=1.3),
+             dict(temperature=0.9, top_k=20, min_p=0.3, presence_penalty=0.5), dict(temperature=1.0, top_k=1)]
+    for planted in (slice(7000, 7070), slice(0, cfg.vocab)):
+        lm = base_model.lm_head.copy()
+        lm[planted] = lm[r]
+        model = dataclasses.replace(base_model, lm_head=lm)
+        dec = tqd.Decoder(model, 16, 1)
+        dec.prefill(ids)
+        logits = dec.logits()
+        assert np.count_nonzero(logits == logits.max()) >= 70
+        for i, p in enumerate(cases):
+            for seed in range(5):
+                got = dec.sample(tqd.sampling(seed=seed, **p))
+                check_draw(got, logits, ids, len(ids), p, seed, f"rows {planted} case {i} seed {seed}")
+        dec.close()

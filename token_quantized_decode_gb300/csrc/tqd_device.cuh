@@ -297,6 +297,7 @@ struct DevSeq {
   uint32_t* scnt;         // [V] the sampler's input-token counts (zero between draws)
   float* xacc;            // [2][4][H] the persistent schedule's down-projection sums (two sets of four copies)
   uint64_t* qkv_tag;      // [qw + 2 kvw] the persistent schedule's projections as (tag << 32 | f32 bits) words
+  unsigned long long* sparts;  // the sampler's per-slice top_k keys [ceil(V / 1024)][64], or null
   int32_t tok_in;         // persistent schedule: the first step's input token when >= 0 (the kernel
                           // stores it at tokens[pos]); -1: the token is already at tokens[pos]
 };

@@ -463,7 +463,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
   const bool batched = batch_supported(shape) && (V + 127) / 128 <= kMaxArgmaxBlocks;
   const bool kv16 = cfg->kv_type == TQD_KV_F16;
   struct SeqOff { size_t state, tokens, kc, vc, x, xmid, qkv, attn, h, logits, po, pml, acnt, av, ai, acount, bar, gbar,
-                  opart, sz, scnt, xacc, qkvt; };
+                  opart, sz, scnt, xacc, qkvt, sparts; };
   std::vector<SeqOff> so(cfg->max_batch);
   const size_t kv_bytes = (kv16 ? 2 : 4) * static_cast<size_t>(L) * S * kvw;
   for (int b = 0; b < cfg->max_batch; ++b) {
@@ -490,6 +490,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     so[b].scnt = take(4 * align_up(static_cast<size_t>(V), 4));
     so[b].xacc = persist ? take(4ull * 2 * 4 * H) : 0;
     so[b].qkvt = persist ? take(8ull * (qw + 2 * kvw)) : 0;
+    so[b].sparts = take(8ull * kSamplePartK * ((static_cast<size_t>(V) + kSampleSlice - 1) / kSampleSlice));
   }
   const size_t o_dseqs = take(sizeof(DevSeq) * cfg->max_batch);  // the descriptors, for kernels over sequences
   // batched-step buffers (several sequences per step, or a prompt's tiles),
@@ -716,6 +717,7 @@ int32_t tqd_create(const tqd_config* cfg, const tqd_host_weights* w, void* strea
     d.scnt = reinterpret_cast<uint32_t*>(base + so[b].scnt);
     d.xacc = persist ? reinterpret_cast<float*>(base + so[b].xacc) : nullptr;
     d.qkv_tag = persist ? reinterpret_cast<uint64_t*>(base + so[b].qkvt) : nullptr;
+    d.sparts = reinterpret_cast<unsigned long long*>(base + so[b].sparts);
     d.tok_in = -1;
   }
   m->dseqs = reinterpret_cast<DevSeq*>(base + o_dseqs);
@@ -982,7 +984,7 @@ int32_t generate_impl(tqd_model* m, int32_t seq, int32_t first_token, int32_t n_
   } else {
     for (int i = 0; i < n_steps; ++i) {
       if ((rc = run_steps(m, s, 1, 0))) return rc;
-      CK(launch_sample(m->dseqs + seq, 1, m->cfg.vocab, m->cfg.max_seq, *sa, m->stream), "sampler launch");
+      CK(launch_sample(m->dseqs + seq, 1, m->cfg.vocab, m->cfg.max_seq, *sa, m->stream, true), "sampler launch");
     }
   }
   CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + pos + 1, 4ull * n_steps, cudaMemcpyDeviceToHost,
@@ -1034,7 +1036,7 @@ int32_t tqd_sample(tqd_model* m, int32_t seq, const tqd_sampling* sampling, int3
     return TQD_ERR_NOT_PREFILLED;
   }
   // (greedy too: an earlier draw may have replaced the step's argmax at this position)
-  CK(launch_sample(m->dseqs + seq, 1, m->cfg.vocab, m->cfg.max_seq, a, m->stream), "sampler launch");
+  CK(launch_sample(m->dseqs + seq, 1, m->cfg.vocab, m->cfg.max_seq, a, m->stream, true), "sampler launch");
   CK(cudaMemcpyAsync(m->h_tokens, s.d.tokens + s.next_pos, 4, cudaMemcpyDeviceToHost, m->stream), "read token");
   if ((rc = finish(m, s))) return rc;
   *token_out = m->h_tokens[0];
@@ -1210,7 +1212,7 @@ int32_t generate_batch_impl(tqd_model* m, int32_t n_seq, const int32_t* first_to
   } else {
     for (int i = 0; i < n_steps; ++i) {
       if ((rc = run_batch(m, n_seq, 1))) return rc;
-      CK(launch_sample(m->dseqs, n_seq, m->cfg.vocab, m->cfg.max_seq, *sa, m->stream), "sampler launch");
+      CK(launch_sample(m->dseqs, n_seq, m->cfg.vocab, m->cfg.max_seq, *sa, m->stream, true), "sampler launch");
     }
   }
   CK(cudaStreamSynchronize(m->stream), "synchronize");

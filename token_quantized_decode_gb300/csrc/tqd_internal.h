@@ -136,10 +136,19 @@ struct SampleArgs {
   float repeat, presence, frequency;
   int penalize;        // any penalty differs from neutral
   unsigned long long seed;
+  int parts;           // set by launch_sample: vocabulary slices whose top_k lists k_sample merges (0: none)
 };
+// Vocabulary entries per slice of the sampler's first pass, and the largest
+// top_k that pass serves (per sequence: DevSeq::sparts holds
+// ceil(V / kSampleSlice) * kSamplePartK keys).
+constexpr int kSampleSlice = 1024;
+constexpr int kSamplePartK = 64;
 // Groups of batch_max() sequences a batched step can run (tqd_config.max_batch <= 64).
 constexpr int kBatchGroups = 4;
-cudaError_t launch_sample(const DevSeq* seqs, int n, int V, int max_seq, const SampleArgs& a, cudaStream_t st);
+// slices: the sequences' DevSeq::sparts hold the per-slice lists (the
+// engine's sequences), so top_k <= kSamplePartK draws take the two-pass path.
+cudaError_t launch_sample(const DevSeq* seqs, int n, int V, int max_seq, const SampleArgs& a, cudaStream_t st,
+                          bool slices = false);
 // Validate the caller's sampling controls into a, and say whether they are greedy.
 int32_t sampling_args(const ::tqd_sampling* p, SampleArgs& a, bool* greedy);
 

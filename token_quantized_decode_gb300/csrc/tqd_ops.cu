@@ -128,7 +128,7 @@ int32_t tqd_op_argmax(const float* x, int64_t n, int32_t* idx_out, void* scratch
 size_t tqd_sample_scratch_bytes(int32_t vocab) {
   if (vocab <= 0) return 0;
   const size_t v4 = (static_cast<size_t>(vocab) + 3) / 4 * 4;
-  return 256 + 3 * 4 * v4;
+  return 384 + 3 * 4 * v4;
 }
 
 int32_t tqd_op_sample(const float* logits, int32_t vocab, int32_t* tokens, int32_t n_inputs,
@@ -146,15 +146,15 @@ int32_t tqd_op_sample(const float* logits, int32_t vocab, int32_t* tokens, int32
   const size_t v4 = (static_cast<size_t>(vocab) + 3) / 4 * 4;
   uint8_t* base = static_cast<uint8_t*>(scratch);
   DevSeq* dseq = reinterpret_cast<DevSeq*>(base);
-  DevState* dstate = reinterpret_cast<DevState*>(base + 192);
-  float* lg = reinterpret_cast<float*>(base + 256);
+  DevState* dstate = reinterpret_cast<DevState*>(base + 256);
+  float* lg = reinterpret_cast<float*>(base + 384);
   DevSeq h{};
   h.state = dstate;
   h.tokens = tokens;
   h.logits = lg;
   h.sz = lg + v4;
   h.scnt = reinterpret_cast<uint32_t*>(lg + 2 * v4);
-  static_assert(sizeof(DevSeq) <= 192, "descriptor fits the scratch header");
+  static_assert(sizeof(DevSeq) <= 256, "descriptor fits the scratch header");
   DevState st{static_cast<uint32_t>(n_inputs), 0u, 0u, 0u};
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // copies from pageable host memory are staged before cudaMemcpyAsync returns

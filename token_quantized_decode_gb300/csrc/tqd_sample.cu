@@ -558,6 +558,111 @@ __device__ int topk_list(const float* z, int V, int k, float hi, float lo_all, S
   return -1;
 }
 
+// top_p, min_p and the draw on the list sm.cand[0, n) sorted (penalised
+// logit descending, index ascending), n >= top_k: its first top_k entries are
+// the kept set of step 3.  Returns the drawn token (every thread).
+__device__ int list_draw(int n, const SampleArgs& a, const LWeight& wl, unsigned long long m24, SampleSm& sm) {
+  const float zmax = wl.zmax;
+  const int t = threadIdx.x;
+  const int K = a.top_k;
+  auto w_desc = [&](int i) { return wl(key_float(static_cast<uint32_t>(sm.cand[i] >> 32))); };
+  int nk = K;
+  if (a.top_p < 1.f) {
+    unsigned long long wk = 0;
+    for (int i = t; i < K; i += kSThreads) wk += w_desc(i);
+    wk = block_sum(wk, sm);
+    unsigned long long need =
+        static_cast<unsigned long long>(ceil(static_cast<double>(a.top_p) * static_cast<double>(wk)));
+    need = need < 1ull ? 1ull : (need > wk ? wk : need);
+    nk = list_first_ge(K, w_desc, need, sm) + 1;
+  }
+  // min_p, then the kept tokens in index order: (index << 32) | key
+  int P = 1;
+  while (P < n) P <<= 1;
+  unsigned long long kept = 0;
+  for (int i = t; i < P; i += kSThreads) {
+    const unsigned long long c = sm.cand[i];
+    bool keep = false;
+    if (i < nk) {
+      const float lv = key_float(static_cast<uint32_t>(c >> 32));
+      keep = __fsub_rn(__fdiv_rn(lv, a.temperature), zmax) >= a.ln_min_p;
+    }
+    const unsigned long long v = 0xFFFFFFFFull - (c & 0xFFFFFFFFull);
+    sm.cand[i] = keep ? ((v << 32) | (c >> 32)) : ~0ull;
+    kept += keep ? 1ull : 0ull;
+  }
+  const int nkept = static_cast<int>(block_sum(kept, sm));
+  sort_cand(P, false, sm);
+  auto w_idx = [&](int i) { return wl(key_float(static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull))); };
+  unsigned long long W = 0;
+  for (int i = t; i < nkept; i += kSThreads) W += w_idx(i);
+  W = block_sum(W, sm);
+  const unsigned long long target = (W >> 24) * m24 + (((W & 0xFFFFFFull) * m24) >> 24);  // floor(u W)
+  const int i = list_first_ge(nkept, w_idx, target + 1ull, sm);
+  return static_cast<int32_t>(sm.cand[i] >> 32);
+}
+
+// The first pass of a top_k <= kSamplePartK draw: block (x, y) takes the
+// vocabulary slice [x kSampleSlice, (x + 1) kSampleSlice) of sequence y,
+// counts the history tokens that fall in it, applies the penalties exactly as
+// k_sample does (step 1), and writes the slice's first top_k entries in the
+// order of step 2 as keys (order key of l << 32 | 2^32 - 1 - index) to
+// DevSeq::sparts.  Every token of the global first top_k is among its
+// slice's first top_k, so the merge needs nothing else.
+constexpr int kPThreads = 256;
+__global__ void __launch_bounds__(kPThreads) k_sample_part(const DevSeq* seqs, int V, int max_seq, SampleArgs a) {
+  __shared__ unsigned long long key[kSampleSlice];
+  __shared__ unsigned int cnt[kSampleSlice];
+  const DevSeq& s = seqs[blockIdx.y];
+  const int t = threadIdx.x;
+  const uint32_t S = s.state->pos;
+  if (S == 0u || S > static_cast<uint32_t>(max_seq)) return;
+  const int v0 = static_cast<int>(blockIdx.x) * kSampleSlice;
+  if (a.penalize) {
+    for (int i = t; i < kSampleSlice; i += kPThreads) cnt[i] = 0u;
+    __syncthreads();
+    for (int i = t; i < static_cast<int>(S); i += kPThreads) {
+      const int x = s.tokens[i] - v0;
+      if (x >= 0 && x < kSampleSlice) atomicAdd(&cnt[x], 1u);
+    }
+    __syncthreads();
+  }
+  for (int i = t; i < kSampleSlice; i += kPThreads) {
+    const int v = v0 + i;
+    unsigned long long k = 0ull;  // below every token's key: the slice's padding
+    if (v < V) {
+      float l = s.logits[v];
+      if (isnan(l)) l = -INFINITY;
+      const unsigned c = a.penalize ? cnt[i] : 0u;
+      if (c && l > -INFINITY) {
+        l = l > 0.f ? __fdiv_rn(l, a.repeat) : __fmul_rn(l, a.repeat);
+        l = __fsub_rn(l, a.presence);
+        l = __fsub_rn(l, __fmul_rn(a.frequency, static_cast<float>(c)));
+        if (isnan(l)) l = -INFINITY;
+      }
+      k = (static_cast<unsigned long long>(order_key(l)) << 32) | (0xFFFFFFFFull - static_cast<unsigned>(v));
+    }
+    key[i] = k;
+  }
+  __syncthreads();
+  for (int k2 = 2; k2 <= kSampleSlice; k2 <<= 1)  // bitonic sort, descending
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      for (int i = t; i < kSampleSlice; i += kPThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x = key[i], y = key[ixj];
+          if (((i & k2) == 0) ? (x < y) : (x > y)) {
+            key[i] = y;
+            key[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  unsigned long long* out = s.sparts + static_cast<size_t>(blockIdx.x) * kSamplePartK;
+  for (int i = t; i < a.top_k; i += kPThreads) out[i] = key[i];
+}
+
 __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int V, int max_seq, SampleArgs a) {
   __shared__ SampleSm sm;
   const DevSeq& s = seqs[blockIdx.x];
@@ -608,6 +713,65 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
       tok[S] = bi;
     }
     return;
+  }
+  if (a.parts > 0) {
+    // the slices' first top_k entries hold the global first top_k.  tau, the
+    // top_k-th largest of the slices' first m keys (a subset of those
+    // entries), is at most the global top_k-th key, so the keys at or above
+    // tau hold the first top_k; with m large enough for the subset to hold
+    // top_k keys, few more than top_k survive unless one slice holds most of
+    // them
+    const int K = a.top_k, np = a.parts;
+    const unsigned long long* sp = s.sparts;
+    int m = (2 * K + np - 1) / np;
+    m = m < 4 ? 4 : m;
+    m = m > K ? K : m;
+    if (np * m > kSCand) m = kSCand / np;
+    const int ns = np * m;
+    int Ps = 1;
+    while (Ps < ns) Ps <<= 1;
+    for (int i = t; i < Ps; i += kSThreads) {
+      unsigned long long k = 0ull;
+      if (i < ns) {
+        const int b = i / m, j = i - b * m;
+        k = __ldcg(sp + static_cast<size_t>(b) * kSamplePartK + j);
+      }
+      sm.cand[i] = k;
+    }
+    if (t == 0) sm.ncand = 0u;
+    __syncthreads();
+    sort_cand(Ps, true, sm);
+    const unsigned long long tau = ns >= K ? sm.cand[K - 1] : 0ull;
+    __syncthreads();
+    for (int i = t; i < np * K; i += kSThreads) {
+      const int b = i / K, j = i - b * K;
+      const unsigned long long k = __ldcg(sp + static_cast<size_t>(b) * kSamplePartK + j);
+      if (k >= tau) {
+        const unsigned slot = atomicAdd(&sm.ncand, 1u);
+        if (slot < static_cast<unsigned>(kSCand)) sm.cand[slot] = k;
+      }
+    }
+    __syncthreads();
+    const unsigned nc = sm.ncand;
+    if (nc <= static_cast<unsigned>(kSCand)) {
+      const int n = static_cast<int>(nc);
+      int P = 1;
+      while (P < n) P <<= 1;
+      for (int i = n + t; i < P; i += kSThreads) sm.cand[i] = 0ull;
+      __syncthreads();
+      sort_cand(P, true, sm);
+      const float lmax = key_float(static_cast<uint32_t>(sm.cand[0] >> 32));
+      const float zmax = __fdiv_rn(lmax, a.temperature);
+      // every logit NaN, or l_max / T overflowing: the one-pass path below decides
+      if (n >= K && lmax > -INFINITY && zmax > -INFINITY && zmax < INFINITY) {
+        const LWeight wl{a.temperature, zmax};
+        const unsigned long long m24 = mix64(a.seed + (static_cast<unsigned long long>(S) + 1ull) * kGolden) >> 40;
+        const int v = list_draw(n, a, wl, m24, sm);
+        if (t == 0) tok[S] = v;
+        return;
+      }
+    }
+    __syncthreads();
   }
   if (a.penalize)
     for (int i = t; i < n_in; i += kSThreads) {
@@ -678,42 +842,8 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
     // the kept tokens fit shared memory: top_p, min_p and the draw on that list
     const int n = topk_list(z, V, a.top_k, lmax, lmin, sm);
     if (n >= 0) {
-      const int K = a.top_k;
-      auto w_desc = [&](int i) { return wl(key_float(static_cast<uint32_t>(sm.cand[i] >> 32))); };
-      int nk = K;
-      if (a.top_p < 1.f) {
-        unsigned long long wk = 0;
-        for (int i = t; i < K; i += kSThreads) wk += w_desc(i);
-        wk = block_sum(wk, sm);
-        unsigned long long need =
-            static_cast<unsigned long long>(ceil(static_cast<double>(a.top_p) * static_cast<double>(wk)));
-        need = need < 1ull ? 1ull : (need > wk ? wk : need);
-        nk = list_first_ge(K, w_desc, need, sm) + 1;
-      }
-      // min_p, then the kept tokens in index order: (index << 32) | key
-      int P = 1;
-      while (P < n) P <<= 1;
-      unsigned long long kept = 0;
-      for (int i = t; i < P; i += kSThreads) {
-        const unsigned long long c = sm.cand[i];
-        bool keep = false;
-        if (i < nk) {
-          const float lv = key_float(static_cast<uint32_t>(c >> 32));
-          keep = __fsub_rn(__fdiv_rn(lv, a.temperature), zmax) >= a.ln_min_p;
-        }
-        const unsigned long long v = 0xFFFFFFFFull - (c & 0xFFFFFFFFull);
-        sm.cand[i] = keep ? ((v << 32) | (c >> 32)) : ~0ull;
-        kept += keep ? 1ull : 0ull;
-      }
-      const int nkept = static_cast<int>(block_sum(kept, sm));
-      sort_cand(P, false, sm);
-      auto w_idx = [&](int i) { return wl(key_float(static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull))); };
-      unsigned long long W = 0;
-      for (int i = t; i < nkept; i += kSThreads) W += w_idx(i);
-      W = block_sum(W, sm);
-      const unsigned long long target = (W >> 24) * m24 + (((W & 0xFFFFFFull) * m24) >> 24);  // floor(u W)
-      const int i = list_first_ge(nkept, w_idx, target + 1ull, sm);
-      if (t == 0) tok[S] = static_cast<int32_t>(sm.cand[i] >> 32);
+      const int v = list_draw(n, a, wl, m24, sm);
+      if (t == 0) tok[S] = v;
       return;
     }
   }
@@ -753,8 +883,17 @@ __global__ void __launch_bounds__(kSThreads, 1) k_sample(const DevSeq* seqs, int
 
 }  // namespace
 
-cudaError_t launch_sample(const DevSeq* seqs, int n, int V, int max_seq, const SampleArgs& a, cudaStream_t st) {
-  k_sample<<<n, kSThreads, 0, st>>>(seqs, V, max_seq, a);
+cudaError_t launch_sample(const DevSeq* seqs, int n, int V, int max_seq, const SampleArgs& a, cudaStream_t st,
+                          bool slices) {
+  SampleArgs b = a;
+  b.parts = 0;
+  if (slices && a.temperature > 0.f && a.top_k >= 1 && a.top_k <= kSamplePartK && a.top_k < V) {
+    b.parts = (V + kSampleSlice - 1) / kSampleSlice;
+    k_sample_part<<<dim3(b.parts, n), kPThreads, 0, st>>>(seqs, V, max_seq, b);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  k_sample<<<n, kSThreads, 0, st>>>(seqs, V, max_seq, b);
   return cudaGetLastError();
 }
 
