@@ -288,13 +288,17 @@ typedef struct tqd_sampling {
 int32_t tqd_sample(tqd_model* model, int32_t seq, const tqd_sampling* sampling, int32_t* token_out);
 
 /* As tqd_generate, with every step's token drawn under `sampling` instead of
- * the argmax, on the device (one sampling block after each step; no host
- * round trip between steps). */
+ * the argmax, on the device (the draw runs after each step; no host round
+ * trip between steps).  With 1 <= top_k <= 64 the draw takes two passes: one
+ * block per 1024-token vocabulary slice keeps the slice's first top_k, one
+ * block merges them; otherwise one block per sequence draws from the whole
+ * vocabulary.  Both give the same token. */
 int32_t tqd_generate_sampled(tqd_model* model, int32_t seq, int32_t first_token, int32_t n_steps,
                              const tqd_sampling* sampling, int32_t* ids_out);
 
 /* As tqd_generate_batch, with every sequence's token drawn under `sampling`
- * (one sampling block per sequence after each batched step). */
+ * (the draw of every sequence after each batched step, as in
+ * tqd_generate_sampled). */
 int32_t tqd_generate_batch_sampled(tqd_model* model, int32_t n_seq, const int32_t* first_tokens,
                                    int32_t n_steps, const tqd_sampling* sampling, int32_t* ids_out);
 
