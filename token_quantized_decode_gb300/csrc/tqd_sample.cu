@@ -2,7 +2,11 @@
 // the sampled arm of the batched prefill+decode section: temperature, top_k,
 // top_p, min_p, repeat / presence / frequency penalties and a seed;
 // temperature <= 0 falls back to the greedy token and top_k = 1 reproduces
-// it).  One block per sequence, in this order:
+// it).  With 1 <= top_k <= kSamplePartK the draw takes two passes
+// (k_sample_part keeps each vocabulary slice's first top_k under the
+// penalties, k_sample merges them and runs the list path below); otherwise,
+// and where the merge cannot decide, one block per sequence does everything,
+// in this order:
 //   1. penalties on the distinct tokens among the sequence's inputs (counted
 //      in a per-sequence array the block leaves zeroed), each an f32
 //      operation: a = l > 0 ? l / r : l * r; a -= presence; a -= frequency * c;
