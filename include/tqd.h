@@ -127,8 +127,8 @@ typedef struct tqd_host_weights {
 typedef struct tqd_model tqd_model;
 
 /* Create a model whose weights are the seeded synthetic ones the tests and
- * the benchmark use (north star: "load synthetic model"; "Metal LLM decode",
- * section "Functions": one call stands up the session): every matrix
+ * the benchmark use, in one call ("Metal LLM decode", section "Functions":
+ * one call stands up the session): every matrix
  * N(0, 0.02), quantized to Q8_0 (scale = max|w| / 127 as f16, quants
  * rint(w / scale) clamped to +-127) or rounded to bf16, every norm gain
  * 1 + N(0, 0.1) in f32, the lm_head tied to the embedding.  Draws come from
