@@ -129,3 +129,31 @@ def test_binding_structs_match_the_header_layout(name, cls):
     size, offsets = _c_layout(name, fields)
     assert ctypes.sizeof(cls) == size, name
     assert [getattr(cls, f).offset for f in fields] == offsets, name
+
+
+def _build_client(d):
+    """tests/c/tqd_client.c compiled against include/tqd.h and linked to the
+    in-tree libtqd.so (rpath to its directory)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    lib = _lib.LIB_PATH
+    if not os.path.exists(lib):
+        pytest.skip("libtqd is not built")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c", "tqd_client.c")
+    exe = os.path.join(d, "tqd_client")
+    libdir = os.path.dirname(lib)
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), src, "-o", exe,
+                    "-L", libdir, "-ltqd", f"-Wl,-rpath,{libdir}"], check=True, capture_output=True)
+    return exe
+
+
+def test_c_client_compiles_and_links_against_the_library():
+    """A C program that uses only include/tqd.h and libtqd.so builds (its run
+    is a GPU test: tests/test_gpu_synthetic.py)."""
+    import tempfile
+    with tempfile.TemporaryDirectory() as d:
+        exe = _build_client(d)
+        assert os.path.exists(exe)

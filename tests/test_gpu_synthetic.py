@@ -70,3 +70,39 @@ def test_export_of_an_uploaded_model_round_trips(tqd):
     dec = tqd.Decoder(model, 8, 2)
     assert_same_weights(dec.export_weights(), model)
     dec.close()
+
+
+@pytest.mark.parametrize("schedule", ["persistent", "graph"])
+def test_c_client_generates_the_oracle_tokens(tqd, schedule):
+    """tests/c/tqd_client.c, a C program using the C ABI alone
+    (tqd_create_synthetic, tqd_prefill, tqd_generate), prints the oracle's
+    greedy tokens for the seeded tiny model.  A token may differ only where
+    the oracle's two candidates lie within the decode tests' top-2 gap (then the
+    sequences part and the comparison stops)."""
+    import subprocess
+    import tempfile
+    from tests.test_abi import _build_client
+    from tests.test_gpu_decode import TOP2_GAP
+    cfg, seed, steps = synth.TINY, 5, 8
+    ids = synth.token_ids(1000, 3, 12, cfg.vocab)
+    sched = tqd.TQD_SCHED_PERSISTENT if schedule == "persistent" else tqd.TQD_SCHED_GRAPH
+    shape = (cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.intermediate, cfg.vocab,
+             int(cfg.qk_norm), 0 if cfg.weight_type == "q8_0" else 1)
+    with tempfile.TemporaryDirectory() as d:
+        exe = _build_client(d)
+        args = [exe, str(seed), str(steps), str(sched), *map(str, shape), repr(cfg.rope_theta), repr(cfg.rms_eps),
+                *(str(int(t)) for t in ids)]
+        r = subprocess.run(args, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    got = [int(x) for x in r.stdout.split()]
+    assert len(got) == steps + 1
+    om = oracle.OracleModel(synth.make_model(cfg, seed), len(ids) + steps + 1)
+    tok, lg = om.prefill(ids)
+    p = len(ids)
+    for i in range(steps + 1):
+        if got[i] != tok:
+            assert lg[tok] - lg[got[i]] <= TOP2_GAP, (i, got[i], tok)
+            break
+        if i < steps:
+            tok, lg = om.step(tok, p)
+            p += 1
