@@ -244,6 +244,14 @@ __device__ __forceinline__ int rows_per_piece(size_t rb) {
   return r & ~1;
 }
 
+// Rows per ring piece taking every row a slot holds (even, at most 2 kCW
+// pairs' worth: two pairs per warp at most).
+__device__ __forceinline__ int rows_per_piece_all(size_t rb) {
+  int r = static_cast<int>(kSlotBytes / static_cast<uint32_t>(rb));
+  if (r > 4 * kCW) r = 4 * kCW;
+  return r & ~1;
+}
+
 // K/V rows per attention piece (K rows then V rows in one slot).
 __device__ __forceinline__ int kv_rows_per_piece(int hd, int esz) {
   return static_cast<int>(kSlotBytes / (2u * esz * hd));
@@ -338,8 +346,7 @@ struct Producer {
     if (use > 0 && !mwait(r.empty + slot, (use - 1) & 1u, err)) ok = false;
     return ok;
   }
-  __device__ void rows(const uint8_t* W, size_t rb, int r0, int r1) {
-    const int rpp = rows_per_piece(rb);
+  __device__ void rows(const uint8_t* W, size_t rb, int r0, int r1, int rpp) {
     for (int a = r0; a < r1 && ok; a += rpp) {
       const int n = min(rpp, r1 - a);
       if (!acquire()) return;
@@ -420,7 +427,7 @@ __device__ void run_producer(const DevModel& m, const DevSeq& s, int n_steps, in
     if (pos >= m.max_seq) break;
     for (int l = 0; l < m.n_layers && P.ok; ++l) {
       const DevLayer& L = m.layers[l];
-      for (int i = 0; i < 3; ++i) P.rows(L.wqkv, m.row_bytes_h, pl.qr0[i], pl.qr1[i]);
+      for (int i = 0; i < 3; ++i) P.rows(L.wqkv, m.row_bytes_h, pl.qr0[i], pl.qr1[i], rows_per_piece(m.row_bytes_h));
       if (pl.chunk >= 0) {
         int t0, t1;
         chunk_range(pos + 1, m.n_chunks, pl.chunk, t0, t1);
@@ -430,11 +437,12 @@ __device__ void run_producer(const DevModel& m, const DevSeq& s, int n_steps, in
              reinterpret_cast<const uint8_t*>(s.vcache) + head * esz, m.hd, esz, t0, min(t1, pos));
       }
       if (pl.grp >= 0)
-        P.rows(L.wo_g + static_cast<size_t>(pl.grp) * m.H * m.row_bytes_gh, m.row_bytes_gh, pl.o0, pl.o1);
-      P.rows(L.wgu, m.row_bytes_h, pl.g0, pl.g1);
+        P.rows(L.wo_g + static_cast<size_t>(pl.grp) * m.H * m.row_bytes_gh, m.row_bytes_gh, pl.o0, pl.o1,
+               rows_per_piece(m.row_bytes_gh));
+      P.rows(L.wgu, m.row_bytes_h, pl.g0, pl.g1, rows_per_piece_all(m.row_bytes_h));
       P.dcols(L.wd_c, m, pl.g0 / 2, pl.g1 / 2);
     }
-    if (step >= full_from) P.rows(m.lm_head, m.row_bytes_h, pl.v0, pl.v1);
+    if (step >= full_from) P.rows(m.lm_head, m.row_bytes_h, pl.v0, pl.v1, rows_per_piece(m.row_bytes_h));
   }
   if (!P.ok) P.drain();
 }
@@ -649,6 +657,37 @@ __device__ __forceinline__ void dot_rows(const float* xin, const uint8_t* wa, co
   acc_b += b2;
 }
 
+// dot_rows for two row pairs at once (rows w[0..3]), every chunk round's x
+// loaded once for the four rows.
+template <int FMT>
+__device__ __forceinline__ void dot_rows4(const float* xin, const uint8_t* const (&w)[4], int K, int nchunks,
+                                          int iters, float (&acc)[4]) {
+  constexpr int XS = FMT == kFmtQ8 ? 20 : 12;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) acc[r] = 0.f;
+#pragma unroll 1
+  for (int i = 0; i < iters; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nchunks) {
+      const float4* xp = reinterpret_cast<const float4*>(xin + XS * c);
+      uint4 wv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) wv[r] = *reinterpret_cast<const uint4*>(w[r] + 16 * c);
+      if (FMT == kFmtQ8) {
+        float sc[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sc[r] = __half2float(*reinterpret_cast<const __half*>(w[r] + K + 2 * (c >> 1)));
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] = fmaf(sc[r], dot16_q8(wv[r], xp), acc[r]);
+      } else {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] += dot8_bf16(wv[r], xp);
+      }
+    }
+  }
+}
+
 // One phase of matvec rows [r0, r1) streamed through the ring, with epilogue
 // EPI.  The row pairs of a piece go whole to the warps, kCW at a time (each
 // warp applies the epilogue of its own pairs); the pairs left over are split
@@ -656,8 +695,11 @@ __device__ __forceinline__ void dot_rows(const float* xin, const uint8_t* wa, co
 // and one thread per row applies their epilogue after a consumer sync.  SHORT (rows of at most 16 chunks, K known at compile time at
 // the call site) gives each half-warp its own row pair; the general path
 // handles any K, short rows included.  One instance holds one path and one
-// epilogue only, which keeps the per-layer code small.
-template <int FMT, int EPI, bool SHORT>
+// epilogue only, which keeps the per-layer code small.  WHOLE (pieces of at
+// most 2 kCW pairs) takes every pair whole: a warp with two pairs computes
+// both in one pass over K (four independent dot chains sharing the x loads),
+// so the piece needs no K split and no consumer sync.
+template <int FMT, int EPI, bool SHORT, bool WHOLE = false>
 __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvOut& o) {
   constexpr int EPC = FMT == kFmtQ8 ? 16 : 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -670,7 +712,7 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
     int full = pairs / kCW * kCW, rem = pairs - full;
     int nseg = rem > 0 ? small_div(kCW, rem) : 1;
     if (nseg > iters) nseg = iters;
-    if (nseg <= 1) {
+    if (WHOLE || nseg <= 1) {
       nseg = 1;
       full = pairs;
       rem = 0;
@@ -730,6 +772,35 @@ __device__ void mv_phase(Cons& C, size_t rb, int rpp, int K, int r0, int r1, MvO
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(C.r.empty + C.r.n % kSlots)) : "memory");
       ++C.r.n;
       continue;
+    }
+    if constexpr (WHOLE) {
+      // at most two pairs per warp (pairs <= 2 kCW): pair warp and warp + kCW together
+      const int pA = warp, pB = warp + kCW;
+      if (pB < full) {
+        const uint8_t* w[4];
+        const int rows[4] = {2 * pA, 2 * pA + 1, 2 * pB, 2 * pB + 1};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) w[r] = slot + static_cast<size_t>(rows[r] < n ? rows[r] : rows[r] - 1) * rb;
+        float acc[4];
+        dot_rows4<FMT>(C.xin, w, K, nchunks, iters, acc);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] = warp_sum(acc[r]) * o.scale;
+        if (lane == 0) {
+          if constexpr (EPI == kEpiSwiGLU) {
+            o.y[(a + rows[0]) >> 1] = silu_mul_fast(acc[0], acc[1]);
+            o.y[(a + rows[2]) >> 1] = silu_mul_fast(acc[2], acc[3]);
+          } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+              if (rows[r] < n) epi_row<EPI>(o, a + rows[r], acc[r]);
+          }
+        }
+        full = 0;  // this warp's pairs are done
+      } else if (pA >= full) {
+        full = 0;
+      } else {
+        full = pA + 1;  // one pair: the loop below takes pair pA only
+      }
     }
     for (int p = warp; p < full; p += kCW) {  // whole pairs: the warp applies the epilogue
       const int ra = 2 * p, rbw = 2 * p + 1;
@@ -1265,6 +1336,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
   // grid barrier that starts FFN phase k + 1.  Set 0 is cleared here.
   const int H = m.H;
   const int rpp_h = rows_per_piece(m.row_bytes_h), rpp_gh = rows_per_piece(m.row_bytes_gh);  // rows per ring piece
+  const int rpp_gu = rows_per_piece_all(m.row_bytes_h);
   int kph = 0;
   zero_share(s.xacc, pl.zx0, pl.zx1);
   zero_share(s.opart, pl.zo0, pl.zo1);
@@ -1345,7 +1417,7 @@ __device__ void run_consumers(Cons& C, int n_steps, int full_from, uint32_t pos0
       zero_share(s.opart + static_cast<size_t>((kph + 1) & 1) * m.H, pl.zo0, pl.zo1);
       const int j0 = pl.g0 / 2, j1 = pl.g1 / 2;
       o.y = C.scr - j0;  // h[j] of this block's rows, in shared memory at scr[j - j0]
-      mv_phase<FMT, kEpiSwiGLU, false>(C, m.row_bytes_h, rpp_h, H, pl.g0, pl.g1, o);
+      mv_phase<FMT, kEpiSwiGLU, false, true>(C, m.row_bytes_h, rpp_gu, H, pl.g0, pl.g1, o);
       csync();
       down_cols<FMT>(C, j0, j1, C.scr, s.xacc + (kph & 1) * kAccCopies * H + (b % kAccCopies) * H);
       zero_share(s.xacc + ((kph + 1) & 1) * kAccCopies * H, pl.zx0, pl.zx1);
